@@ -1,0 +1,180 @@
+/*
+ * mla_verify.h - speculative-decoding verify attention for Multi-head Latent
+ * Attention (MLA) over a paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  "The Decisive A/B: When Benchmarking Honesty Reveals the
+ * Real Bottleneck" (section "The Context") describes the verify step: the
+ * drafter's speculative tokens attend to the target model's cached MLA
+ * latent KV, stored with page_size=1 (one slot per token, rows scattered
+ * through the cache), computed by a KV-split "partial" kernel plus a
+ * "reduce" kernel, with a fixed split count, pre-allocated workspace and no
+ * host synchronisation so the call can be captured in a CUDA graph.  "The
+ * Moment of Truth: Benchmarking a Custom sm_120 Verify Kernel Against
+ * Triton" (sections "The Raw Numbers" and "The CUDA Graph Dilemma") names
+ * the tree ("kdtree") verify and the static-buffer requirement.
+ *
+ * For request b with n_b = kv_lens[b] cached rows (the last T rows are the
+ * drafts' own rows, P_b = n_b - T is the prefix), draft t, head h:
+ *
+ *     s_j  = scale * dot(q[b,t,h,0:576], k_j[0:576])
+ *     key j is visible iff j < P_b, or j - P_b is t or an ancestor of t
+ *     lse  = log(sum over visible j of exp(s_j))              (natural log)
+ *     out  = sum over visible j of exp(s_j - lse) * k_j[0:512]
+ *
+ * k_j is the cache row of logical key j: slot kv_indices[kv_indptr[b] + j]
+ * when page_size == 1, or row j % 64 of page kv_indices[kv_indptr[b] + j/64]
+ * when page_size == 64.  Values are the first 512 (latent) dims of each row;
+ * the last 64 (rope) dims enter the scores only.
+ *
+ * Layouts (all row-major, contiguous):
+ *     q            bf16  [B, T, H, 576]          (query row r = t*H + h)
+ *     kv_cache     bf16  [num_slots, 576]        (1152-byte rows)
+ *     kv_indices   int32 [kv_indptr[B]]          slot ids (ps 1) or page ids (ps 64)
+ *     kv_indptr    int32 [B + 1]                 non-decreasing, kv_indptr[0] >= 0
+ *     kv_lens      int32 [B]                     n_b = P_b + T, T <= n_b <= max_kv_len
+ *     draft_parent int32 [B, T]                  -1 (hangs off the prefix) or an earlier draft
+ *     out          fp32 or bf16 [B, T, H, 512]   (plan's out_dtype)
+ *     lse          fp32  [B, T, H]
+ * Every device pointer must be 16-byte aligned.
+ *
+ * Numerics: both products run on the tensor cores in fp16 with fp32
+ * accumulation; the bf16 inputs are widened to fp16 in shared memory, which
+ * is exact for |x| in [2^-14, 65504] (smaller magnitudes keep an absolute
+ * error below 2^-25; values beyond the fp16 range are not supported).  The
+ * softmax runs in fp32.
+ *
+ * Ownership: the caller owns every tensor.  The plan owns its workspace
+ * (split partials), a device error word and, for mla_verify_attn_host, its
+ * device staging buffers; all are allocated by mla_verify_plan_create and
+ * freed by mla_verify_plan_destroy.
+ *
+ * Errors: functions return MLA_VERIFY_OK (0) or a negative status for
+ * problems visible on the host (null or misaligned pointer, sizes beyond the
+ * plan, unsupported shape, CUDA launch failure).  Problems only visible in
+ * device data (slot or page id out of range, a kv_len outside [T,
+ * max_kv_len], indptr inconsistent with kv_lens, a parent that is not an
+ * earlier draft) never fault: the kernels set a sticky bit in the plan's
+ * device error word, mask the offending key (bad slot), treat the parent as
+ * -1 (bad parent) or write NaN for the whole request (bad length/indptr),
+ * and carry on.  Read and clear the word with mla_verify_get_error.
+ */
+#ifndef MLA_VERIFY_H_
+#define MLA_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define MLA_VERIFY_OK                 0
+#define MLA_VERIFY_ERR_NULL          -1   /* a required pointer is NULL            */
+#define MLA_VERIFY_ERR_ALIGN         -2   /* a pointer is not 16-byte aligned      */
+#define MLA_VERIFY_ERR_SHAPE         -3   /* unsupported T/H/page_size/dtype/sizes */
+#define MLA_VERIFY_ERR_BATCH         -4   /* batch < 1 or > plan's max_batch       */
+#define MLA_VERIFY_ERR_SCALE         -5   /* scale not finite                      */
+#define MLA_VERIFY_ERR_CUDA          -6   /* a CUDA runtime call or launch failed  */
+#define MLA_VERIFY_ERR_DEVICE        -7   /* current device is not the plan's      */
+#define MLA_VERIFY_ERR_OOM           -8   /* device or pinned allocation failed    */
+#define MLA_VERIFY_ERR_ARG           -9   /* other invalid argument                */
+
+/* Bits of the device error word (mla_verify_get_error). */
+#define MLA_VERIFY_DEV_BAD_SLOT       1   /* slot or page id outside the cache     */
+#define MLA_VERIFY_DEV_BAD_LEN        2   /* kv_len < T or > max_kv_len            */
+#define MLA_VERIFY_DEV_BAD_PARENT     4   /* draft_parent[i] not in {-1} U [0, i)  */
+#define MLA_VERIFY_DEV_BAD_INDPTR     8   /* indptr range does not match kv_len    */
+#define MLA_VERIFY_DEV_TIMEOUT       16   /* a bounded device wait gave up         */
+
+/* Output element type. */
+#define MLA_VERIFY_OUT_F32            0
+#define MLA_VERIFY_OUT_BF16           1
+
+/* Kernel family for the partial (split-KV) step. */
+#define MLA_VERIFY_KERNEL_AUTO        0
+#define MLA_VERIFY_KERNEL_MMA         1   /* warp-level mma.sync, O in registers   */
+
+typedef struct mla_verify_plan mla_verify_plan;
+
+/*
+ * Create a plan for calls with batch <= max_batch on CUDA device `device`.
+ * num_drafts (T) in [1, 32]; num_heads (H) >= 1 with T*H <= 4096;
+ * page_size 1 or 64; num_slots >= 1 (a multiple of 64 when page_size is 64);
+ * 1 <= max_kv_len; out_dtype MLA_VERIFY_OUT_F32 or _BF16.
+ * Allocates all device memory the plan will ever use (cudaMalloc) and sets
+ * kernel attributes; makes `device` current on the calling thread.
+ * On success *plan receives the handle.  Not to be called during capture.
+ */
+int mla_verify_plan_create(mla_verify_plan** plan, int max_batch, int num_drafts,
+                           int num_heads, int page_size, int64_t num_slots,
+                           int max_kv_len, int out_dtype, int device);
+
+/* Release everything the plan owns (synchronises the plan's device). */
+void mla_verify_plan_destroy(mla_verify_plan* plan);
+
+/*
+ * Fix the split count used by later calls (1..MLA_VERIFY_MAX_NSPLIT), or 0
+ * to choose it from the batch, the plan's max_kv_len and the SM count.
+ * The workspace was sized for the largest count; larger values are refused.
+ */
+#define MLA_VERIFY_MAX_NSPLIT 32
+int mla_verify_plan_set_nsplit(mla_verify_plan* plan, int nsplit);
+
+/* The split count a call with `batch` requests will use (>= 1), or < 0. */
+int mla_verify_plan_get_nsplit(const mla_verify_plan* plan, int batch);
+
+/* Select the partial-kernel family (MLA_VERIFY_KERNEL_*). */
+int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
+
+/* Bytes of device workspace the plan holds (partials + error word). */
+size_t mla_verify_plan_workspace_bytes(const mla_verify_plan* plan);
+
+/*
+ * The verify attention, all pointers on the plan's device (layouts above).
+ * Enqueues its kernels on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and returns: no allocation, no synchronisation, no device-memory
+ * read on the host, and the launch grid depends only on `batch` and the plan,
+ * so the call may be captured into a CUDA graph and replayed with new data
+ * in the same buffers.  Calls sharing one plan must not overlap on the GPU
+ * (they share the workspace); use one plan per concurrent stream.
+ */
+int mla_verify_attn(mla_verify_plan* plan, int batch, const void* q,
+                    const void* kv_cache, const int32_t* kv_indices,
+                    const int32_t* kv_indptr, const int32_t* kv_lens,
+                    const int32_t* draft_parent, float scale, void* out,
+                    float* lse, void* stream);
+
+/*
+ * The same operation with q, kv_indices, kv_indptr, kv_lens, draft_parent,
+ * out and lse in HOST memory (pinned memory gives the fastest copies) and
+ * kv_cache on the device (the cache is resident model state).  Copies the
+ * inputs into the plan's device staging buffers on `stream`, runs
+ * mla_verify_attn, copies out/lse back and synchronises `stream` before
+ * returning.  kv_indptr[batch] entries of kv_indices are copied; that count
+ * must not exceed max_batch * max_kv_len.  Not capturable.
+ */
+int mla_verify_attn_host(mla_verify_plan* plan, int batch, const void* q_host,
+                         const void* kv_cache, const int32_t* kv_indices_host,
+                         const int32_t* kv_indptr_host, const int32_t* kv_lens_host,
+                         const int32_t* draft_parent_host, float scale,
+                         void* out_host, float* lse_host, void* stream);
+
+/*
+ * Read the sticky device error word (MLA_VERIFY_DEV_* bits) into
+ * *device_status; clear it when `clear` is nonzero.  Synchronises the
+ * plan's device: call outside graph capture.
+ */
+int mla_verify_get_error(mla_verify_plan* plan, int* device_status, int clear);
+
+/* Static text for a status code. */
+const char* mla_verify_strerror(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int mla_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_VERIFY_H_ */

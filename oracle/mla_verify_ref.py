@@ -1,0 +1,186 @@
+"""fp64 NumPy oracle: gather, masked softmax, weighted sum.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the product path never
+imports this module.
+
+Inputs are NumPy arrays.  bf16 tensors are passed as their raw 16-bit
+patterns (``uint16``/``int16``) or as any float dtype that holds the bf16
+values exactly; ``bf16_bits_to_f64`` widens them exactly.
+"""
+from __future__ import annotations
+
+from typing import Iterable, List, Optional, Sequence, Set, Tuple
+
+import numpy as np
+
+D_QK = 576
+D_V = 512
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 values to fp64.
+
+    A bf16 number is the upper half of an IEEE binary32 pattern, so shifting
+    its 16 bits left by 16 gives the binary32 of the same value, which fp64
+    holds exactly.  Float inputs are taken to hold bf16 values already.
+    """
+    a = np.asarray(a)
+    if a.dtype in (np.uint16, np.int16):
+        bits = a.astype(np.uint16).astype(np.uint32) << np.uint32(16)
+        return bits.view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def ancestor_sets(parent: Sequence[int]) -> List[Set[int]]:
+    """anc[t] = {t} plus every draft reached by following parent links.
+
+    parent[i] is -1 (the draft hangs off the prefix) or an earlier draft.
+    Walking the links is the plain reading of a tree given by a parent array;
+    a link that does not point to an earlier draft ends the walk (the library
+    reports such a link as an input error).
+    """
+    T = len(parent)
+    out = []
+    for t in range(T):
+        s, cur = {t}, t
+        while True:
+            p = int(parent[cur])
+            if p < 0 or p >= cur:
+                break
+            s.add(p)
+            cur = p
+        out.append(s)
+    return out
+
+
+def gather_request_keys(kv_cache: np.ndarray, kv_indices: np.ndarray,
+                        kv_indptr: np.ndarray, b: int, n: int,
+                        page_size: int) -> np.ndarray:
+    """Rows of request b's n logical keys, in logical order, as fp64 [n, 576].
+
+    page_size 1: logical key j lives in slot kv_indices[indptr[b] + j].
+    page_size p: it lives in row j % p of page kv_indices[indptr[b] + j // p],
+    i.e. slot page * p + j % p.  (Scattered page_size=1 reads are the case
+    named in "The Decisive A/B ...", section "The Context".)
+    """
+    base = int(kv_indptr[b])
+    j = np.arange(n, dtype=np.int64)
+    if page_size == 1:
+        slots = np.asarray(kv_indices[base:base + n], dtype=np.int64)
+    else:
+        pages = np.asarray(kv_indices, dtype=np.int64)[base + j // page_size]
+        slots = pages * page_size + j % page_size
+    return bf16_bits_to_f64(kv_cache[slots])
+
+
+def _visible(P: int, n: int, anc_t: Set[int]) -> np.ndarray:
+    vis = np.zeros(n, dtype=bool)
+    vis[:P] = True
+    for i in anc_t:
+        vis[P + i] = True
+    return vis
+
+
+def _attend(qrows: np.ndarray, keys: np.ndarray, vis: np.ndarray,
+            scale: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Masked softmax attention of query rows over the visible keys (fp64).
+
+    qrows [m, 576], keys [n, 576], vis [n] -> out [m, 512], lse [m].
+    The max is subtracted before exp only to avoid overflow; it cancels
+    exactly in the definition.
+    """
+    kv = keys[vis]
+    s = scale * (qrows @ kv.T)                      # [m, n_vis]
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    z = e.sum(axis=1, keepdims=True)
+    lse = (m + np.log(z))[:, 0]
+    out = (e / z) @ kv[:, :D_V]
+    return out, lse
+
+
+def mla_verify(q, kv_cache, kv_indices, kv_indptr, kv_lens, draft_parent,
+               scale: float, page_size: int = 1):
+    """Whole-batch oracle.  q [B,T,H,576] -> out [B,T,H,512], lse [B,T,H]."""
+    qf = bf16_bits_to_f64(q)
+    B, T, H, _ = qf.shape
+    out = np.empty((B, T, H, D_V))
+    lse = np.empty((B, T, H))
+    for b in range(B):
+        n = int(kv_lens[b])
+        P = n - T
+        keys = gather_request_keys(kv_cache, kv_indices, kv_indptr, b, n, page_size)
+        anc = ancestor_sets(np.asarray(draft_parent)[b])
+        for t in range(T):
+            o, l = _attend(qf[b, t], keys, _visible(P, n, anc[t]), scale)
+            out[b, t], lse[b, t] = o, l
+    return out, lse
+
+
+def mla_verify_rows(rows: Iterable[Tuple[int, int, int]], q, kv_cache,
+                    kv_indices, kv_indptr, kv_lens, draft_parent, scale: float,
+                    page_size: int = 1):
+    """Oracle evaluated only at the given (b, t, h) query rows.
+
+    Used for sampled checks on workloads too large to evaluate whole.
+    Returns out [len(rows), 512], lse [len(rows)].
+    """
+    rows = list(rows)
+    T = np.asarray(q).shape[1]
+    out = np.empty((len(rows), D_V))
+    lse = np.empty(len(rows))
+    by_req = {}
+    for i, (b, t, h) in enumerate(rows):
+        by_req.setdefault(int(b), []).append((i, int(t), int(h)))
+    for b, items in by_req.items():
+        n = int(kv_lens[b])
+        P = n - T
+        keys = gather_request_keys(kv_cache, kv_indices, kv_indptr, b, n, page_size)
+        anc = ancestor_sets(np.asarray(draft_parent)[b])
+        for i, t, h in items:
+            qr = bf16_bits_to_f64(np.asarray(q)[b, t, h])[None, :]
+            o, l = _attend(qr, keys, _visible(P, n, anc[t]), scale)
+            out[i], lse[i] = o[0], l[0]
+    return out, lse
+
+
+def mla_verify_split_combine(q, kv_cache, kv_indices, kv_indptr, kv_lens,
+                             draft_parent, scale: float, page_size: int,
+                             nsplit: int):
+    """The oracle evaluated on nsplit key ranges, then merged by their LSEs.
+
+    This is the partial + reduce structure of "The Decisive A/B ...",
+    section "The Context" (KV split across workers, partials merged by a
+    reduce step), written in fp64: each range r yields o_r (its own softmax
+    over the visible keys in range, normalised) and lse_r; then
+        lse = log sum_r exp(lse_r),  out = sum_r exp(lse_r - lse) * o_r.
+    A range with no visible key has lse_r = -inf and weight 0.
+    """
+    qf = bf16_bits_to_f64(q)
+    B, T, H, _ = qf.shape
+    out = np.zeros((B, T, H, D_V))
+    lse = np.empty((B, T, H))
+    for b in range(B):
+        n = int(kv_lens[b])
+        P = n - T
+        keys = gather_request_keys(kv_cache, kv_indices, kv_indptr, b, n, page_size)
+        anc = ancestor_sets(np.asarray(draft_parent)[b])
+        edges = np.linspace(0, n, nsplit + 1).round().astype(int)
+        for t in range(T):
+            vis = _visible(P, n, anc[t])
+            parts = []
+            for r in range(nsplit):
+                lo, hi = edges[r], edges[r + 1]
+                vr = np.zeros(n, dtype=bool)
+                vr[lo:hi] = vis[lo:hi]
+                if not vr.any():
+                    parts.append((np.zeros((H, D_V)), np.full(H, -np.inf)))
+                    continue
+                parts.append(_attend(qf[b, t], keys, vr, scale))
+            L = np.stack([p[1] for p in parts])          # [nsplit, H]
+            mx = L.max(axis=0)
+            tot = mx + np.log(np.exp(L - mx).sum(axis=0))
+            w = np.exp(L - tot)                            # exp(-inf) = 0
+            out[b, t] = sum(w[r][:, None] * parts[r][0] for r in range(nsplit))
+            lse[b, t] = tot
+    return out, lse
