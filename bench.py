@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 verify attention (MLA, paged KV cache, draft tree).
+
+One step = one verify call (split-KV partial kernel + LSE combine) over the
+decode-batch workload (B=8 requests, 4096-token prefix each, T=8 chain
+drafts, H=64 heads, page_size=1 scattered slots in a 65536-slot cache, 1% of
+keys x8), inputs resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle as reference arm
+
+Timing: every step writes a 512 MB buffer (larger than the 126 MB L2) before
+the call, then CUDA events on the call's stream bracket the call; an event
+the library records between its two kernels splits partial and combine.
+Under torchrun every rank runs an independent replica (the operation has no
+cross-request exchange), and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="decode_batch")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "paged_mla_speculative_gb300", "csrc")
+    for name in ("common.cuh", "partial_mma.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the partial kernel from a committed ncu
+    summary, if it was taken on the current kernel source and workload."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get("partial_mma_kernel", {})
+        if e.get("source_sha1") == kernel_source_hash() and e.get("workload") == workload:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.proc = None
+        self.uuid = uuid
+
+    def __enter__(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, value):
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def config_of(w, extra=None):
+    prefix = w.prefix if w.prefix[0] != "uniform" else f"U[{w.prefix[1]},{w.prefix[2]}]"
+    c = {"workload": w.name, "batch": w.batch,
+         "context": prefix[0] if isinstance(prefix, tuple) and len(set(prefix)) == 1 else prefix,
+         "drafts": w.num_drafts, "tree": w.tree, "heads": w.num_heads, "page_size": w.page_size,
+         "cache_slots": w.num_slots, "spiky_keys": f"{w.spike_frac:.0%} x{w.spike_mult:g}",
+         "input_dtype": "bf16", "out_dtype": "fp32", "parallelism": "replicas",
+         "l2": "flushed: 512 MB write before every call"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def _bits(t):
+    """bf16 tensor -> numpy uint16 bit patterns (the oracle's input form)."""
+    import torch
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def oracle_seconds_per_call(inp, budget_s):
+    """CPU oracle on whole requests, round robin, until the budget is spent."""
+    import numpy as np
+    import oracle
+    qb, cb = _bits(inp.q), _bits(inp.kv_cache)
+    idx = inp.kv_indices.cpu().numpy()
+    ptr = inp.kv_indptr.cpu().numpy()
+    lens = inp.kv_lens.cpu().numpy()
+    par = inp.draft_parent.cpu().numpy()
+    B = len(lens)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b = done % B
+        sub_ptr = np.array([0, ptr[b + 1] - ptr[b]], dtype=np.int64)
+        oracle.mla_verify(qb[b:b + 1], cb, idx[ptr[b]:ptr[b + 1]], sub_ptr, lens[b:b + 1],
+                          par[b:b + 1], inp.scale, inp.page_size)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return el / done * B, done
+
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from paged_mla_speculative_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w, device="cpu")
+    qb, cb = _bits(inp.q), _bits(inp.kv_cache)
+    idx, ptr = inp.kv_indices.numpy(), inp.kv_indptr.numpy()
+    lens, par = inp.kv_lens.numpy(), inp.draft_parent.numpy()
+    B, T, H = w.batch, w.num_drafts, w.num_heads
+    rows_per_call = B * T * H
+
+    def step(i, nrows):
+        b, t = (i // T) % B, i % T
+        rows = [(b, t, h) for h in range(nrows)]
+        oracle.mla_verify_rows(rows, qb, cb, idx, ptr, lens, par, inp.scale, inp.page_size)
+
+    # Size the per-step sample so warm-up + steps end within ~150 s.
+    t0 = time.perf_counter()
+    step(0, 1)
+    t_row = max(time.perf_counter() - t0, 1e-4)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    nrows = max(1, min(H, int(budget / t_row)))
+    for i in range(args.warmup):
+        step(i, nrows)
+    times, t_start = [], time.perf_counter()
+    steps_run = 0
+    for i in range(args.steps):
+        s0 = time.perf_counter()
+        step(i, nrows)
+        times.append(time.perf_counter() - s0)
+        steps_run += 1
+        if time.perf_counter() - t_start > 180.0:
+            break
+    per_row = sum(times) / (steps_run * nrows)
+    us_per_call = per_row * rows_per_call * 1e6
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": "verify_attn_us_per_call", "value": us_per_call,
+        "unit": "us/call", "n_gpus": ws, "steps": args.steps, "steps_run": steps_run,
+        "warmup": args.warmup, "ms_per_step": sum(times) / steps_run * 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded), generated on the host",
+        "config": config_of(w),
+        "cpu_baseline": {"value": us_per_call, "unit": "us/call", "cores": cores, "kind": "oracle",
+                         "sample": f"{nrows} query rows of one (request, draft) per step, "
+                                   f"gather included, scaled to {rows_per_call} rows per call"},
+        "e2e": {"value": us_per_call, "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300(args):
+    import torch
+    ws, rank, local = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (the verify attention has no CPU path)")
+    torch.cuda.set_device(local)
+    from paged_mla_speculative_gb300 import binding as mb
+    from paged_mla_speculative_gb300 import build as mbuild
+    from paged_mla_speculative_gb300 import workloads as W
+    if rank == 0:
+        mbuild.build()
+    barrier(ws)
+
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w, device="cuda")
+    work = W.algorithmic_work(inp.prefix, w.num_drafts, w.num_heads)
+    max_len = max(inp.kv_lens.tolist())
+    plan = mb.Plan(w.batch, w.num_drafts, w.num_heads, w.page_size, w.num_slots, max_len)
+    ns = plan.nsplit(w.batch)
+    out, lse = plan.new_outputs(w.batch)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def call():
+        mb.mla_verify_attn(plan, inp.q, inp.kv_cache, inp.kv_indices, inp.kv_indptr,
+                           inp.kv_lens, inp.draft_parent, inp.scale, out, lse, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    assert plan.get_error() == 0, "device error word set during warm-up"
+
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ev_m:
+        e.record(stream)
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        t0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            plan.set_profile_event(ev_m[i])
+            ev_a[i].record(stream)
+            call()
+            ev_b[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(ws)
+    plan.set_profile_event(None)
+
+    call_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    part_ms = [a.elapsed_time(m) for a, m in zip(ev_a, ev_m)]
+    comb_ms = [m.elapsed_time(b) for m, b in zip(ev_m, ev_b)]
+    mean_call = max_over_ranks(ws, statistics.fmean(call_ms))
+    mean_part = max_over_ranks(ws, statistics.fmean(part_ms))
+    mean_comb = max_over_ranks(ws, statistics.fmean(comb_ms))
+    us_per_call = mean_call * 1e3 / ws          # whole job: ws replicas in parallel
+    q = statistics.quantiles(call_ms, n=10)
+
+    # CUDA-graph replay of the same call (capture-safe path), device timed.
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        call_s = lambda: mb.mla_verify_attn(plan, inp.q, inp.kv_cache, inp.kv_indices,  # noqa: E731
+                                            inp.kv_indptr, inp.kv_lens, inp.draft_parent,
+                                            inp.scale, out, lse, stream=s)
+        call_s()
+    s.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        call_s()
+    gk = min(K, 500)
+    ga = [torch.cuda.Event(enable_timing=True) for _ in range(gk)]
+    gb = [torch.cuda.Event(enable_timing=True) for _ in range(gk)]
+    for i in range(gk):
+        flush.zero_()
+        ga[i].record(stream)
+        g.replay()
+        gb[i].record(stream)
+    torch.cuda.synchronize()
+    graph_us = statistics.fmean(a.elapsed_time(b) for a, b in zip(ga, gb)) * 1e3
+
+    # End to end through the host-buffer entry point: H2D of the step's
+    # inputs from pinned memory, the call, D2H of out/lse, stream sync.
+    hq = inp.q.cpu().pin_memory()
+    hidx = inp.kv_indices.cpu().pin_memory()
+    hptr = inp.kv_indptr.cpu().pin_memory()
+    hlen = inp.kv_lens.cpu().pin_memory()
+    hpar = inp.draft_parent.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        mb.mla_verify_attn_host(plan, hq, inp.kv_cache, hidx, hptr, hlen, hpar, inp.scale,
+                                hout, hlse, stream=stream)
+    e2e_steps = min(args.e2e_steps, K)
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        mb.mla_verify_attn_host(plan, hq, inp.kv_cache, hidx, hptr, hlen, hpar, inp.scale,
+                                hout, hlse, stream=stream)
+    e2e_s = max_over_ranks(ws, time.perf_counter() - t0)
+    e2e_us = e2e_s / e2e_steps / ws * 1e6
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hidx, hptr, hlen, hpar))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
+    assert torch.equal(hout, out.cpu()), "host entry point disagrees with device entry point"
+    assert plan.get_error() == 0
+
+    peaks, peak_src = load_peaks()
+    flops = work["flops"]
+    achieved = flops / (mean_part * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    kv_gbs = work["kv_bytes"] / (mean_call * 1e-3) / 1e9
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    t_roof_us = max(work["bytes"] / (hbm * 1e9), flops / (peak * 1e12)) * 1e6
+    clocks = clk.summary()
+    launches = K * (2 if ns > 1 else 1)
+
+    line = {
+        "metric": "verify_attn_us_per_call", "value": us_per_call, "unit": "us/call",
+        "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": mean_call,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic (seeded), bf16 inputs resident in HBM",
+        "config": config_of(w, {"nsplit": ns, "kernel": "partial_mma_kernel + combine_kernel"}),
+        "us_per_call_p10_p50_p90": [q[0] * 1e3, statistics.median(call_ms) * 1e3, q[-1] * 1e3],
+        "partial_us": mean_part * 1e3, "combine_us": mean_comb * 1e3,
+        "graph_replay_us_per_call": graph_us,
+        "kv_gbs": kv_gbs, "kv_frac_of_hbm": kv_gbs / hbm,
+        "roofline_time_us": t_roof_us, "frac_of_roofline": t_roof_us / (mean_call * 1e3),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                     "kernel": "partial_mma_kernel",
+                     "peak_source": f"{peak_src} bf16 burst (fp16 has the same tensor rate)"},
+        "clocks": clocks, "gpu_launches": launches,
+        "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "timed_wall_s": wall,
+    }
+    if ws == 1 and rank == 0 and not args.no_cpu_baseline:
+        sec, nreq = oracle_seconds_per_call(inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": sec * 1e6, "unit": "us/call",
+                                "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                "sample": f"{nreq} whole requests of the same inputs (fp64 NumPy), "
+                                          f"scaled to {w.batch} requests per call"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

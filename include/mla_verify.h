@@ -116,7 +116,10 @@ void mla_verify_plan_destroy(mla_verify_plan* plan);
 /*
  * Fix the split count used by later calls (1..MLA_VERIFY_MAX_NSPLIT), or 0
  * to choose it from the batch, the plan's max_kv_len and the SM count.
- * The workspace was sized for the largest count; larger values are refused.
+ * A count above the number of 64-key blocks in max_kv_len is clamped to it.
+ * A call whose batch x split count exceeds the workspace the plan sized
+ * (the automatic choice at every batch, or at least 64 MB) returns
+ * MLA_VERIFY_ERR_SHAPE.
  */
 #define MLA_VERIFY_MAX_NSPLIT 32
 int mla_verify_plan_set_nsplit(mla_verify_plan* plan, int nsplit);
@@ -126,6 +129,17 @@ int mla_verify_plan_get_nsplit(const mla_verify_plan* plan, int batch);
 
 /* Select the partial-kernel family (MLA_VERIFY_KERNEL_*). */
 int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
+
+/*
+ * Profiling hook.  When `event` (a cudaEvent_t created with timing enabled)
+ * is not NULL, every later mla_verify_attn call records it on the call's
+ * stream right after the split-KV partial kernel, so the time from an event
+ * recorded just before the call measures that kernel alone, and the time to
+ * an event recorded just after the call measures the combine.  The record
+ * is an ordinary stream operation and is captured into graphs like the
+ * kernels.  Pass NULL to stop.
+ */
+int mla_verify_plan_set_profile_event(mla_verify_plan* plan, void* event);
 
 /* Bytes of device workspace the plan holds (partials + error word). */
 size_t mla_verify_plan_workspace_bytes(const mla_verify_plan* plan);

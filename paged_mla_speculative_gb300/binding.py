@@ -1,0 +1,248 @@
+"""ctypes binding of libmla_verify.so (argument marshalling only).
+
+Every step of the verify attention runs in the library's CUDA kernels; this
+module checks tensor dtypes, shapes, devices and contiguity, passes raw
+pointers and the current CUDA stream, and turns status codes into
+exceptions.  There is no fallback: if the library is missing or fails to
+load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libmla_verify.so")
+
+OUT_F32 = 0
+OUT_BF16 = 1
+KERNEL_AUTO = 0
+KERNEL_MMA = 1
+MAX_NSPLIT = 32
+
+DEV_BAD_SLOT = 1
+DEV_BAD_LEN = 2
+DEV_BAD_PARENT = 4
+DEV_BAD_INDPTR = 8
+DEV_TIMEOUT = 16
+
+STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_ALIGN", -3: "ERR_SHAPE", -4: "ERR_BATCH",
+          -5: "ERR_SCALE", -6: "ERR_CUDA", -7: "ERR_DEVICE", -8: "ERR_OOM", -9: "ERR_ARG"}
+
+# name -> (restype, argtypes): every entry point the header declares.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "mla_verify_plan_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, ctypes.c_int64, _I, _I, _I]),
+    "mla_verify_plan_destroy": (None, [_P]),
+    "mla_verify_plan_set_nsplit": (_I, [_P, _I]),
+    "mla_verify_plan_get_nsplit": (_I, [_P, _I]),
+    "mla_verify_plan_set_kernel": (_I, [_P, _I]),
+    "mla_verify_plan_workspace_bytes": (ctypes.c_size_t, [_P]),
+    "mla_verify_plan_set_profile_event": (_I, [_P, _P]),
+    "mla_verify_attn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
+    "mla_verify_attn_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
+    "mla_verify_get_error": (_I, [_P, ctypes.POINTER(_I), _I]),
+    "mla_verify_strerror": (ctypes.c_char_p, [_I]),
+    "mla_verify_version": (_I, []),
+}
+
+_lib = None
+
+
+class MlaVerifyError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({strerror(status)})")
+
+
+def load_library(path: Optional[str] = None):
+    """Load (once) and return the ctypes handle; raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build it with `python -m paged_mla_speculative_gb300.build` "
+            "(the verify attention has no non-CUDA implementation)")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def strerror(status: int) -> str:
+    return load_library().mla_verify_strerror(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise MlaVerifyError(status, what)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return int(t.data_ptr())
+
+
+class Plan:
+    """Owns one mla_verify_plan (its workspace and error word)."""
+
+    def __init__(self, max_batch: int, num_drafts: int, num_heads: int, page_size: int,
+                 num_slots: int, max_kv_len: int, out_dtype=torch.float32,
+                 device: Optional[int] = None):
+        lib = load_library()
+        if device is None:
+            device = torch.cuda.current_device()
+        od = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}[out_dtype]
+        h = ctypes.c_void_p()
+        _check(lib.mla_verify_plan_create(ctypes.byref(h), max_batch, num_drafts, num_heads,
+                                          page_size, num_slots, max_kv_len, od, device),
+               "mla_verify_plan_create")
+        self._h = h
+        self.max_batch, self.T, self.H = max_batch, num_drafts, num_heads
+        self.page_size, self.num_slots, self.max_kv_len = page_size, num_slots, max_kv_len
+        self.out_dtype, self.device = out_dtype, device
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("plan already destroyed")
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            load_library().mla_verify_plan_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def set_nsplit(self, nsplit: int):
+        _check(load_library().mla_verify_plan_set_nsplit(self.handle, nsplit), "set_nsplit")
+
+    def nsplit(self, batch: int) -> int:
+        v = load_library().mla_verify_plan_get_nsplit(self.handle, batch)
+        if v < 0:
+            raise MlaVerifyError(v, "get_nsplit")
+        return v
+
+    def set_kernel(self, kernel: int):
+        _check(load_library().mla_verify_plan_set_kernel(self.handle, kernel), "set_kernel")
+
+    def set_profile_event(self, event):
+        """Record ``event`` (a torch.cuda.Event with timing, or None) after
+        the partial kernel of every later call."""
+        ptr = None
+        if event is not None:
+            if int(event.cuda_event) == 0:   # torch creates the event on first record
+                event.record()
+                event.synchronize()
+            ptr = int(event.cuda_event)
+        _check(load_library().mla_verify_plan_set_profile_event(self.handle, ptr),
+               "set_profile_event")
+        self._profile_event = event
+
+    def workspace_bytes(self) -> int:
+        return int(load_library().mla_verify_plan_workspace_bytes(self.handle))
+
+    def get_error(self, clear: bool = True) -> int:
+        v = ctypes.c_int(0)
+        _check(load_library().mla_verify_get_error(self.handle, ctypes.byref(v), int(clear)),
+               "get_error")
+        return v.value
+
+    def new_outputs(self, batch: int):
+        dev = torch.device("cuda", self.device)
+        out = torch.empty((batch, self.T, self.H, 512), dtype=self.out_dtype, device=dev)
+        lse = torch.empty((batch, self.T, self.H), dtype=torch.float32, device=dev)
+        return out, lse
+
+
+def _expect(t: torch.Tensor, name: str, dtype, device=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def mla_verify_attn(plan: Plan, q, kv_cache, kv_indices, kv_indptr, kv_lens, draft_parent,
+                    scale: float, out=None, lse=None, stream=None):
+    """Verify attention on the plan's device; returns (out, lse).
+
+    q [B,T,H,576] bf16, kv_cache [S,576] bf16, kv_indices/kv_indptr/kv_lens/
+    draft_parent int32, out [B,T,H,512] (plan's dtype), lse [B,T,H] fp32.
+    Enqueued on ``stream`` (default: the current torch stream); no sync.
+    """
+    B = q.shape[0]
+    dev = torch.device("cuda", plan.device)
+    _expect(q, "q", torch.bfloat16, dev, (B, plan.T, plan.H, 576))
+    _expect(kv_cache, "kv_cache", torch.bfloat16, dev)
+    if kv_cache.dim() != 2 or kv_cache.shape[1] != 576 or kv_cache.shape[0] != plan.num_slots:
+        raise ValueError(f"kv_cache must be [{plan.num_slots}, 576]")
+    _expect(kv_indices, "kv_indices", torch.int32, dev)
+    _expect(kv_indptr, "kv_indptr", torch.int32, dev, (B + 1,))
+    _expect(kv_lens, "kv_lens", torch.int32, dev, (B,))
+    _expect(draft_parent, "draft_parent", torch.int32, dev, (B, plan.T))
+    if out is None or lse is None:
+        o2, l2 = plan.new_outputs(B)
+        out = o2 if out is None else out
+        lse = l2 if lse is None else lse
+    _expect(out, "out", plan.out_dtype, dev, (B, plan.T, plan.H, 512))
+    _expect(lse, "lse", torch.float32, dev, (B, plan.T, plan.H))
+    st = load_library().mla_verify_attn(
+        plan.handle, B, _ptr(q), _ptr(kv_cache), _ptr(kv_indices), _ptr(kv_indptr),
+        _ptr(kv_lens), _ptr(draft_parent), float(scale), _ptr(out), _ptr(lse),
+        _stream_ptr(stream))
+    _check(st, "mla_verify_attn")
+    return out, lse
+
+
+def mla_verify_attn_host(plan: Plan, q, kv_cache, kv_indices, kv_indptr, kv_lens,
+                         draft_parent, scale: float, out, lse, stream=None):
+    """Host-buffer variant: q/indices/indptr/lens/parent/out/lse are CPU
+    tensors (pinned for speed), kv_cache is on the device.  Copies in, runs,
+    copies back and synchronises ``stream``."""
+    B = q.shape[0]
+    cpu = torch.device("cpu")
+    dev = torch.device("cuda", plan.device)
+    _expect(q, "q", torch.bfloat16, cpu, (B, plan.T, plan.H, 576))
+    _expect(kv_cache, "kv_cache", torch.bfloat16, dev)
+    _expect(kv_indices, "kv_indices", torch.int32, cpu)
+    _expect(kv_indptr, "kv_indptr", torch.int32, cpu, (B + 1,))
+    _expect(kv_lens, "kv_lens", torch.int32, cpu, (B,))
+    _expect(draft_parent, "draft_parent", torch.int32, cpu, (B, plan.T))
+    _expect(out, "out", plan.out_dtype, cpu, (B, plan.T, plan.H, 512))
+    _expect(lse, "lse", torch.float32, cpu, (B, plan.T, plan.H))
+    if kv_indices.numel() < int(kv_indptr[B]):
+        raise ValueError("kv_indices shorter than kv_indptr[B]")
+    st = load_library().mla_verify_attn_host(
+        plan.handle, B, _ptr(q), _ptr(kv_cache), _ptr(kv_indices), _ptr(kv_indptr),
+        _ptr(kv_lens), _ptr(draft_parent), float(scale), _ptr(out), _ptr(lse),
+        _stream_ptr(stream))
+    _check(st, "mla_verify_attn_host")
+    return out, lse

@@ -1,0 +1,326 @@
+// C ABI of the verify-attention library: plan (workspace owner), argument
+// checks, split planning and the capture-safe launch sequence.
+//
+// The launch path follows the capture-safety recipe of "The Decisive A/B:
+// When Benchmarking Honesty Reveals the Real Bottleneck" (section "The
+// Context"): a fixed split count, workspace allocated ahead of time, native
+// buffer pointers, and no host synchronisation or device-memory read per
+// call, so the whole call can be recorded in a CUDA graph.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <algorithm>
+#include <new>
+
+#include "../../include/mla_verify.h"
+#include "kernels.h"
+
+using mlav::Params;
+
+struct mla_verify_plan {
+  int device;
+  int max_batch, T, H, R, page_size;
+  int64_t num_slots;
+  int max_kv_len;
+  int out_dtype;
+  int num_sms;
+  int forced_nsplit;      // 0 = choose per call
+  int kernel;             // MLA_VERIFY_KERNEL_*
+  long long ws_capacity;  // request-splits the workspace holds
+  float* ws_o;
+  float* ws_lse;
+  int* err;
+  size_t ws_bytes;
+  // Device staging for mla_verify_attn_host.
+  void* st_q;
+  int32_t* st_idx;
+  int32_t* st_indptr;
+  int32_t* st_lens;
+  int32_t* st_parent;
+  void* st_out;
+  float* st_lse;
+  long long st_idx_cap;
+  cudaEvent_t profile_event;  // recorded after the partial kernel, or null
+};
+
+namespace {
+
+constexpr int kRowsPerTile = 64;
+constexpr int kKeysPerBlock = 64;
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Split count for `batch` requests: minimise (waves of CTAs) x (key blocks
+// per CTA) plus the cost of moving the split partials through the combine,
+// in units of one CTA key-block step.
+int auto_nsplit(const mla_verify_plan* pl, int batch) {
+  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, kRowsPerTile);
+  const long long max_blocks = ceil_div(pl->max_kv_len, kKeysPerBlock);
+  const int cap = static_cast<int>(std::min<long long>(mlav::MAX_NSPLIT, max_blocks));
+  // Bytes one CTA block-step is worth (about 2 us of HBM time at 6 TB/s).
+  const double bytes_per_step = 12e6;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int ns = 1; ns <= cap; ++ns) {
+    const long long ctas = units * ns;
+    const double waves = static_cast<double>(ceil_div(ctas, pl->num_sms));
+    const double steps = static_cast<double>(ceil_div(max_blocks, ns));
+    double cost = waves * steps;
+    if (ns > 1) cost += 1.0 + static_cast<double>(units) * kRowsPerTile * ns * 4096.0 / bytes_per_step;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = ns;
+    }
+  }
+  return best;
+}
+
+// Forced counts are clamped to the number of key blocks of max_kv_len.
+int effective_nsplit(const mla_verify_plan* pl, int batch) {
+  if (!pl->forced_nsplit) return auto_nsplit(pl, batch);
+  return static_cast<int>(std::min<long long>(pl->forced_nsplit, ceil_div(pl->max_kv_len, kKeysPerBlock)));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void free_all(mla_verify_plan* p) {
+  void* bufs[] = {p->ws_o, p->ws_lse, p->err, p->st_q, p->st_idx, p->st_indptr,
+                  p->st_lens, p->st_parent, p->st_out, p->st_lse};
+  for (void* b : bufs)
+    if (b) cudaFree(b);
+}
+
+int check_device(const mla_verify_plan* pl) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  return dev == pl->device ? MLA_VERIFY_OK : MLA_VERIFY_ERR_DEVICE;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_verify_version(void) { return 100; }
+
+const char* mla_verify_strerror(int status) {
+  switch (status) {
+    case MLA_VERIFY_OK: return "ok";
+    case MLA_VERIFY_ERR_NULL: return "a required pointer is NULL";
+    case MLA_VERIFY_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case MLA_VERIFY_ERR_SHAPE: return "unsupported shape, page size, dtype or split count";
+    case MLA_VERIFY_ERR_BATCH: return "batch outside [1, max_batch]";
+    case MLA_VERIFY_ERR_SCALE: return "scale is not finite";
+    case MLA_VERIFY_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case MLA_VERIFY_ERR_DEVICE: return "the current CUDA device is not the plan's device";
+    case MLA_VERIFY_ERR_OOM: return "device memory allocation failed";
+    case MLA_VERIFY_ERR_ARG: return "invalid argument";
+    default: return "unknown status";
+  }
+}
+
+int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts, int num_heads,
+                           int page_size, int64_t num_slots, int max_kv_len, int out_dtype,
+                           int device) {
+  if (!out) return MLA_VERIFY_ERR_NULL;
+  *out = nullptr;
+  if (max_batch < 1 || num_drafts < 1 || num_drafts > mlav::MAX_T || num_heads < 1 ||
+      static_cast<long long>(num_drafts) * num_heads > 4096 ||
+      (page_size != 1 && page_size != mlav::PAGE) || num_slots < 1 ||
+      (page_size == mlav::PAGE && num_slots % mlav::PAGE) || max_kv_len < num_drafts ||
+      (out_dtype != MLA_VERIFY_OUT_F32 && out_dtype != MLA_VERIFY_OUT_BF16))
+    return MLA_VERIFY_ERR_SHAPE;
+  if (cudaSetDevice(device) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return MLA_VERIFY_ERR_CUDA;
+  if (mlav::partial_mma_prepare() != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+
+  mla_verify_plan* pl = new (std::nothrow) mla_verify_plan();
+  if (!pl) return MLA_VERIFY_ERR_OOM;
+  pl->device = device;
+  pl->max_batch = max_batch;
+  pl->T = num_drafts;
+  pl->H = num_heads;
+  pl->R = num_drafts * num_heads;
+  pl->page_size = page_size;
+  pl->num_slots = num_slots;
+  pl->max_kv_len = max_kv_len;
+  pl->out_dtype = out_dtype;
+  pl->num_sms = sms;
+  pl->kernel = MLA_VERIFY_KERNEL_AUTO;
+
+  // Workspace capacity in request-splits: enough for the automatic choice at
+  // every batch size, and for forced split counts up to a 64 MB floor.
+  const long long max_blocks = ceil_div(max_kv_len, kKeysPerBlock);
+  long long cap = 0;
+  for (int b = 1; b <= max_batch; ++b) cap = std::max<long long>(cap, 1LL * b * auto_nsplit(pl, b));
+  const long long floor_rs = (64LL << 20) / (1LL * pl->R * (mlav::D_V + 1) * 4);
+  cap = std::max(cap, std::min(1LL * max_batch * std::min<long long>(mlav::MAX_NSPLIT, max_blocks),
+                               std::max(floor_rs, std::min<long long>(mlav::MAX_NSPLIT, max_blocks))));
+  pl->ws_capacity = cap;
+  const size_t rows = static_cast<size_t>(cap) * pl->R;
+  const size_t out_elt = out_dtype == MLA_VERIFY_OUT_BF16 ? 2 : 4;
+  const long long idx_per_req = page_size == 1 ? max_kv_len : ceil_div(max_kv_len, mlav::PAGE);
+  pl->st_idx_cap = idx_per_req * max_batch;
+  const size_t qrows = static_cast<size_t>(max_batch) * pl->R;
+
+  bool ok = cudaMalloc(&pl->ws_o, rows * mlav::D_V * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&pl->ws_lse, rows * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&pl->err, 256) == cudaSuccess &&
+            cudaMalloc(&pl->st_q, qrows * mlav::ROW_BYTES) == cudaSuccess &&
+            cudaMalloc(&pl->st_idx, static_cast<size_t>(pl->st_idx_cap) * 4) == cudaSuccess &&
+            cudaMalloc(&pl->st_indptr, static_cast<size_t>(max_batch + 1) * 4) == cudaSuccess &&
+            cudaMalloc(&pl->st_lens, static_cast<size_t>(max_batch) * 4) == cudaSuccess &&
+            cudaMalloc(&pl->st_parent, static_cast<size_t>(max_batch) * num_drafts * 4) == cudaSuccess &&
+            cudaMalloc(&pl->st_out, qrows * mlav::D_V * out_elt) == cudaSuccess &&
+            cudaMalloc(&pl->st_lse, qrows * sizeof(float)) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_all(pl);
+    delete pl;
+    return MLA_VERIFY_ERR_OOM;
+  }
+  pl->ws_bytes = rows * (mlav::D_V + 1) * sizeof(float) + 256;
+  if (cudaMemset(pl->err, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    free_all(pl);
+    delete pl;
+    return MLA_VERIFY_ERR_CUDA;
+  }
+  *out = pl;
+  return MLA_VERIFY_OK;
+}
+
+void mla_verify_plan_destroy(mla_verify_plan* pl) {
+  if (!pl) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(pl->device);
+  cudaDeviceSynchronize();
+  free_all(pl);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete pl;
+}
+
+int mla_verify_plan_set_nsplit(mla_verify_plan* pl, int nsplit) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  if (nsplit < 0 || nsplit > mlav::MAX_NSPLIT) return MLA_VERIFY_ERR_SHAPE;
+  pl->forced_nsplit = nsplit;
+  return MLA_VERIFY_OK;
+}
+
+int mla_verify_plan_get_nsplit(const mla_verify_plan* pl, int batch) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  return effective_nsplit(pl, batch);
+}
+
+int mla_verify_plan_set_kernel(mla_verify_plan* pl, int kernel) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  if (kernel != MLA_VERIFY_KERNEL_AUTO && kernel != MLA_VERIFY_KERNEL_MMA) return MLA_VERIFY_ERR_ARG;
+  pl->kernel = kernel;
+  return MLA_VERIFY_OK;
+}
+
+int mla_verify_plan_set_profile_event(mla_verify_plan* pl, void* event) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  pl->profile_event = static_cast<cudaEvent_t>(event);
+  return MLA_VERIFY_OK;
+}
+
+size_t mla_verify_plan_workspace_bytes(const mla_verify_plan* pl) { return pl ? pl->ws_bytes : 0; }
+
+int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* kv_cache,
+                    const int32_t* kv_indices, const int32_t* kv_indptr, const int32_t* kv_lens,
+                    const int32_t* draft_parent, float scale, void* out, float* lse,
+                    void* stream) {
+  if (!pl || !q || !kv_cache || !kv_indices || !kv_indptr || !kv_lens || !draft_parent || !out ||
+      !lse)
+    return MLA_VERIFY_ERR_NULL;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(kv_indices) || !aligned16(kv_indptr) ||
+      !aligned16(kv_lens) || !aligned16(draft_parent) || !aligned16(out) || !aligned16(lse))
+    return MLA_VERIFY_ERR_ALIGN;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  if (!std::isfinite(scale)) return MLA_VERIFY_ERR_SCALE;
+  const int dev_status = check_device(pl);
+  if (dev_status != MLA_VERIFY_OK) return dev_status;
+  const int ns = effective_nsplit(pl, batch);
+  if (1LL * batch * ns > pl->ws_capacity) return MLA_VERIFY_ERR_SHAPE;
+
+  Params p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv = static_cast<const uint16_t*>(kv_cache);
+  p.kv_indices = kv_indices;
+  p.kv_indptr = kv_indptr;
+  p.kv_lens = kv_lens;
+  p.draft_parent = draft_parent;
+  p.scale_log2 = scale * mlav::kLog2e;
+  p.batch = batch;
+  p.T = pl->T;
+  p.H = pl->H;
+  p.R = pl->R;
+  p.page_size = pl->page_size;
+  p.num_slots = pl->num_slots;
+  p.max_kv_len = pl->max_kv_len;
+  p.nsplit = ns;
+  p.ws_o = pl->ws_o;
+  p.ws_lse = pl->ws_lse;
+  p.out = out;
+  p.lse = lse;
+  p.out_bf16 = pl->out_dtype == MLA_VERIFY_OUT_BF16;
+  p.err = pl->err;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mlav::launch_partial_mma(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (pl->profile_event && cudaEventRecord(pl->profile_event, s) != cudaSuccess)
+    return MLA_VERIFY_ERR_CUDA;
+  if (ns > 1 && mlav::launch_combine(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  return MLA_VERIFY_OK;
+}
+
+int mla_verify_attn_host(mla_verify_plan* pl, int batch, const void* q_host, const void* kv_cache,
+                         const int32_t* kv_indices_host, const int32_t* kv_indptr_host,
+                         const int32_t* kv_lens_host, const int32_t* draft_parent_host,
+                         float scale, void* out_host, float* lse_host, void* stream) {
+  if (!pl || !q_host || !kv_cache || !kv_indices_host || !kv_indptr_host || !kv_lens_host ||
+      !draft_parent_host || !out_host || !lse_host)
+    return MLA_VERIFY_ERR_NULL;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  const long long nidx = kv_indptr_host[batch];
+  if (nidx < 0 || nidx > pl->st_idx_cap || kv_indptr_host[0] < 0) return MLA_VERIFY_ERR_ARG;
+  const int dev_status = check_device(pl);
+  if (dev_status != MLA_VERIFY_OK) return dev_status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(batch) * pl->R;
+  const size_t out_elt = pl->out_dtype == MLA_VERIFY_OUT_BF16 ? 2 : 4;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  bool ok =
+      cudaMemcpyAsync(pl->st_q, q_host, rows * mlav::ROW_BYTES, h2d, s) == cudaSuccess &&
+      cudaMemcpyAsync(pl->st_idx, kv_indices_host, static_cast<size_t>(nidx) * 4, h2d, s) == cudaSuccess &&
+      cudaMemcpyAsync(pl->st_indptr, kv_indptr_host, static_cast<size_t>(batch + 1) * 4, h2d, s) == cudaSuccess &&
+      cudaMemcpyAsync(pl->st_lens, kv_lens_host, static_cast<size_t>(batch) * 4, h2d, s) == cudaSuccess &&
+      cudaMemcpyAsync(pl->st_parent, draft_parent_host, static_cast<size_t>(batch) * pl->T * 4, h2d, s) == cudaSuccess;
+  if (!ok) return MLA_VERIFY_ERR_CUDA;
+  const int st = mla_verify_attn(pl, batch, pl->st_q, kv_cache, pl->st_idx, pl->st_indptr,
+                                 pl->st_lens, pl->st_parent, scale, pl->st_out, pl->st_lse, stream);
+  if (st != MLA_VERIFY_OK) return st;
+  ok = cudaMemcpyAsync(out_host, pl->st_out, rows * mlav::D_V * out_elt, d2h, s) == cudaSuccess &&
+       cudaMemcpyAsync(lse_host, pl->st_lse, rows * sizeof(float), d2h, s) == cudaSuccess &&
+       cudaStreamSynchronize(s) == cudaSuccess;
+  return ok ? MLA_VERIFY_OK : MLA_VERIFY_ERR_CUDA;
+}
+
+int mla_verify_get_error(mla_verify_plan* pl, int* device_status, int clear) {
+  if (!pl || !device_status) return MLA_VERIFY_ERR_NULL;
+  const int dev_status = check_device(pl);
+  if (dev_status != MLA_VERIFY_OK) return dev_status;
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (cudaMemcpy(&v, pl->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_VERIFY_ERR_CUDA;
+  if (clear && cudaMemset(pl->err, 0, sizeof(int)) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (clear && cudaDeviceSynchronize() != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  *device_status = v;
+  return MLA_VERIFY_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// Shared device-side definitions of the verify-attention kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mlav {
+
+constexpr int D_QK = 576;                 // latent 512 + rope 64
+constexpr int D_V = 512;                  // value = latent part of each row
+constexpr int ROW_BYTES = D_QK * 2;       // 1152 bytes per bf16/fp16 row
+constexpr int ROW_CHUNKS = ROW_BYTES / 16;  // 72 sixteen-byte chunks per row
+constexpr int PAGE = 64;                  // the paged layout's rows per page
+constexpr int MAX_T = 32;                 // drafts per request (one mask bit each)
+constexpr int MAX_NSPLIT = 32;
+
+// Device error bits (mirrors MLA_VERIFY_DEV_* in the public header).
+enum : int {
+  ERR_SLOT = 1,
+  ERR_LEN = 2,
+  ERR_PARENT = 4,
+  ERR_INDPTR = 8,
+  ERR_TIMEOUT = 16,
+};
+
+// Arguments of one verify call, shared by every kernel of the call.
+struct Params {
+  const uint16_t* q;            // bf16 [B, R, 576], R = T*H
+  const uint16_t* kv;           // bf16 [num_slots, 576]
+  const int32_t* kv_indices;
+  const int32_t* kv_indptr;     // [B+1]
+  const int32_t* kv_lens;       // [B]
+  const int32_t* draft_parent;  // [B, T]
+  float scale_log2;             // scale * log2(e): scores kept in base 2
+  int batch, T, H, R;
+  int page_size;                // 1 or 64
+  int64_t num_slots;
+  int max_kv_len;
+  int nsplit;
+  float* ws_o;                  // [B][nsplit][R][512] normalised split outputs
+  float* ws_lse;                // [B][nsplit][R] natural-log split LSEs
+  void* out;                    // fp32 or bf16 [B, R, 512]
+  float* lse;                   // [B, R]
+  int out_bf16;
+  int* err;                     // sticky device error word
+};
+
+// Per-request facts every CTA of the request derives the same way.
+struct Request {
+  int n;        // kv_len: prefix + drafts
+  int P;        // prefix length
+  int ip0;      // first index position
+  bool ok;      // length and indptr consistent
+};
+
+__device__ __forceinline__ Request load_request(const Params& p, int b) {
+  Request r;
+  r.n = p.kv_lens[b];
+  r.P = r.n - p.T;
+  r.ip0 = p.kv_indptr[b];
+  const int ip1 = p.kv_indptr[b + 1];
+  const int ipn = p.kv_indptr[p.batch];
+  const long long need = p.page_size == 1 ? (long long)r.n : ((long long)r.n + PAGE - 1) / PAGE;
+  const bool len_ok = r.n >= p.T && r.n <= p.max_kv_len;
+  const bool ptr_ok = r.ip0 >= 0 && ip1 >= r.ip0 && ip1 <= ipn && (long long)(ip1 - r.ip0) == need;
+  r.ok = len_ok && ptr_ok;
+  return r;
+}
+
+// Bit i of the result is set iff draft i is t itself or an ancestor of t.
+// A parent that is not an earlier draft ends the walk and is reported.
+__device__ __forceinline__ uint32_t ancestor_mask(const int32_t* parent, int t, int* err) {
+  uint32_t m = 1u << t;
+  int cur = t;
+  for (int it = 0; it < MAX_T; ++it) {
+    const int par = parent[cur];
+    if (par < 0) {
+      if (par != -1) atomicOr(err, ERR_PARENT);
+      break;
+    }
+    if (par >= cur) {
+      atomicOr(err, ERR_PARENT);
+      break;
+    }
+    m |= 1u << par;
+    cur = par;
+  }
+  return m;
+}
+
+// Slot of logical key j, or -1 when the table points outside the cache.
+__device__ __forceinline__ long long key_slot(const Params& p, int ip0, int j) {
+  if (p.page_size == 1) {
+    const long long s = p.kv_indices[ip0 + j];
+    return (s >= 0 && s < p.num_slots) ? s : -1;
+  }
+  const long long pg = p.kv_indices[ip0 + j / PAGE];
+  return (pg >= 0 && pg < p.num_slots / PAGE) ? pg * PAGE + (j % PAGE) : -1;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+}  // namespace mlav

@@ -1,0 +1,18 @@
+// Internal launch interface between the C ABI and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace mlav {
+
+// Split-KV partial kernel on warp-level mma.sync.
+int partial_mma_smem_bytes();
+cudaError_t partial_mma_prepare();
+cudaError_t launch_partial_mma(const Params& p, cudaStream_t stream);
+
+// LSE combine of the split partials into out/lse.
+cudaError_t launch_combine(const Params& p, cudaStream_t stream);
+
+}  // namespace mlav

@@ -1,0 +1,143 @@
+"""Error behaviour: host-visible problems return a status; problems only
+visible in device data set the sticky device word and never fault.
+
+Every bad index here is caught by the kernels' own range checks before any
+memory access (the key is masked or the request is written as NaN)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from paged_mla_speculative_gb300 import binding as mb
+from paged_mla_speculative_gb300 import workloads as W
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_mla_speculative_gb300 import build
+    build.build()
+
+
+def _case(seed=1, **kw):
+    base = dict(name="e", batch=2, num_drafts=4, num_heads=16, prefix=(200, 100),
+                tree="random", num_slots=2048, seed=seed)
+    base.update(kw)
+    return G.to_cuda(W.make_inputs(W.Workload(**base)))
+
+
+def _raw(plan, inp, batch=None, **over):
+    lib = mb.load_library()
+    out, lse = plan.new_outputs(inp.q.shape[0])
+    a = dict(q=inp.q.data_ptr(), kv=inp.kv_cache.data_ptr(), idx=inp.kv_indices.data_ptr(),
+             indptr=inp.kv_indptr.data_ptr(), lens=inp.kv_lens.data_ptr(),
+             par=inp.draft_parent.data_ptr(), scale=inp.scale, out=out.data_ptr(),
+             lse=lse.data_ptr())
+    a.update(over)
+    return lib.mla_verify_attn(plan.handle, batch or inp.q.shape[0], a["q"], a["kv"], a["idx"],
+                               a["indptr"], a["lens"], a["par"], ctypes.c_float(a["scale"]),
+                               a["out"], a["lse"], None)
+
+
+def test_host_argument_errors():
+    inp = _case()
+    with G.make_plan(inp) as plan:
+        assert _raw(plan, inp) == 0
+        assert _raw(plan, inp, q=None) == -1
+        assert _raw(plan, inp, lse=None) == -1
+        assert _raw(plan, inp, q=inp.q.data_ptr() + 2) == -2
+        assert _raw(plan, inp, batch=3) == -4
+        assert _raw(plan, inp, scale=float("nan")) == -5
+        assert _raw(plan, inp, scale=float("inf")) == -5
+        assert plan.set_nsplit(0) is None
+        with pytest.raises(mb.MlaVerifyError):
+            plan.set_nsplit(33)
+        torch.cuda.synchronize()
+        assert plan.get_error() == 0
+
+
+def test_slot_out_of_range_is_masked_and_reported():
+    """A prefix key whose slot lies outside the cache is masked: the result
+    equals the oracle on the request with that key removed."""
+    inp = _case(seed=2)
+    bad = inp.kv_indices.clone()
+    bad[5] = 2048                       # request 0, prefix key 5: one past the cache
+    bad[204 + 46] = -7                  # request 1, prefix key 46: negative
+    import dataclasses
+    binp = dataclasses.replace(inp, kv_indices=bad)
+    with G.make_plan(binp) as plan:
+        out, lse = G.run(plan, binp)
+        assert plan.get_error() & mb.DEV_BAD_SLOT
+        assert plan.get_error() == 0    # cleared by the previous read
+    keep = torch.ones(inp.kv_indices.numel(), dtype=torch.bool)
+    keep[5] = False
+    keep[204 + 46] = False
+    cpu = W.make_inputs(inp.workload)
+    ref_inp = dataclasses.replace(
+        cpu, kv_indices=cpu.kv_indices[keep],
+        kv_lens=cpu.kv_lens - 1,
+        kv_indptr=torch.tensor([0, 203, 203 + 103], dtype=torch.int32))
+    ref_o, ref_l = G.oracle_full(ref_inp)
+    G.assert_parity(out.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+
+
+def test_bad_parent_is_reported_and_treated_as_root():
+    inp = _case(seed=3, tree="chain")
+    par = inp.draft_parent.clone()
+    par[0, 2] = 2          # self-parent: not an earlier draft
+    import dataclasses
+    binp = dataclasses.replace(inp, draft_parent=par)
+    star_par = par.clone()
+    star_par[0, 2] = -1
+    sinp = dataclasses.replace(inp, draft_parent=star_par)
+    with G.make_plan(binp) as plan:
+        o1, l1 = G.run(plan, binp)
+        assert plan.get_error() & mb.DEV_BAD_PARENT
+        o2, l2 = G.run(plan, sinp)
+        assert plan.get_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("nsplit", [1, 3])
+def test_bad_length_gives_nan_request_and_flag(nsplit):
+    inp = _case(seed=4)
+    lens = inp.kv_lens.clone()
+    lens[1] = 2            # fewer rows than drafts
+    import dataclasses
+    binp = dataclasses.replace(inp, kv_lens=lens)
+    with G.make_plan(inp, nsplit=nsplit) as plan:
+        out, lse = G.run(plan, binp)
+        assert plan.get_error() & (mb.DEV_BAD_LEN | mb.DEV_BAD_INDPTR)
+        good_o, good_l = G.run(plan, inp)
+    assert torch.isnan(out[1]).all() and torch.isnan(lse[1]).all()
+    assert torch.equal(out[0], good_o[0]) and torch.equal(lse[0], good_l[0])
+
+
+def test_indptr_mismatch_is_reported():
+    inp = _case(seed=5)
+    ip = inp.kv_indptr.clone()
+    ip[1] -= 1
+    import dataclasses
+    binp = dataclasses.replace(inp, kv_indptr=ip)
+    with G.make_plan(inp) as plan:
+        out, lse = G.run(plan, binp)
+        assert plan.get_error() & mb.DEV_BAD_INDPTR
+    assert torch.isnan(out).all()
+
+
+def test_host_entry_point_matches_device_entry_point():
+    inp = _case(seed=6)
+    with G.make_plan(inp) as plan:
+        o_dev, l_dev = G.run(plan, inp)
+        B = inp.q.shape[0]
+        out = torch.empty((B, 4, 16, 512), dtype=torch.float32).pin_memory()
+        lse = torch.empty((B, 4, 16), dtype=torch.float32).pin_memory()
+        mb.mla_verify_attn_host(plan, inp.q.cpu().pin_memory(), inp.kv_cache,
+                                inp.kv_indices.cpu().pin_memory(), inp.kv_indptr.cpu(),
+                                inp.kv_lens.cpu(), inp.draft_parent.cpu(), inp.scale, out, lse)
+    assert torch.equal(out, o_dev.cpu()) and torch.equal(lse, l_dev.cpu())

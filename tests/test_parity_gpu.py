@@ -1,0 +1,143 @@
+"""GPU parity of the verify attention against the fp64 oracle, through the C ABI.
+
+Small cases (several 64-row tiles, several 64-key blocks, ragged tails) are
+compared element by element; the full-size workloads, in the launch
+configuration the benchmark times, are compared on sampled query rows.
+Tolerances: out max abs 1e-2 and mean abs 1e-3, lse max abs 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+from paged_mla_speculative_gb300 import workloads as W
+from tests import gpu_util as G
+from tests.conftest import bits
+
+pytestmark = pytest.mark.gpu
+
+
+def small(**kw):
+    base = dict(name="s", batch=2, num_drafts=4, num_heads=16, prefix=(300, 77),
+                tree="random", num_slots=4096, spike_frac=0.01, seed=100)
+    base.update(kw)
+    return W.Workload(**base)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_mla_speculative_gb300 import build
+    build.build()
+
+
+def check_full(inp, **plan_kw):
+    g = G.to_cuda(inp)
+    with G.make_plan(g, **plan_kw) as plan:
+        out, lse = G.run(plan, g)
+        assert plan.get_error() == 0
+    ref_o, ref_l = G.oracle_full(inp)
+    return G.assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+
+
+def test_tiny_workload_elementwise():
+    check_full(W.make_inputs(W.WORKLOADS["tiny"]))
+
+
+@pytest.mark.parametrize("T,H", [(1, 64), (2, 16), (4, 16), (8, 64), (16, 64), (3, 5), (32, 2)])
+def test_shapes_T_H(T, H):
+    w = small(num_drafts=T, num_heads=H, prefix=(130, 64), seed=200 + T * 7 + H)
+    check_full(W.make_inputs(w))
+
+
+@pytest.mark.parametrize("prefix", [(0, 1), (63, 64), (65, 127), (128, 0), (1000, 5)])
+@pytest.mark.parametrize("ps", [1, 64])
+def test_prefix_edges_and_page_sizes(prefix, ps):
+    w = small(prefix=prefix, page_size=ps, tree="chain", seed=300 + sum(prefix) + ps)
+    check_full(W.make_inputs(w))
+
+
+@pytest.mark.parametrize("nsplit", [1, 2, 3, 5, 32])
+def test_split_counts(nsplit):
+    # 32 splits over ~7 key blocks leaves most splits empty: weight 0.
+    w = small(prefix=(400, 33), seed=400 + nsplit)
+    check_full(W.make_inputs(w), nsplit=nsplit)
+
+
+@pytest.mark.parametrize("tree", ["chain", "star", "random"])
+def test_tree_shapes(tree):
+    w = small(num_drafts=16, num_heads=8, tree=tree, prefix=(200, 90), seed=500)
+    check_full(W.make_inputs(w))
+
+
+def test_ragged_small_batch():
+    w = small(batch=5, prefix=(1, 700, 64, 0, 333), num_drafts=8, num_heads=16, seed=600)
+    check_full(W.make_inputs(w))
+
+
+def test_bf16_output_is_the_rounded_fp32_output():
+    inp = G.to_cuda(W.make_inputs(small(seed=700)))
+    for ns in (1, 3):
+        with G.make_plan(inp, nsplit=ns) as p32, G.make_plan(inp, torch.bfloat16, nsplit=ns) as p16:
+            o32, l32 = G.run(p32, inp)
+            o16, l16 = G.run(p16, inp)
+        assert torch.equal(o32.to(torch.bfloat16), o16)
+        assert torch.equal(l32, l16)
+
+
+def test_slot_permutation_gives_identical_bits():
+    a = W.make_inputs(small(seed=800, num_slots=2048))
+    perm = torch.randperm(2048, generator=torch.Generator().manual_seed(9))
+    b_cache = torch.full_like(a.kv_cache, float("nan"))
+    b_cache[perm] = a.kv_cache
+    import dataclasses
+    b = dataclasses.replace(a, kv_cache=b_cache, kv_indices=perm[a.kv_indices.long()].to(torch.int32))
+    ga, gb = G.to_cuda(a), G.to_cuda(b)
+    with G.make_plan(ga) as plan:
+        oa, la = G.run(plan, ga)
+        ob, lb = G.run(plan, gb)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_page_size_64_matches_page_size_1_bits():
+    """Same logical rows through a page table and through a slot table."""
+    a = W.make_inputs(small(seed=900, page_size=64, num_slots=4096))
+    n = a.kv_lens.tolist()
+    slots = []
+    for bb in range(2):
+        pages = a.kv_indices[a.kv_indptr[bb]:a.kv_indptr[bb + 1]].long()
+        j = torch.arange(n[bb])
+        slots.append(pages[j // 64] * 64 + j % 64)
+    import dataclasses
+    b = dataclasses.replace(
+        a, page_size=1, kv_indices=torch.cat(slots).to(torch.int32),
+        kv_indptr=torch.tensor([0, n[0], n[0] + n[1]], dtype=torch.int32))
+    ga, gb = G.to_cuda(a), G.to_cuda(b)
+    with G.make_plan(ga) as pa, G.make_plan(gb) as pb:
+        oa, la = G.run(pa, ga)
+        ob, lb = G.run(pb, gb)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+# ------------------------------------------------------------ full size
+FULL = ["decode_batch", "tree", "sweep_p1024", "sweep_p4096", "sweep_p16384", "sweep_p65536",
+        "sweep_p93184", "ragged_ps1", "ragged_ps64"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(name):
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, device="cuda")
+    with G.make_plan(inp) as plan:
+        out, lse = G.run(plan, inp)
+        assert plan.get_error() == 0
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    assert np.isfinite(o).all() and np.isfinite(l).all()
+    rows = G.sample_rows(inp, per_request=3 if w.batch > 8 else 6, seed=1)
+    if w.batch > 8:
+        rows = [r for r in rows if r[0] % 8 == 0]   # a quarter of the requests
+    ref_o, ref_l = G.oracle_rows(inp, rows)
+    got_o = np.stack([o[b, t, h] for b, t, h in rows])
+    got_l = np.array([l[b, t, h] for b, t, h in rows])
+    G.assert_parity(got_o, got_l, ref_o, ref_l, name)
