@@ -100,7 +100,7 @@ typedef struct mla_verify_plan mla_verify_plan;
 /*
  * Create a plan for calls with batch <= max_batch on CUDA device `device`.
  * num_drafts (T) in [1, 32]; num_heads (H) >= 1 with T*H <= 4096;
- * page_size 1 or 64; num_slots >= 1 (a multiple of 64 when page_size is 64);
+ * page_size 1 or 64; 1 <= num_slots < 2^31 (a multiple of 64 when page_size is 64);
  * 1 <= max_kv_len; out_dtype MLA_VERIFY_OUT_F32 or _BF16.
  * Allocates all device memory the plan will ever use (cudaMalloc) and sets
  * kernel attributes; makes `device` current on the calling thread.

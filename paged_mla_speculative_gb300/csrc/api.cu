@@ -125,7 +125,7 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   *out = nullptr;
   if (max_batch < 1 || num_drafts < 1 || num_drafts > mlav::MAX_T || num_heads < 1 ||
       static_cast<long long>(num_drafts) * num_heads > 4096 ||
-      (page_size != 1 && page_size != mlav::PAGE) || num_slots < 1 ||
+      (page_size != 1 && page_size != mlav::PAGE) || num_slots < 1 || num_slots > INT32_MAX ||
       (page_size == mlav::PAGE && num_slots % mlav::PAGE) || max_kv_len < num_drafts ||
       (out_dtype != MLA_VERIFY_OUT_F32 && out_dtype != MLA_VERIFY_OUT_BF16))
     return MLA_VERIFY_ERR_SHAPE;

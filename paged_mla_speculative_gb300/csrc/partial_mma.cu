@@ -37,8 +37,8 @@ constexpr int OFF_KV0 = SMEM_Q;
 constexpr int OFF_KV1 = OFF_KV0 + SMEM_KV;
 constexpr int OFF_P = OFF_KV1 + SMEM_KV;
 constexpr int OFF_RED = OFF_P + SMEM_P;          // float [2][64]: block max / row sums
-constexpr int OFF_OK = OFF_RED + 2 * 64 * 4;      // uint8 [2][64]: key loaded and in range
-constexpr int OFF_MASK = OFF_OK + 2 * 64;         // uint32 [32]: ancestor masks
+constexpr int OFF_SLOT = OFF_RED + 2 * 64 * 4;    // int32 [3][64]: slot of each key, -1 if none
+constexpr int OFF_MASK = OFF_SLOT + 3 * 64 * 4;   // uint32 [32]: ancestor masks
 constexpr int SMEM_TOTAL = OFF_MASK + MAX_T * 4;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 
@@ -100,21 +100,27 @@ __device__ __forceinline__ void widen_tile(uint8_t* tile, int rows, int tid) {
   }
 }
 
-__device__ __forceinline__ void load_kv_block(const Params& p, const Request& rq, int kb,
-                                              uint8_t* stage, uint8_t* ok_flags, int tid) {
+// Slot of key r of block kb, or -1 past the end of the request or when the
+// table points outside the cache (reported).
+__device__ __forceinline__ int block_slot(const Params& p, const Request& rq, int kb, int r) {
+  const int j = kb * BN + r;
+  if (j >= rq.n) return -1;
+  const long long s = key_slot(p, rq.ip0, j);
+  if (s < 0) atomicOr(p.err, ERR_SLOT);
+  return static_cast<int>(s);
+}
+
+// Gather the 64 rows of one key block into a stage with 16-byte cp.async
+// vectors; rows without a slot are zero-filled.
+__device__ __forceinline__ void load_kv_block(const Params& p, const int* slots, uint8_t* stage,
+                                              int tid) {
   const uint32_t base = smem_u32(stage);
-#pragma unroll 1
+#pragma unroll 2
   for (int c = tid; c < BN * ROW_CHUNKS; c += NTHREADS) {
     const int r = c / ROW_CHUNKS;
     const int ch = c - r * ROW_CHUNKS;
-    const int j = kb * BN + r;
-    long long slot = -1;
-    if (j < rq.n) slot = key_slot(p, rq.ip0, j);
-    if (ch == 0) {
-      ok_flags[r] = slot >= 0;
-      if (j < rq.n && slot < 0) atomicOr(p.err, ERR_SLOT);
-    }
-    const uint16_t* src = slot >= 0 ? p.kv + slot * D_QK + ch * 8 : p.kv;
+    const int slot = slots[r];
+    const uint16_t* src = slot >= 0 ? p.kv + static_cast<long long>(slot) * D_QK + ch * 8 : p.kv;
     cp_async16(base + sw_row(r, ch), src, slot >= 0 ? 16 : 0);
   }
 }
@@ -128,7 +134,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
   const int row0 = rt * BM;
 
   float* s_red = reinterpret_cast<float*>(smem + OFF_RED);
-  uint8_t* s_ok = smem + OFF_OK;
+  int* s_slot = reinterpret_cast<int*>(smem + OFF_SLOT);
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
 
   const Request rq = load_request(p, b);
@@ -167,6 +173,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
   const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * nblk) / p.nsplit);
 
   if (tid < p.T) s_mask[tid] = ancestor_mask(p.draft_parent + b * p.T, tid, p.err);
+  // Slots of the first two blocks; later blocks' slots are fetched one
+  // iteration ahead so the gather never waits on an index load.
+  if (tid < BN && kb1 > kb0) {
+    s_slot[tid] = block_slot(p, rq, kb0, tid);
+    if (kb0 + 1 < kb1) s_slot[BN + tid] = block_slot(p, rq, kb0 + 1, tid);
+  }
+  __syncthreads();
 
   // Q tile: rows beyond R are zero.
   if (kb1 > kb0) {
@@ -181,7 +194,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
                  in ? 16 : 0);
     }
     cp_async_commit();
-    load_kv_block(p, rq, kb0, smem + OFF_KV0, s_ok, tid);
+    load_kv_block(p, s_slot, smem + OFF_KV0, tid);
     cp_async_commit();
   }
 
@@ -199,10 +212,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
 
 #pragma unroll 1
   for (int kb = kb0; kb < kb1; ++kb) {
-    const int st = (kb - kb0) & 1;
+    const int it = kb - kb0;
+    const int st = it & 1;
+    const int ring = it % 3;
     uint8_t* stage = smem + (st ? OFF_KV1 : OFF_KV0);
+    int pending = -1;
+    if (tid < BN && kb + 2 < kb1) pending = block_slot(p, rq, kb + 2, tid);
     if (kb + 1 < kb1) {
-      load_kv_block(p, rq, kb + 1, smem + (st ? OFF_KV0 : OFF_KV1), s_ok + (st ^ 1) * 64, tid);
+      load_kv_block(p, s_slot + ((it + 1) % 3) * BN, smem + (st ? OFF_KV0 : OFF_KV1), tid);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
@@ -238,7 +255,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
     }
 
     // ---- mask, scale to base 2, block max.
-    const uint8_t* ok = s_ok + st * 64;
+    const int* ok = s_slot + ring * BN;
     float bmA = -INFINITY, bmB = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -247,7 +264,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
         const int kl = half * 32 + nt * 8 + 2 * (lane & 3) + (e & 1);
         const int j = kb * BN + kl;
         const int t = (e < 2) ? tA : tB;
-        bool vis = ok[kl] && t >= 0;
+        bool vis = ok[kl] >= 0 && t >= 0;
         if (vis && j >= rq.P) vis = (s_mask[t] >> (j - rq.P)) & 1u;
         const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
         s[nt][e] = v;
@@ -323,6 +340,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
         }
       }
     }
+    if (tid < BN && kb + 2 < kb1) s_slot[((it + 2) % 3) * BN + tid] = pending;
     __syncthreads();
   }
 
