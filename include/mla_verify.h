@@ -86,6 +86,7 @@ extern "C" {
 #define MLA_VERIFY_DEV_BAD_PARENT     4   /* draft_parent[i] not in {-1} U [0, i)  */
 #define MLA_VERIFY_DEV_BAD_INDPTR     8   /* indptr range does not match kv_len    */
 #define MLA_VERIFY_DEV_TIMEOUT       16   /* a bounded device wait gave up         */
+#define MLA_VERIFY_DEV_INTERNAL      32   /* an internal layout invariant failed   */
 
 /* Output element type. */
 #define MLA_VERIFY_OUT_F32            0
@@ -94,6 +95,7 @@ extern "C" {
 /* Kernel family for the partial (split-KV) step. */
 #define MLA_VERIFY_KERNEL_AUTO        0
 #define MLA_VERIFY_KERNEL_MMA         1   /* warp-level mma.sync, O in registers   */
+#define MLA_VERIFY_KERNEL_TC          2   /* tcgen05 MMAs, O^T in tensor memory    */
 
 typedef struct mla_verify_plan mla_verify_plan;
 
@@ -116,7 +118,8 @@ void mla_verify_plan_destroy(mla_verify_plan* plan);
 /*
  * Fix the split count used by later calls (1..MLA_VERIFY_MAX_NSPLIT), or 0
  * to choose it from the batch, the plan's max_kv_len and the SM count.
- * A count above the number of 64-key blocks in max_kv_len is clamped to it.
+ * A count above the number of key blocks in max_kv_len (64 keys for the
+ * MMA family, 128 for the TC family) is clamped to it.
  * A call whose batch x split count exceeds the workspace the plan sized
  * (the automatic choice at every batch, or at least 64 MB) returns
  * MLA_VERIFY_ERR_SHAPE.
@@ -127,7 +130,7 @@ int mla_verify_plan_set_nsplit(mla_verify_plan* plan, int nsplit);
 /* The split count a call with `batch` requests will use (>= 1), or < 0. */
 int mla_verify_plan_get_nsplit(const mla_verify_plan* plan, int batch);
 
-/* Select the partial-kernel family (MLA_VERIFY_KERNEL_*). */
+/* Select the partial-kernel family (MLA_VERIFY_KERNEL_*; AUTO = TC). */
 int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
 
 /*

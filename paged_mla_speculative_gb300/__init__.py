@@ -8,6 +8,7 @@ synthetic-input generator (``workloads.py``).
 from .binding import (  # noqa: F401
     KERNEL_AUTO,
     KERNEL_MMA,
+    KERNEL_TC,
     OUT_BF16,
     OUT_F32,
     MlaVerifyError,

@@ -21,6 +21,7 @@ OUT_F32 = 0
 OUT_BF16 = 1
 KERNEL_AUTO = 0
 KERNEL_MMA = 1
+KERNEL_TC = 2
 MAX_NSPLIT = 32
 
 DEV_BAD_SLOT = 1
@@ -28,6 +29,7 @@ DEV_BAD_LEN = 2
 DEV_BAD_PARENT = 4
 DEV_BAD_INDPTR = 8
 DEV_TIMEOUT = 16
+DEV_INTERNAL = 32
 
 STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_ALIGN", -3: "ERR_SHAPE", -4: "ERR_BATCH",
           -5: "ERR_SCALE", -6: "ERR_CUDA", -7: "ERR_DEVICE", -8: "ERR_OOM", -9: "ERR_ARG"}

@@ -46,16 +46,18 @@ struct mla_verify_plan {
 namespace {
 
 constexpr int kRowsPerTile = 64;
-constexpr int kKeysPerBlock = 64;
+
+// Keys per block of the partial kernel the plan runs.
+int keys_per_block(int kernel) { return kernel == MLA_VERIFY_KERNEL_MMA ? 64 : 128; }
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 // Split count for `batch` requests: minimise (waves of CTAs) x (key blocks
 // per CTA) plus the cost of moving the split partials through the combine,
 // in units of one CTA key-block step.
-int auto_nsplit(const mla_verify_plan* pl, int batch) {
+int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel) {
   const long long units = static_cast<long long>(batch) * ceil_div(pl->R, kRowsPerTile);
-  const long long max_blocks = ceil_div(pl->max_kv_len, kKeysPerBlock);
+  const long long max_blocks = ceil_div(pl->max_kv_len, keys_per_block(kernel));
   const int cap = static_cast<int>(std::min<long long>(mlav::MAX_NSPLIT, max_blocks));
   // Bytes one CTA block-step is worth (about 2 us of HBM time at 6 TB/s).
   const double bytes_per_step = 12e6;
@@ -77,8 +79,9 @@ int auto_nsplit(const mla_verify_plan* pl, int batch) {
 
 // Forced counts are clamped to the number of key blocks of max_kv_len.
 int effective_nsplit(const mla_verify_plan* pl, int batch) {
-  if (!pl->forced_nsplit) return auto_nsplit(pl, batch);
-  return static_cast<int>(std::min<long long>(pl->forced_nsplit, ceil_div(pl->max_kv_len, kKeysPerBlock)));
+  if (!pl->forced_nsplit) return auto_nsplit(pl, batch, pl->kernel);
+  return static_cast<int>(std::min<long long>(
+      pl->forced_nsplit, ceil_div(pl->max_kv_len, keys_per_block(pl->kernel))));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -133,7 +136,8 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
-  if (mlav::partial_mma_prepare() != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (mlav::partial_mma_prepare() != cudaSuccess || mlav::partial_tc_prepare() != cudaSuccess)
+    return MLA_VERIFY_ERR_CUDA;
 
   mla_verify_plan* pl = new (std::nothrow) mla_verify_plan();
   if (!pl) return MLA_VERIFY_ERR_OOM;
@@ -147,13 +151,15 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   pl->max_kv_len = max_kv_len;
   pl->out_dtype = out_dtype;
   pl->num_sms = sms;
-  pl->kernel = MLA_VERIFY_KERNEL_AUTO;
+  pl->kernel = MLA_VERIFY_KERNEL_TC;
 
   // Workspace capacity in request-splits: enough for the automatic choice at
   // every batch size, and for forced split counts up to a 64 MB floor.
-  const long long max_blocks = ceil_div(max_kv_len, kKeysPerBlock);
+  const long long max_blocks = ceil_div(max_kv_len, 64);
   long long cap = 0;
-  for (int b = 1; b <= max_batch; ++b) cap = std::max<long long>(cap, 1LL * b * auto_nsplit(pl, b));
+  for (int b = 1; b <= max_batch; ++b)
+    for (int k : {MLA_VERIFY_KERNEL_MMA, MLA_VERIFY_KERNEL_TC})
+      cap = std::max<long long>(cap, 1LL * b * auto_nsplit(pl, b, k));
   const long long floor_rs = (64LL << 20) / (1LL * pl->R * (mlav::D_V + 1) * 4);
   cap = std::max(cap, std::min(1LL * max_batch * std::min<long long>(mlav::MAX_NSPLIT, max_blocks),
                                std::max(floor_rs, std::min<long long>(mlav::MAX_NSPLIT, max_blocks))));
@@ -216,8 +222,10 @@ int mla_verify_plan_get_nsplit(const mla_verify_plan* pl, int batch) {
 
 int mla_verify_plan_set_kernel(mla_verify_plan* pl, int kernel) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
-  if (kernel != MLA_VERIFY_KERNEL_AUTO && kernel != MLA_VERIFY_KERNEL_MMA) return MLA_VERIFY_ERR_ARG;
-  pl->kernel = kernel;
+  if (kernel != MLA_VERIFY_KERNEL_AUTO && kernel != MLA_VERIFY_KERNEL_MMA &&
+      kernel != MLA_VERIFY_KERNEL_TC)
+    return MLA_VERIFY_ERR_ARG;
+  pl->kernel = kernel == MLA_VERIFY_KERNEL_AUTO ? MLA_VERIFY_KERNEL_TC : kernel;
   return MLA_VERIFY_OK;
 }
 
@@ -270,7 +278,9 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   p.err = pl->err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mlav::launch_partial_mma(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  const cudaError_t le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
+                                                             : mlav::launch_partial_tc(p, s);
+  if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   if (pl->profile_event && cudaEventRecord(pl->profile_event, s) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
   if (ns > 1 && mlav::launch_combine(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;

@@ -21,6 +21,7 @@ enum : int {
   ERR_PARENT = 4,
   ERR_INDPTR = 8,
   ERR_TIMEOUT = 16,
+  ERR_INTERNAL = 32,
 };
 
 // Arguments of one verify call, shared by every kernel of the call.

@@ -12,6 +12,10 @@ int partial_mma_smem_bytes();
 cudaError_t partial_mma_prepare();
 cudaError_t launch_partial_mma(const Params& p, cudaStream_t stream);
 
+// Split-KV partial kernel on tcgen05 tensor cores with TMEM accumulators.
+cudaError_t partial_tc_prepare();
+cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream);
+
 // LSE combine of the split partials into out/lse.
 cudaError_t launch_combine(const Params& p, cudaStream_t stream);
 

@@ -22,11 +22,12 @@ def to_cuda(inp: W.VerifyInputs) -> W.VerifyInputs:
 
 
 def make_plan(inp: W.VerifyInputs, out_dtype=torch.float32, nsplit=0, max_kv_len=None,
-              max_batch=None):
+              max_batch=None, kernel=mb.KERNEL_AUTO):
     w = inp.workload
     mk = max_kv_len or max(int(x) for x in inp.kv_lens.tolist())
     plan = mb.Plan(max_batch or w.batch, w.num_drafts, w.num_heads, inp.page_size,
                    inp.kv_cache.shape[0], mk, out_dtype)
+    plan.set_kernel(kernel)
     if nsplit:
         plan.set_nsplit(nsplit)
     return plan

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+from paged_mla_speculative_gb300 import binding as mb
 from paged_mla_speculative_gb300 import workloads as W
 from tests import gpu_util as G
 from tests.conftest import bits
@@ -40,8 +41,27 @@ def check_full(inp, **plan_kw):
     return G.assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
 
 
-def test_tiny_workload_elementwise():
-    check_full(W.make_inputs(W.WORKLOADS["tiny"]))
+KERNELS = [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_MMA, id="mma")]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_tiny_workload_elementwise(kernel):
+    check_full(W.make_inputs(W.WORKLOADS["tiny"]), kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("nsplit", [1, 3])
+def test_kernel_families_small_ragged(kernel, nsplit):
+    w = small(batch=3, prefix=(700, 129, 0), num_drafts=8, num_heads=16, seed=150)
+    check_full(W.make_inputs(w), kernel=kernel, nsplit=nsplit)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_kernel_families_spiky_long(kernel):
+    """Spiky keys (1% x8) over a few thousand keys: the precision case."""
+    w = small(batch=2, prefix=(3000, 2500), num_drafts=8, num_heads=64, tree="chain",
+              num_slots=8192, spike_frac=0.01, seed=160)
+    check_full(W.make_inputs(w), kernel=kernel)
 
 
 @pytest.mark.parametrize("T,H", [(1, 64), (2, 16), (4, 16), (8, 64), (16, 64), (3, 5), (32, 2)])
@@ -128,7 +148,7 @@ FULL = ["decode_batch", "tree", "sweep_p1024", "sweep_p4096", "sweep_p16384", "s
 def test_full_size_sampled_rows(name):
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w, device="cuda")
-    with G.make_plan(inp) as plan:
+    with G.make_plan(inp) as plan:   # the automatic configuration the benchmark times
         out, lse = G.run(plan, inp)
         assert plan.get_error() == 0
     o = out.float().cpu().numpy()
