@@ -12,8 +12,10 @@
 // rows = 256 columns) and S^T in another 64 columns.  With one thread per
 // key, the softmax reduces each query row across the 128 TMEM lanes
 // (redux.sync per warp, shared memory across the four warps).  The running
-// max of a row is only moved when a block's max exceeds it by more than 2^8
-// (then O^T and the row sums are rescaled), so P = 2^(s - m) <= 256 fits fp16.
+// row max is exact (P <= 1, and the key holding the max has P = 1 exactly):
+// a lazily moved max would round the dominant key's weight to fp16 too, which
+// measurably doubles the worst-case output error on spiky keys.  O^T columns
+// are rescaled in TMEM only for the 32-row groups whose max moved.
 //
 // Per 128-key block:
 //   A. gather the 128 scattered 1152-byte rows with 16-byte cp.async vectors
@@ -22,7 +24,7 @@
 //   C. warps 0-3: softmax of S^T, P^T as fp16 into the (now unused) rope
 //      chunk tile; warps 4-7: widen the value chunks 0-7 to fp16 in place
 //      (P in bf16 would cost more than the 1e-2 output tolerance allows);
-//   D. if a row max moved, rescale that column of O^T in TMEM;
+//   D. rescale the O^T columns of the 32-row groups whose max moved;
 //   E. one thread issues the 32 O^T MMAs (fp16 operands).
 // The next block's slots are read and its rows prefetched into L2 while the
 // tensor core runs step B.
@@ -52,7 +54,7 @@ constexpr int OFF_SLOT = OFF_L + 64 * 4;        // int [2][128] slots of this / 
 constexpr int OFF_MASK = OFF_SLOT + 2 * BN * 4; // uint32 [32] ancestor masks
 constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -1 past R
 constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [2]: S^T done, O^T done
-constexpr int OFF_MISC = OFF_MBAR + 16;         // uint32 tmem base, int rescale flag
+constexpr int OFF_MISC = OFF_MBAR + 16;         // uint32 tmem base, int rescale flags [2]
 constexpr int SMEM_TOTAL = OFF_MISC + 16;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -60,7 +62,6 @@ static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t TM_S = 256;                  // S^T columns; O^T tile d at d * 64
 constexpr long long WAIT_LIMIT = 1LL << 31;     // cycles before a wait gives up
-constexpr float RESCALE_THRESHOLD = 8.f;        // log2 of the largest P allowed
 
 constexpr uint32_t IDESC_S = tc::idesc_f16(128, BM, 1, 0, 0);   // bf16, both K-major
 constexpr uint32_t IDESC_O = tc::idesc_f16(128, BM, 0, 1, 1);   // fp16, both MN-major
@@ -159,7 +160,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     tc::mbar_init(mbar_s, 1);
     tc::mbar_init(mbar_o, 1);
     tc::mbar_fence_init();
-    *s_flag = 0;
+    s_flag[0] = 0;
+    s_flag[1] = 0;
   }
   if (warp == 0) tc::tmem_alloc<TMEM_COLS>(smem_u32(s_tmem));
   tc::fence_before_sync();
@@ -279,13 +281,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
                                fmaxf(s_red[2 * BM + tid], s_red[3 * BM + tid]));
         const float old = s_mref[tid];
         float alpha = 1.f;
-        if (bm != -INFINITY) {
-          if (old == -INFINITY) {
-            s_mref[tid] = bm;
-          } else if (bm > old + RESCALE_THRESHOLD) {
-            s_mref[tid] = bm;
+        if (bm > old) {
+          s_mref[tid] = bm;
+          if (old != -INFINITY) {
             alpha = ex2(old - bm);
-            *s_flag = 1;
+            s_flag[tid >> 5] = 1;
           }
         }
         s_alpha[tid] = alpha;
@@ -326,14 +326,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     __syncthreads();
     tc::fence_after_sync();
 
-    // ---- D. rescale the O^T columns whose row max moved.
-    const bool rescale = *s_flag != 0;
-    if (rescale) {
+    // ---- D. rescale the O^T columns of the row groups whose max moved.
+    const bool rescale0 = s_flag[0] != 0, rescale1 = s_flag[1] != 0;
+    if (rescale0 || rescale1) {
       const int d0 = (warp >> 2) * 2;   // warps 0-3: tiles 0,1; warps 4-7: tiles 2,3
 #pragma unroll 1
       for (int d = d0; d < d0 + 2; ++d) {
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
+          if (!(h ? rescale1 : rescale0)) continue;
           const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + h * 32;
           uint32_t v[32];
           tc::tmem_ld32(ta, v);
@@ -349,7 +350,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (tid == 0) *s_flag = 0;
+    if (tid == 0) {
+      s_flag[0] = 0;
+      s_flag[1] = 0;
+    }
 
     // ---- E. O^T += V^T P^T, issued by one thread.
     if (tid == 0) {
