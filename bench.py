@@ -62,7 +62,7 @@ def load_peaks():
 def kernel_source_hash():
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "paged_mla_speculative_gb300", "csrc")
-    for name in ("common.cuh", "partial_mma.cu"):
+    for name in ("common.cuh", "tc_ptx.cuh", "partial_tc.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -77,7 +77,7 @@ def profiled_traffic(workload):
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d.get("partial_mma_kernel", {})
+        e = d.get("partial_tc_kernel", {})
         if e.get("source_sha1") == kernel_source_hash() and e.get("workload") == workload:
             return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -405,7 +405,7 @@ def run_gb300(args):
         "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": mean_call,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded), bf16 inputs resident in HBM",
-        "config": config_of(w, {"nsplit": ns, "kernel": "partial_mma_kernel + combine_kernel"}),
+        "config": config_of(w, {"nsplit": ns, "kernel": "partial_tc_kernel + combine_kernel"}),
         "us_per_call_p10_p50_p90": [q[0] * 1e3, statistics.median(call_ms) * 1e3, q[-1] * 1e3],
         "partial_us": mean_part * 1e3, "combine_us": mean_comb * 1e3,
         "graph_replay_us_per_call": graph_us,
@@ -413,7 +413,7 @@ def run_gb300(args):
         "roofline_time_us": t_roof_us, "frac_of_roofline": t_roof_us / (mean_call * 1e3),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
-                     "kernel": "partial_mma_kernel",
+                     "kernel": "partial_tc_kernel",
                      "peak_source": f"{peak_src} bf16 burst (fp16 has the same tensor rate)"},
         "clocks": clocks, "gpu_launches": launches,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,

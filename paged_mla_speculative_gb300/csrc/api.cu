@@ -12,7 +12,7 @@
 #include <algorithm>
 #include <new>
 
-#include "../../include/mla_verify.h"
+#include "mla_verify.h"
 #include "kernels.h"
 
 using mlav::Params;

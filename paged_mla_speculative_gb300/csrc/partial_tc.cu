@@ -1,33 +1,40 @@
-// Split-KV partial kernel on the sm_103a tensor cores (tcgen05 + TMEM).
+// Split-KV partial kernel on the sm_103a tensor cores (tcgen05 + TMEM),
+// warp-specialised and pipelined.
 //
 // One CTA = one request b, one tile of 64 query rows (r = t*H + h), one key
 // split: the KV-split "partial" half of the partial + reduce design in "The
 // Decisive A/B: When Benchmarking Honesty Reveals the Real Bottleneck"
-// (sections "The Context" and "What This Reveals About the Bottleneck").
+// (sections "The Context" and "What This Reveals About the Bottleneck": KV
+// split for occupancy, 128-bit vector loads of scattered page_size=1 rows).
 //
 // The products are taken transposed so that every MMA has M = 128:
 //     S^T[key, row] = K_block[128 x 576] . Q_tile[64 x 576]^T          (bf16)
 //     O^T[dim, row] += V_block^T[512 x 128] . P^T[128 x 64]              (fp16)
 // O^T lives in tensor memory for the whole split (4 tiles of 128 dims x 64
-// rows = 256 columns) and S^T in another 64 columns.  With one thread per
-// key, the softmax reduces each query row across the 128 TMEM lanes
-// (redux.sync per warp, shared memory across the four warps).  The running
-// row max is exact (P <= 1, and the key holding the max has P = 1 exactly):
-// a lazily moved max would round the dominant key's weight to fp16 too, which
-// measurably doubles the worst-case output error on spiky keys.  O^T columns
-// are rescaled in TMEM only for the 32-row groups whose max moved.
+// rows = columns 0..255) and S^T in columns 256..319.  With one thread per
+// key the softmax reduces each query row across the 128 TMEM lanes
+// (redux.sync per warp, shared memory across four warps).  The running row
+// max is exact, so P <= 1 and the key holding the max has P = 1 exactly (a
+// lazily moved max would round the dominant key's weight too, which doubles
+// the worst-case output error on spiky keys); O^T columns are rescaled in
+// TMEM only for the 32-row groups whose max moved.  P is fp16 and the values
+// are widened to fp16 in shared memory, because P in bf16 costs more than the
+// 1e-2 output tolerance allows.
 //
-// Per 128-key block:
-//   A. gather the 128 scattered 1152-byte rows with 16-byte cp.async vectors
-//      into nine 128-byte-swizzled 16 KB chunk tiles (the MMA operand layout);
-//   B. one thread issues the 36 S^T MMAs (bf16 operands, fp32 in TMEM);
-//   C. warps 0-3: softmax of S^T, P^T as fp16 into the (now unused) rope
-//      chunk tile; warps 4-7: widen the value chunks 0-7 to fp16 in place
-//      (P in bf16 would cost more than the 1e-2 output tolerance allows);
-//   D. rescale the O^T columns of the 32-row groups whose max moved;
-//   E. one thread issues the 32 O^T MMAs (fp16 operands).
-// The next block's slots are read and its rows prefetched into L2 while the
-// tensor core runs step B.
+// Roles (13 warps):
+//   warps 0-7  softmax: one thread per (key of the block, half of the 64 query
+//              rows); warps w and w+4 share TMEM lane quadrant w;
+//   warps 8-11 loaders: gather the block's 128 scattered 1152-byte rows with
+//              16-byte cp.async vectors into nine 128-byte-swizzled 16 KB
+//              chunk tiles (the MMA operand layout), then widen the value
+//              chunks 0-7 to fp16 in place once S^T no longer reads them;
+//   warp 12    lane 0 issues the MMAs; the warp owns the TMEM allocation.
+// Pipeline over 128-key blocks k (mbarriers, all waits bounded):
+//   loaders:  chunk pair d of block k+1 is gathered as soon as O^T(k) tile d
+//             has finished with it; the rope chunk (which holds P^T(k)) last;
+//   MMA:      S^T(k) chunk pair by chunk pair as the pairs land, then, once
+//             softmax(k) and the widening are done, O^T(k) tile by tile;
+//   softmax:  after S^T(k): mask, max, P^T(k) into the rope chunk tile.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -40,7 +47,10 @@ namespace {
 
 constexpr int BM = 64;          // query rows per CTA: MMA N
 constexpr int BN = 128;         // keys per block: MMA M of S^T
-constexpr int NTHREADS = 256;
+constexpr int NWARPS = 13;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int LOADER_WARP0 = 8, MMA_WARP = 12;
+constexpr int HALF = BM / 2;    // query-row columns per softmax thread
 constexpr int Q_CHUNK = BM * 128;   // one 64-dim chunk of the Q tile
 constexpr int KV_CHUNK = BN * 128;  // one 64-dim chunk of the key block
 constexpr int OFF_Q = 0;
@@ -53,11 +63,18 @@ constexpr int OFF_L = OFF_ALPHA + 64 * 4;       // float [64] final row sums
 constexpr int OFF_SLOT = OFF_L + 64 * 4;        // int [2][128] slots of this / next block
 constexpr int OFF_MASK = OFF_SLOT + 2 * BN * 4; // uint32 [32] ancestor masks
 constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -1 past R
-constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [2]: S^T done, O^T done
-constexpr int OFF_MISC = OFF_MBAR + 16;         // uint32 tmem base, int rescale flags [2]
+constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [16] mbarriers
+constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, rescale flags [2], abort flag
 constexpr int SMEM_TOTAL = OFF_MISC + 16;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+// mbarrier indices
+constexpr int MB_CHUNK = 0;   // [5] chunk pairs 0..3 and the rope chunk landed (count 128)
+constexpr int MB_S = 5;       // S^T done (tcgen05.commit)
+constexpr int MB_P = 6;       // P^T written, O^T rescaled (count 256)
+constexpr int MB_CONV = 7;    // values widened to fp16 (count 128)
+constexpr int MB_OT = 8;      // [4] O^T tile d done (tcgen05.commit)
 
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t TM_S = 256;                  // S^T columns; O^T tile d at d * 64
@@ -70,20 +87,35 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int sr
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(src_bytes));
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
-__device__ __forceinline__ void named_sync_softmax() {
-  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+
+// Bounded wait; a timeout (or an earlier one anywhere in the CTA) sets the
+// abort flag so every later wait returns at once.
+__device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t parity, volatile int* abort,
+                                           int* err) {
+  if (tc::mbar_test(mbar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (tc::mbar_try(mbar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > WAIT_LIMIT) {
+      *abort = 1;
+      atomicOr(err, ERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // Slot of key r of 128-key block kb, or -1 past the end of the request or
-// when the table points outside the cache (reported).
-__device__ __forceinline__ int block_slot(const Params& p, const Request& rq, int kb, int r) {
+// when the table points outside the cache (reported when `report`).
+__device__ __forceinline__ int block_slot(const Params& p, const Request& rq, int kb, int r,
+                                          bool report) {
   const int j = kb * BN + r;
   if (j >= rq.n) return -1;
   const long long s = key_slot(p, rq.ip0, j);
-  if (s < 0) atomicOr(p.err, ERR_SLOT);
+  if (s < 0 && report) atomicOr(p.err, ERR_SLOT);
   return static_cast<int>(s);
 }
 
@@ -113,6 +145,36 @@ __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split
   }
 }
 
+// Loader: gather chunk group g of a key block (g < 4: value chunks 2g, 2g+1;
+// g == 4: the rope chunk 8) for the keys whose slots are given; rows without
+// a slot are zero-filled.  Two rows per warp instruction, 16 lanes per
+// 256-byte row segment.
+__device__ __forceinline__ void gather_group(const Params& p, const int* slots, uint32_t sbase,
+                                             int g, int li) {
+  if (g < 4) {
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int e = li + 128 * i;
+      const int j = e >> 4, gq = e & 15;
+      const int c = 2 * g + (gq >> 3), gr = gq & 7;
+      const int slot = slots[j];
+      cp_async16(sbase + OFF_KV + c * KV_CHUNK + j * 128 + ((gr ^ (j & 7)) << 4),
+                 slot >= 0 ? p.kv + static_cast<long long>(slot) * D_QK + c * 64 + gr * 8 : p.kv,
+                 slot >= 0 ? 16 : 0);
+    }
+  } else {
+#pragma unroll 4
+    for (int i = 0; i < 8; ++i) {
+      const int e = li + 128 * i;
+      const int j = e >> 3, gr = e & 7;
+      const int slot = slots[j];
+      cp_async16(sbase + OFF_KV + 8 * KV_CHUNK + j * 128 + ((gr ^ (j & 7)) << 4),
+                 slot >= 0 ? p.kv + static_cast<long long>(slot) * D_QK + 512 + gr * 8 : p.kv,
+                 slot >= 0 ? 16 : 0);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int split = blockIdx.x, rt = blockIdx.y, b = blockIdx.z;
@@ -128,10 +190,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
   int* s_tofr = reinterpret_cast<int*>(smem + OFF_TOFR);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* s_flag = reinterpret_cast<int*>(smem + OFF_MISC + 4);
-  const uint32_t mbar_s = smem_u32(smem + OFF_MBAR);
-  const uint32_t mbar_o = mbar_s + 8;
+  volatile int* s_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
   const uint32_t sbase = smem_u32(smem);
+  const uint32_t mbar0 = sbase + OFF_MBAR;
+  auto mbar = [&](int i) { return mbar0 + 8u * static_cast<uint32_t>(i); };
 
   const Request rq = load_request(p, b);
   if (!rq.ok) {
@@ -149,169 +212,73 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   const int nblk = (rq.n + BN - 1) / BN;
   const int kb0 = static_cast<int>((static_cast<long long>(split) * nblk) / p.nsplit);
   const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * nblk) / p.nsplit);
+  const int nb = kb1 - kb0;
 
   if (tid < p.T) s_mask[tid] = ancestor_mask(p.draft_parent + b * p.T, tid, p.err);
   if (tid < BM) {
     s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
     s_mref[tid] = -INFINITY;
   }
-  if (tid < BN && kb1 > kb0) s_slot[tid] = block_slot(p, rq, kb0, tid);
+  if (warp >= LOADER_WARP0 && warp < MMA_WARP && nb > 0) {
+    const int li = tid - LOADER_WARP0 * 32;
+    s_slot[li] = block_slot(p, rq, kb0, li, true);
+  }
   if (tid == 0) {
-    tc::mbar_init(mbar_s, 1);
-    tc::mbar_init(mbar_o, 1);
+    for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 128);
+    tc::mbar_init(mbar(MB_S), 1);
+    tc::mbar_init(mbar(MB_P), 256);
+    tc::mbar_init(mbar(MB_CONV), 128);
+    for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_OT + i), 1);
     tc::mbar_fence_init();
     s_flag[0] = 0;
     s_flag[1] = 0;
+    *s_abort = 0;
   }
-  if (warp == 0) tc::tmem_alloc<TMEM_COLS>(smem_u32(s_tmem));
+  if (warp == MMA_WARP) tc::tmem_alloc<TMEM_COLS>(smem_u32(s_tmem));
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
 
-  // Q tile: 64 rows x 9 swizzled chunks; rows beyond R are zero.
-  if (kb1 > kb0) {
-    const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
+  if (warp >= LOADER_WARP0 && warp < MMA_WARP) {
+    // =========================== loaders ===================================
+    const int li = tid - LOADER_WARP0 * 32;
+    if (nb > 0) {
+      // Q tile (64 rows x 9 chunks, rows beyond R zero) rides on group 0.
+      const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
 #pragma unroll 1
-    for (int e = tid; e < BM * ROW_CHUNKS; e += NTHREADS) {
-      const int r = e / ROW_CHUNKS, q = e - r * ROW_CHUNKS;
-      const int gr = row0 + r;
-      const bool in = gr < p.R;
-      cp_async16(sbase + OFF_Q + (q >> 3) * Q_CHUNK + r * 128 + (((q & 7) ^ (r & 7)) << 4),
-                 in ? qb + static_cast<size_t>(gr) * D_QK + q * 8 : p.q, in ? 16 : 0);
+      for (int e = li; e < BM * ROW_CHUNKS; e += 128) {
+        const int r = e / ROW_CHUNKS, q = e - r * ROW_CHUNKS;
+        const int gr = row0 + r;
+        const bool in = gr < p.R;
+        cp_async16(sbase + OFF_Q + (q >> 3) * Q_CHUNK + r * 128 + (((q & 7) ^ (r & 7)) << 4),
+                   in ? qb + static_cast<size_t>(gr) * D_QK + q * 8 : p.q, in ? 16 : 0);
+      }
+      for (int g = 0; g < 5; ++g) {
+        gather_group(p, s_slot, sbase, g, li);
+        tc::cp_async_arrive_noinc(mbar(MB_CHUNK + g));
+      }
     }
-  }
-
-  const bool all_rows = row0 + BM <= p.R;
-  const float scale2 = p.scale_log2;
-  float lpart[BM];   // softmax threads: this key's share of every row sum
-#pragma unroll
-  for (int c = 0; c < BM; ++c) lpart[c] = 0.f;
-  bool alive = true;
-
 #pragma unroll 1
-  for (int kb = kb0; kb < kb1; ++kb) {
-    const int it = kb - kb0;
-    const int cur = it & 1;
-    const uint32_t par = static_cast<uint32_t>(it & 1);
-
-    // ---- A. gather the key block (cp.async, 36 vectors per thread).
-    {
-      const int* slots = s_slot + cur * BN;
-#pragma unroll 4
-      for (int e = tid; e < BN * ROW_CHUNKS; e += NTHREADS) {
-        const int j = e / ROW_CHUNKS, q = e - j * ROW_CHUNKS;
-        const int slot = slots[j];
-        cp_async16(sbase + OFF_KV + (q >> 3) * KV_CHUNK + j * 128 + (((q & 7) ^ (j & 7)) << 4),
-                   slot >= 0 ? p.kv + static_cast<long long>(slot) * D_QK + q * 8 : p.kv,
-                   slot >= 0 ? 16 : 0);
-      }
-      cp_async_wait_all();
-      tc::fence_async_smem();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    // ---- B. S^T = K Q^T, issued by one thread.
-    if (tid == 0) {
-#pragma unroll 4
-      for (int k = 0; k < D_QK / 16; ++k) {
-        const uint64_t a = tc::desc_sw128(sbase + OFF_KV + (k >> 2) * KV_CHUNK + (k & 3) * 32, 16, 1024);
-        const uint64_t bq = tc::desc_sw128(sbase + OFF_Q + (k >> 2) * Q_CHUNK + (k & 3) * 32, 16, 1024);
-        tc::mma_ss(tmem + TM_S, a, bq, IDESC_S, k > 0);
-      }
-      tc::commit(mbar_s);
-    }
-    // Meanwhile: the next block's slots, and its rows into L2.
-    int pending = -1;
-    if (tid < BN && kb + 1 < kb1) {
-      pending = block_slot(p, rq, kb + 1, tid);
-      if (pending >= 0) {
-        const char* row = reinterpret_cast<const char*>(p.kv + static_cast<long long>(pending) * D_QK);
+    for (int it = 0; it < nb; ++it) {
+      const int kb = kb0 + it;
+      const int cur = it & 1;
+      const uint32_t par = static_cast<uint32_t>(it & 1);
+      // Next block's slot for key li, and its row into L2.
+      int pending = -1;
+      if (it + 1 < nb) {
+        pending = block_slot(p, rq, kb + 1, li, true);
+        if (pending >= 0) {
+          const char* row = reinterpret_cast<const char*>(p.kv + static_cast<long long>(pending) * D_QK);
 #pragma unroll
-        for (int l = 0; l < ROW_BYTES / 128; ++l)
-          asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + l * 128));
-      }
-    }
-    alive = tc::mbar_wait_bounded(mbar_s, par, WAIT_LIMIT);
-    tc::fence_after_sync();
-    if (__syncthreads_or(!alive)) break;
-
-    // ---- C. softmax (warps 0-3) and fp16 widening of the values (warps 4-7).
-    if (warp < 4) {
-      const int j = tid;                  // key of this thread = TMEM lane
-      const int jg = kb * BN + j;
-      const bool key_ok = s_slot[cur * BN + j] >= 0;
-      uint32_t sr_lo[32], sr_hi[32];
-      {
-        const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + TM_S;
-        tc::tmem_ld32(ta, sr_lo);
-        tc::tmem_ld32(ta + 32, sr_hi);
-        tc::tmem_wait_ld();
-      }
-#define SR(c) ((c) < 32 ? sr_lo[(c)] : sr_hi[(c) - 32])
-      float s[BM];
-      if (!key_ok) {
-#pragma unroll
-        for (int c = 0; c < BM; ++c) s[c] = -INFINITY;
-      } else if (jg < rq.P && all_rows) {
-#pragma unroll
-        for (int c = 0; c < BM; ++c) s[c] = __uint_as_float(SR(c)) * scale2;
-      } else {
-        const int di = jg - rq.P;   // draft index when >= 0
-#pragma unroll
-        for (int c = 0; c < BM; ++c) {
-          const int t = s_tofr[c];
-          bool vis = t >= 0;
-          if (vis && di >= 0) vis = (s_mask[t] >> di) & 1u;
-          s[c] = vis ? __uint_as_float(SR(c)) * scale2 : -INFINITY;
+          for (int l = 0; l < ROW_BYTES / 128; ++l)
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + l * 128));
         }
       }
-#undef SR
-      // Column (query row) max over this warp's 32 keys, then over 4 warps.
-#pragma unroll
-      for (int c = 0; c < BM; ++c) {
-        const float m = tc::warp_max(s[c]);
-        if ((c & 31) == lane) s_red[warp * BM + c] = m;
-      }
-      named_sync_softmax();
-      if (tid < BM) {
-        const float bm = fmaxf(fmaxf(s_red[tid], s_red[BM + tid]),
-                               fmaxf(s_red[2 * BM + tid], s_red[3 * BM + tid]));
-        const float old = s_mref[tid];
-        float alpha = 1.f;
-        if (bm > old) {
-          s_mref[tid] = bm;
-          if (old != -INFINITY) {
-            alpha = ex2(old - bm);
-            s_flag[tid >> 5] = 1;
-          }
-        }
-        s_alpha[tid] = alpha;
-      }
-      named_sync_softmax();
-      // P^T row of this key (64 query rows) as fp16, 128-byte swizzled.
-      uint32_t pk[BM / 2];
-#pragma unroll
-      for (int c = 0; c < BM; c += 2) {
-        const float m0 = s_mref[c], m1 = s_mref[c + 1];
-        const float p0 = s[c] == -INFINITY ? 0.f : ex2(s[c] - m0);
-        const float p1 = s[c + 1] == -INFINITY ? 0.f : ex2(s[c + 1] - m1);
-        lpart[c] = lpart[c] * s_alpha[c] + p0;
-        lpart[c + 1] = lpart[c + 1] * s_alpha[c + 1] + p1;
-        __half2 h = __floats2half2_rn(p0, p1);
-        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h);
-      }
-      uint8_t* prow = smem + OFF_P + j * 128;
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        *reinterpret_cast<uint4*>(prow + ((g ^ (j & 7)) << 4)) =
-            make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-    } else {
-      const int t2 = tid - 128;
+      // Widen this block's values once S^T(k) is done with them.
+      wait_phase(mbar(MB_S), par, s_abort, p.err);
 #pragma unroll 4
-      for (int e = t2; e < 8 * KV_CHUNK / 16; e += 128) {
+      for (int e = li; e < 8 * KV_CHUNK / 16; e += 128) {
         uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_KV + e * 16);
         uint4 v = *ptr;
         v.x = widen_word(v.x);
@@ -320,103 +287,199 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         v.w = widen_word(v.w);
         *ptr = v;
       }
+      tc::fence_async_smem();
+      tc::mbar_arrive(mbar(MB_CONV));
+      s_slot[(cur ^ 1) * BN + li] = pending;
+      named_sync(2, 128);
+      if (it + 1 < nb) {
+        const int* slots = s_slot + (cur ^ 1) * BN;
+        for (int g = 0; g < 4; ++g) {
+          wait_phase(mbar(MB_OT + g), par, s_abort, p.err);
+          tc::fence_async_smem();
+          gather_group(p, slots, sbase, g, li);
+          tc::cp_async_arrive_noinc(mbar(MB_CHUNK + g));
+        }
+        gather_group(p, slots, sbase, 4, li);   // rope chunk: P^T(k) is no longer read
+        tc::cp_async_arrive_noinc(mbar(MB_CHUNK + 4));
+      }
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    // ---- D. rescale the O^T columns of the row groups whose max moved.
-    const bool rescale0 = s_flag[0] != 0, rescale1 = s_flag[1] != 0;
-    if (rescale0 || rescale1) {
-      const int d0 = (warp >> 2) * 2;   // warps 0-3: tiles 0,1; warps 4-7: tiles 2,3
+  } else if (warp == MMA_WARP) {
+    // ============================ MMA issuer ===============================
+    if (lane == 0) {
 #pragma unroll 1
-      for (int d = d0; d < d0 + 2; ++d) {
+      for (int it = 0; it < nb; ++it) {
+        const uint32_t par = static_cast<uint32_t>(it & 1);
+        for (int g = 0; g < 5; ++g) {
+          wait_phase(mbar(MB_CHUNK + g), par, s_abort, p.err);
+          tc::fence_async_smem();
+          tc::fence_after_sync();
+          const int k0 = g < 4 ? 8 * g : 32, k1 = g < 4 ? k0 + 8 : 36;
+          for (int k = k0; k < k1; ++k) {
+            const uint64_t a = tc::desc_sw128(sbase + OFF_KV + (k >> 2) * KV_CHUNK + (k & 3) * 32, 16, 1024);
+            const uint64_t bq = tc::desc_sw128(sbase + OFF_Q + (k >> 2) * Q_CHUNK + (k & 3) * 32, 16, 1024);
+            tc::mma_ss(tmem + TM_S, a, bq, IDESC_S, k > 0);
+          }
+        }
+        tc::commit(mbar(MB_S));
+        wait_phase(mbar(MB_P), par, s_abort, p.err);
+        wait_phase(mbar(MB_CONV), par, s_abort, p.err);
+        tc::fence_async_smem();
+        tc::fence_after_sync();
+        for (int d = 0; d < 4; ++d) {
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint64_t a = tc::desc_sw128(sbase + OFF_KV + 2 * d * KV_CHUNK + k * 2048, KV_CHUNK, 1024);
+            const uint64_t bp = tc::desc_sw128(sbase + OFF_P + k * 2048, 8192, 1024);
+            tc::mma_ss(tmem + d * BM, a, bp, IDESC_O, (it > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::commit(mbar(MB_OT + d));
+        }
+      }
+    }
+  } else {
+    // ============================= softmax =================================
+    const int j = quad * 32 + lane;     // key of this thread = TMEM lane
+    const int hc = warp >> 2;           // query-row columns hc*32 .. +32
+    const int c0 = hc * HALF;
+    const bool all_rows = row0 + BM <= p.R;
+    const float scale2 = p.scale_log2;
+    float lpart[HALF];                  // this key's share of its rows' sums
+#pragma unroll
+    for (int c = 0; c < HALF; ++c) lpart[c] = 0.f;
+    bool next_ok = nb > 0 && block_slot(p, rq, kb0, j, false) >= 0;
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          if (!(h ? rescale1 : rescale0)) continue;
-          const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + h * 32;
-          uint32_t v[32];
+    for (int it = 0; it < nb; ++it) {
+      const int kb = kb0 + it;
+      const uint32_t par = static_cast<uint32_t>(it & 1);
+      const bool key_ok = next_ok;
+      if (it + 1 < nb) next_ok = block_slot(p, rq, kb + 1, j, false) >= 0;
+      const int jg = kb * BN + j;
+      wait_phase(mbar(MB_S), par, s_abort, p.err);
+      tc::fence_after_sync();
+      uint32_t sr[HALF];
+      tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + TM_S + c0, sr);
+      tc::tmem_wait_ld();
+      float* s = reinterpret_cast<float*>(sr);   // scores overwrite the raw bits in place
+      if (!key_ok) {
+#pragma unroll
+        for (int c = 0; c < HALF; ++c) s[c] = -INFINITY;
+      } else if (jg < rq.P && all_rows) {
+#pragma unroll
+        for (int c = 0; c < HALF; ++c) s[c] = __uint_as_float(sr[c]) * scale2;
+      } else {
+        const int di = jg - rq.P;   // draft index when >= 0
+#pragma unroll
+        for (int c = 0; c < HALF; ++c) {
+          const int t = s_tofr[c0 + c];
+          bool vis = t >= 0;
+          if (vis && di >= 0) vis = (s_mask[t] >> di) & 1u;
+          s[c] = vis ? __uint_as_float(sr[c]) * scale2 : -INFINITY;
+        }
+      }
+      // Column (query row) max over this warp's 32 keys, then over 4 quads.
+#pragma unroll
+      for (int c = 0; c < HALF; ++c) {
+        const float m = tc::warp_max(s[c]);
+        if (c == lane) s_red[quad * BM + c0 + c] = m;
+      }
+      named_sync(1, 256);
+      if (tid < BM) {
+        const float bm = fmaxf(fmaxf(s_red[tid], s_red[BM + tid]),
+                               fmaxf(s_red[2 * BM + tid], s_red[3 * BM + tid]));
+        const float old = s_mref[tid];
+        float alpha = 1.f;
+        if (bm > old) {
+          s_mref[tid] = bm;
+          if (old != -INFINITY) alpha = ex2(old - bm);
+        }
+        s_alpha[tid] = alpha;
+        const bool moved = __any_sync(0xffffffffu, alpha != 1.f);
+        if (lane == 0) s_flag[warp] = moved;
+      }
+      named_sync(1, 256);
+      // Rescale this half's O^T columns if any of its rows' max moved (O^T(k-1)
+      // is complete: S^T(k) finished after it on the in-order tensor pipe).
+      if (s_flag[hc] != 0) {
+#pragma unroll 1
+        for (int d = 0; d < 4; ++d) {
+          const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + c0;
+          uint32_t v[HALF];
           tc::tmem_ld32(ta, v);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            v[c] = __float_as_uint(__uint_as_float(v[c]) * s_alpha[h * 32 + c]);
+          for (int c = 0; c < HALF; ++c)
+            v[c] = __float_as_uint(__uint_as_float(v[c]) * s_alpha[c0 + c]);
           tc::tmem_st32(ta, v);
         }
+        tc::tmem_wait_st();
       }
-      tc::tmem_wait_st();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (tid == 0) {
-      s_flag[0] = 0;
-      s_flag[1] = 0;
-    }
-
-    // ---- E. O^T += V^T P^T, issued by one thread.
-    if (tid == 0) {
-#pragma unroll 1
-      for (int d = 0; d < 4; ++d) {
+      // This key's P^T entries for the half's 32 query rows as fp16 (four
+      // 16-byte granules of the key's 128-byte swizzled row), into the rope
+      // chunk tile (S^T(k) no longer reads it).
+      uint32_t pk[HALF / 2];
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t a = tc::desc_sw128(sbase + OFF_KV + 2 * d * KV_CHUNK + k * 2048, KV_CHUNK, 1024);
-          const uint64_t bp = tc::desc_sw128(sbase + OFF_P + k * 2048, 8192, 1024);
-          tc::mma_ss(tmem + d * BM, a, bp, IDESC_O, (it > 0 || k > 0) ? 1u : 0u);
-        }
+      for (int c = 0; c < HALF; c += 2) {
+        const float2 m = *reinterpret_cast<const float2*>(s_mref + c0 + c);
+        const float2 al = *reinterpret_cast<const float2*>(s_alpha + c0 + c);
+        const float p0 = s[c] == -INFINITY ? 0.f : ex2(s[c] - m.x);
+        const float p1 = s[c + 1] == -INFINITY ? 0.f : ex2(s[c + 1] - m.y);
+        lpart[c] = lpart[c] * al.x + p0;
+        lpart[c + 1] = lpart[c + 1] * al.y + p1;
+        __half2 h = __floats2half2_rn(p0, p1);
+        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h);
       }
-      tc::commit(mbar_o);
-    }
-    alive = tc::mbar_wait_bounded(mbar_o, par, WAIT_LIMIT);
-    tc::fence_after_sync();
-    if (tid < BN) s_slot[(cur ^ 1) * BN + tid] = pending;
-    if (__syncthreads_or(!alive)) break;
-  }
-
-  if (!alive) {
-    if (tid == 0) atomicOr(p.err, ERR_TIMEOUT);
-    // Give in-flight tensor-core work one more bounded wait before freeing TMEM.
-    tc::mbar_wait_bounded(mbar_o, 0, WAIT_LIMIT);
-    write_nan_rows(p, b, split, row0, tid);
-    tc::fence_before_sync();
-    __syncthreads();
-    if (warp == 0) tc::tmem_dealloc<TMEM_COLS>(tmem);
-    return;
-  }
-
-  // ---- finish: row sums over all keys, LSE, normalised O.
-  if (warp < 4) {
+      uint8_t* prow = smem + OFF_P + j * 128;
 #pragma unroll
-    for (int c = 0; c < BM; ++c) {
+      for (int g = 0; g < 4; ++g) {
+        const int gg = hc * 4 + g;
+        *reinterpret_cast<uint4*>(prow + ((gg ^ (j & 7)) << 4)) =
+            make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+      }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(mbar(MB_P));
+    }
+    if (nb > 0) {
+      wait_phase(mbar(MB_OT + 3), static_cast<uint32_t>((nb - 1) & 1), s_abort, p.err);
+      tc::fence_after_sync();
+    }
+    // Row sums over all keys: this warp's 32 keys, then 4 quads.
+#pragma unroll
+    for (int c = 0; c < HALF; ++c) {
       float v = lpart[c];
 #pragma unroll
       for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if ((c & 31) == lane) s_red[warp * BM + c] = v;
+      if (c == lane) s_red[quad * BM + c0 + c] = v;
+    }
+    named_sync(1, 256);
+    if (tid < BM) {
+      const float l = s_red[tid] + s_red[BM + tid] + s_red[2 * BM + tid] + s_red[3 * BM + tid];
+      s_l[tid] = l;
+      const int gr = row0 + tid;
+      if (gr < p.R) {
+        const float lse = l > 0.f ? (s_mref[tid] + log2f(l)) * kLn2 : -INFINITY;
+        if (p.nsplit == 1) p.lse[static_cast<size_t>(b) * p.R + gr] = lse;
+        else p.ws_lse[(static_cast<size_t>(b) * p.nsplit + split) * p.R + gr] = lse;
+      }
     }
   }
+
+  // ---- all roles: normalised O out of TMEM (thread = value dim).
+  tc::fence_before_sync();
   __syncthreads();
-  if (tid < BM) {
-    const float l = s_red[tid] + s_red[BM + tid] + s_red[2 * BM + tid] + s_red[3 * BM + tid];
-    s_l[tid] = l;
-    const int gr = row0 + tid;
-    if (gr < p.R) {
-      const float lse = l > 0.f ? (s_mref[tid] + log2f(l)) * kLn2 : -INFINITY;
-      if (p.nsplit == 1) p.lse[static_cast<size_t>(b) * p.R + gr] = lse;
-      else p.ws_lse[(static_cast<size_t>(b) * p.nsplit + split) * p.R + gr] = lse;
-    }
-  }
-  __syncthreads();
-  {
-    const int d0 = (warp >> 2) * 2;
+  tc::fence_after_sync();
+  if (*s_abort != 0) {
+    write_nan_rows(p, b, split, row0, tid);
+  } else if (warp < LOADER_WARP0) {
+    // Softmax warp (quad, half): the half's 32 rows of every O^T tile.
+    const int h = warp >> 2;
     const int nrows = min(BM, p.R - row0);
 #pragma unroll 1
-    for (int d = d0; d < d0 + 2; ++d) {
+    for (int d = 0; d < 4; ++d) {
       const int dim = d * 128 + quad * 32 + lane;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      {
         uint32_t v[32];
-        if (kb1 > kb0) {
+        if (nb > 0) {
           tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + h * 32, v);
           tc::tmem_wait_ld();
         }
@@ -425,15 +488,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
           const int r = h * 32 + c;
           if (r >= nrows) continue;
           const float l = s_l[r];
-          const float o = l > 0.f ? __uint_as_float(v[c]) / l : 0.f;
+          const float o = (l > 0.f && nb > 0) ? __uint_as_float(v[c]) / l : 0.f;
           const size_t row = static_cast<size_t>(b) * p.R + row0 + r;
           if (p.nsplit == 1) {
-            if (p.out_bf16) {
-              __nv_bfloat16 x = __float2bfloat16_rn(o);
-              reinterpret_cast<__nv_bfloat16*>(p.out)[row * D_V + dim] = x;
-            } else {
+            if (p.out_bf16)
+              reinterpret_cast<__nv_bfloat16*>(p.out)[row * D_V + dim] = __float2bfloat16_rn(o);
+            else
               reinterpret_cast<float*>(p.out)[row * D_V + dim] = o;
-            }
           } else {
             p.ws_o[((static_cast<size_t>(b) * p.nsplit + split) * p.R + row0 + r) * D_V + dim] = o;
           }
@@ -443,7 +504,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc<TMEM_COLS>(tmem);
+  if (warp == MMA_WARP) tc::tmem_dealloc<TMEM_COLS>(tmem);
 }
 
 }  // namespace
