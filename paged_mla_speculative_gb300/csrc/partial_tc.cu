@@ -72,8 +72,8 @@ static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024
 // mbarrier indices
 constexpr int MB_CHUNK = 0;   // [5] chunk pairs 0..3 and the rope chunk landed (count 128)
 constexpr int MB_S = 5;       // S^T done (tcgen05.commit)
-constexpr int MB_P = 6;       // P^T written, O^T rescaled (count 256)
-constexpr int MB_CONV = 7;    // values widened to fp16 (count 128)
+constexpr int MB_P = 6;       // P^T written, O^T rescaled (one arrival per softmax warp)
+constexpr int MB_CONV = 7;    // values widened to fp16 (one arrival per loader warp)
 constexpr int MB_OT = 8;      // [4] O^T tile d done (tcgen05.commit)
 
 constexpr int TMEM_COLS = 512;
@@ -106,6 +106,14 @@ __device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t parity, volat
       return false;
     }
   }
+}
+
+// Warp-wide wait: lane 0 polls (keeping shared-memory traffic away from the
+// tensor core's operand reads), then the warp reconverges behind it.
+__device__ __forceinline__ void wait_warp(uint32_t mbar, uint32_t parity, volatile int* abort,
+                                          int* err, int lane) {
+  if (lane == 0) wait_phase(mbar, parity, abort, err);
+  __syncwarp();
 }
 
 // Slot of key r of 128-key block kb, or -1 past the end of the request or
@@ -226,8 +234,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   if (tid == 0) {
     for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 128);
     tc::mbar_init(mbar(MB_S), 1);
-    tc::mbar_init(mbar(MB_P), 256);
-    tc::mbar_init(mbar(MB_CONV), 128);
+    tc::mbar_init(mbar(MB_P), 8);
+    tc::mbar_init(mbar(MB_CONV), 4);
     for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_OT + i), 1);
     tc::mbar_fence_init();
     s_flag[0] = 0;
@@ -276,25 +284,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         }
       }
       // Widen this block's values once S^T(k) is done with them.
-      wait_phase(mbar(MB_S), par, s_abort, p.err);
-#pragma unroll 4
-      for (int e = li; e < 8 * KV_CHUNK / 16; e += 128) {
-        uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_KV + e * 16);
-        uint4 v = *ptr;
-        v.x = widen_word(v.x);
-        v.y = widen_word(v.y);
-        v.z = widen_word(v.z);
-        v.w = widen_word(v.w);
-        *ptr = v;
+      wait_warp(mbar(MB_S), par, s_abort, p.err, lane);
+#pragma unroll 1
+      for (int e0 = li; e0 < 8 * KV_CHUNK / 16; e0 += 8 * 128) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(smem + OFF_KV + (e0 + u * 128) * 16);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          v[u].x = widen_word(v[u].x);
+          v[u].y = widen_word(v[u].y);
+          v[u].z = widen_word(v[u].z);
+          v[u].w = widen_word(v[u].w);
+          *reinterpret_cast<uint4*>(smem + OFF_KV + (e0 + u * 128) * 16) = v[u];
+        }
       }
       tc::fence_async_smem();
-      tc::mbar_arrive(mbar(MB_CONV));
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(mbar(MB_CONV));
       s_slot[(cur ^ 1) * BN + li] = pending;
       named_sync(2, 128);
       if (it + 1 < nb) {
         const int* slots = s_slot + (cur ^ 1) * BN;
         for (int g = 0; g < 4; ++g) {
-          wait_phase(mbar(MB_OT + g), par, s_abort, p.err);
+          wait_warp(mbar(MB_OT + g), par, s_abort, p.err, lane);
           tc::fence_async_smem();
           gather_group(p, slots, sbase, g, li);
           tc::cp_async_arrive_noinc(mbar(MB_CHUNK + g));
@@ -354,7 +367,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       const bool key_ok = next_ok;
       if (it + 1 < nb) next_ok = block_slot(p, rq, kb + 1, j, false) >= 0;
       const int jg = kb * BN + j;
-      wait_phase(mbar(MB_S), par, s_abort, p.err);
+      wait_warp(mbar(MB_S), par, s_abort, p.err, lane);
       tc::fence_after_sync();
       uint32_t sr[HALF];
       tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + TM_S + c0, sr);
@@ -397,22 +410,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         if (lane == 0) s_flag[warp] = moved;
       }
       named_sync(1, 256);
-      // Rescale this half's O^T columns if any of its rows' max moved (O^T(k-1)
-      // is complete: S^T(k) finished after it on the in-order tensor pipe).
-      if (s_flag[hc] != 0) {
-#pragma unroll 1
-        for (int d = 0; d < 4; ++d) {
-          const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + c0;
-          uint32_t v[HALF];
-          tc::tmem_ld32(ta, v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < HALF; ++c)
-            v[c] = __float_as_uint(__uint_as_float(v[c]) * s_alpha[c0 + c]);
-          tc::tmem_st32(ta, v);
-        }
-        tc::tmem_wait_st();
-      }
       // This key's P^T entries for the half's 32 query rows as fp16 (four
       // 16-byte granules of the key's 128-byte swizzled row), into the rope
       // chunk tile (S^T(k) no longer reads it).
@@ -435,12 +432,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         *reinterpret_cast<uint4*>(prow + ((gg ^ (j & 7)) << 4)) =
             make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
       }
+      // Rescale this half's O^T columns if any of its rows' max moved (O^T(k-1)
+      // is complete: S^T(k) finished after it on the in-order tensor pipe).
+      if (s_flag[hc] != 0) {
+#pragma unroll 1
+        for (int d = 0; d < 4; d += 2) {
+          const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + c0;
+          uint32_t v0[HALF], v1[HALF];
+          tc::tmem_ld32(ta, v0);
+          tc::tmem_ld32(ta + BM, v1);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < HALF; ++c) {
+            const float al = s_alpha[c0 + c];
+            v0[c] = __float_as_uint(__uint_as_float(v0[c]) * al);
+            v1[c] = __float_as_uint(__uint_as_float(v1[c]) * al);
+          }
+          tc::tmem_st32(ta, v0);
+          tc::tmem_st32(ta + BM, v1);
+        }
+        tc::tmem_wait_st();
+      }
       tc::fence_async_smem();
       tc::fence_before_sync();
-      tc::mbar_arrive(mbar(MB_P));
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(mbar(MB_P));
     }
     if (nb > 0) {
-      wait_phase(mbar(MB_OT + 3), static_cast<uint32_t>((nb - 1) & 1), s_abort, p.err);
+      wait_warp(mbar(MB_OT + 3), static_cast<uint32_t>((nb - 1) & 1), s_abort, p.err, lane);
       tc::fence_after_sync();
     }
     // Row sums over all keys: this warp's 32 keys, then 4 quads.
