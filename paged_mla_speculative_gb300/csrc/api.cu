@@ -41,10 +41,6 @@ struct mla_verify_plan {
   float* st_lse;
   long long st_idx_cap;
   cudaEvent_t profile_event;  // recorded after the partial kernel, or null
-  // TMA descriptor of the cache rows, re-encoded (host only) when the cache
-  // pointer changes.
-  CUtensorMap kv_map;
-  const void* kv_map_ptr;
 };
 
 namespace {
@@ -282,17 +278,8 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   p.err = pl->err;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t le;
-  if (pl->kernel == MLA_VERIFY_KERNEL_MMA) {
-    le = mlav::launch_partial_mma(p, s);
-  } else {
-    if (pl->kv_map_ptr != kv_cache) {
-      if (mlav::encode_kv_map(&pl->kv_map, kv_cache, pl->num_slots) != cudaSuccess)
-        return MLA_VERIFY_ERR_CUDA;
-      pl->kv_map_ptr = kv_cache;
-    }
-    le = mlav::launch_partial_tc(p, pl->kv_map, s);
-  }
+  const cudaError_t le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
+                                                             : mlav::launch_partial_tc(p, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   if (pl->profile_event && cudaEventRecord(pl->profile_event, s) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;

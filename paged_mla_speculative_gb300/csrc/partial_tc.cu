@@ -21,24 +21,20 @@
 // are widened to fp16 in shared memory, because P in bf16 costs more than the
 // 1e-2 output tolerance allows.
 //
-// Roles (14 warps):
+// Roles (13 warps):
 //   warps 0-7  softmax: one thread per (key of the block, half of the 64 query
 //              rows); warps w and w+4 share TMEM lane quadrant w;
-//   warps 8-11 load the Q tile once (16-byte cp.async), then widen each
-//              block's value chunks 0-7 to fp16 in place once S^T is done;
-//   warp 12    lane 0 issues the MMAs; the warp owns the TMEM allocation;
-//   warp 13    TMA producer: gathers the block's 128 scattered 1152-byte rows
-//              with tile::gather4 (four rows x 128 bytes per instruction, lane
-//              l owning keys 4l..4l+3) into nine 128-byte-swizzled 16 KB chunk
-//              tiles, the MMA operand layout (the swizzle is applied by TMA).
+//   warps 8-11 loaders: gather the block's 128 scattered 1152-byte rows with
+//              16-byte cp.async vectors into nine 128-byte-swizzled 16 KB
+//              chunk tiles (the MMA operand layout), then widen the value
+//              chunks 0-7 to fp16 in place once S^T no longer reads them;
+//   warp 12    lane 0 issues the MMAs; the warp owns the TMEM allocation.
 // Pipeline over 128-key blocks k (mbarriers, all waits bounded):
-//   producer: chunk pair d of block k+1 is gathered as soon as O^T(k) tile d
+//   loaders:  chunk pair d of block k+1 is gathered as soon as O^T(k) tile d
 //             has finished with it; the rope chunk (which holds P^T(k)) last;
 //   MMA:      S^T(k) chunk pair by chunk pair as the pairs land, then, once
 //             softmax(k) and the widening are done, O^T(k) tile by tile;
 //   softmax:  after S^T(k): mask, max, P^T(k) into the rope chunk tile.
-#include <cuda.h>
-
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -51,9 +47,9 @@ namespace {
 
 constexpr int BM = 64;          // query rows per CTA: MMA N
 constexpr int BN = 128;         // keys per block: MMA M of S^T
-constexpr int NWARPS = 14;
+constexpr int NWARPS = 13;
 constexpr int NTHREADS = NWARPS * 32;
-constexpr int LOADER_WARP0 = 8, MMA_WARP = 12, TMA_WARP = 13;
+constexpr int LOADER_WARP0 = 8, MMA_WARP = 12;
 constexpr int HALF = BM / 2;    // query-row columns per softmax thread
 constexpr int Q_CHUNK = BM * 128;   // one 64-dim chunk of the Q tile
 constexpr int KV_CHUNK = BN * 128;  // one 64-dim chunk of the key block
@@ -64,7 +60,8 @@ constexpr int OFF_RED = OFF_KV + 9 * KV_CHUNK;  // float [4][64] per-warp column
 constexpr int OFF_MREF = OFF_RED + 4 * 64 * 4;  // float [64] running row max (base 2)
 constexpr int OFF_ALPHA = OFF_MREF + 64 * 4;    // float [64] rescale factor of this block
 constexpr int OFF_L = OFF_ALPHA + 64 * 4;       // float [64] final row sums
-constexpr int OFF_MASK = OFF_L + 64 * 4;        // uint32 [32] ancestor masks
+constexpr int OFF_SLOT = OFF_L + 64 * 4;        // int [2][128] slots of this / next block
+constexpr int OFF_MASK = OFF_SLOT + 2 * BN * 4; // uint32 [32] ancestor masks
 constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -1 past R
 constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [16] mbarriers
 constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, rescale flags [2], abort flag
@@ -73,12 +70,11 @@ static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
 // mbarrier indices
-constexpr int MB_CHUNK = 0;   // [5] chunk pairs 0..3 and the rope chunk landed (TMA bytes)
+constexpr int MB_CHUNK = 0;   // [5] chunk pairs 0..3 and the rope chunk landed (count 128)
 constexpr int MB_S = 5;       // S^T done (tcgen05.commit)
 constexpr int MB_P = 6;       // P^T written, O^T rescaled (one arrival per softmax warp)
 constexpr int MB_CONV = 7;    // values widened to fp16 (one arrival per loader warp)
 constexpr int MB_OT = 8;      // [4] O^T tile d done (tcgen05.commit)
-constexpr int MB_Q = 12;      // Q tile landed (cp.async, 128 threads)
 
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t TM_S = 256;                  // S^T columns; O^T tile d at d * 64
@@ -112,12 +108,11 @@ __device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t parity, volat
   }
 }
 
-// Warp-wide wait.  Every lane polls: measured faster here than one polling
-// lane with the rest parked at __syncwarp.
+// Warp-wide wait: lane 0 polls (keeping shared-memory traffic away from the
+// tensor core's operand reads), then the warp reconverges behind it.
 __device__ __forceinline__ void wait_warp(uint32_t mbar, uint32_t parity, volatile int* abort,
                                           int* err, int lane) {
-  (void)lane;
-  wait_phase(mbar, parity, abort, err);
+  if (lane == 0) wait_phase(mbar, parity, abort, err);
   __syncwarp();
 }
 
@@ -158,19 +153,37 @@ __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split
   }
 }
 
-// Producer lane: gather chunk group g of a key block (g < 4: value chunks
-// 2g, 2g+1; g == 4: the rope chunk 8) for this lane's four keys.  Keys
-// without a slot use the row just past the cache: out of range, read as zero.
-__device__ __forceinline__ void tma_group(const CUtensorMap* map, uint32_t sbase, uint32_t mbar,
-                                          int g, int lane, const int (&sl)[4]) {
-  const int c_lo = g < 4 ? 2 * g : 8, c_hi = g < 4 ? 2 * g + 1 : 8;
-  for (int c = c_lo; c <= c_hi; ++c)
-    tc::tma_gather4(sbase + OFF_KV + c * KV_CHUNK + lane * 4 * 128, map, c * 64, sl[0], sl[1],
-                    sl[2], sl[3], mbar);
+// Loader: gather chunk group g of a key block (g < 4: value chunks 2g, 2g+1;
+// g == 4: the rope chunk 8) for the keys whose slots are given; rows without
+// a slot are zero-filled.  Two rows per warp instruction, 16 lanes per
+// 256-byte row segment.
+__device__ __forceinline__ void gather_group(const Params& p, const int* slots, uint32_t sbase,
+                                             int g, int li) {
+  if (g < 4) {
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int e = li + 128 * i;
+      const int j = e >> 4, gq = e & 15;
+      const int c = 2 * g + (gq >> 3), gr = gq & 7;
+      const int slot = slots[j];
+      cp_async16(sbase + OFF_KV + c * KV_CHUNK + j * 128 + ((gr ^ (j & 7)) << 4),
+                 slot >= 0 ? p.kv + static_cast<long long>(slot) * D_QK + c * 64 + gr * 8 : p.kv,
+                 slot >= 0 ? 16 : 0);
+    }
+  } else {
+#pragma unroll 4
+    for (int i = 0; i < 8; ++i) {
+      const int e = li + 128 * i;
+      const int j = e >> 3, gr = e & 7;
+      const int slot = slots[j];
+      cp_async16(sbase + OFF_KV + 8 * KV_CHUNK + j * 128 + ((gr ^ (j & 7)) << 4),
+                 slot >= 0 ? p.kv + static_cast<long long>(slot) * D_QK + 512 + gr * 8 : p.kv,
+                 slot >= 0 ? 16 : 0);
+    }
+  }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1)
-    partial_tc_kernel(const Params p, const __grid_constant__ CUtensorMap kv_map) {
+__global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int split = blockIdx.x, rt = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -181,6 +194,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   float* s_mref = reinterpret_cast<float*>(smem + OFF_MREF);
   float* s_alpha = reinterpret_cast<float*>(smem + OFF_ALPHA);
   float* s_l = reinterpret_cast<float*>(smem + OFF_L);
+  int* s_slot = reinterpret_cast<int*>(smem + OFF_SLOT);
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
   int* s_tofr = reinterpret_cast<int*>(smem + OFF_TOFR);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -213,9 +227,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
     s_mref[tid] = -INFINITY;
   }
+  if (warp >= LOADER_WARP0 && warp < MMA_WARP && nb > 0) {
+    const int li = tid - LOADER_WARP0 * 32;
+    s_slot[li] = block_slot(p, rq, kb0, li, true);
+  }
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 1);
-    tc::mbar_init(mbar(MB_Q), 128);
+    for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 128);
     tc::mbar_init(mbar(MB_S), 1);
     tc::mbar_init(mbar(MB_P), 8);
     tc::mbar_init(mbar(MB_CONV), 4);
@@ -232,10 +249,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *s_tmem;
 
   if (warp >= LOADER_WARP0 && warp < MMA_WARP) {
-    // ====================== Q tile, fp16 widening ==========================
+    // =========================== loaders ===================================
     const int li = tid - LOADER_WARP0 * 32;
     if (nb > 0) {
-      // Q tile: 64 rows x 9 swizzled chunks, rows beyond R zero.
+      // Q tile (64 rows x 9 chunks, rows beyond R zero) rides on group 0.
       const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
 #pragma unroll 1
       for (int e = li; e < BM * ROW_CHUNKS; e += 128) {
@@ -245,15 +262,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         cp_async16(sbase + OFF_Q + (q >> 3) * Q_CHUNK + r * 128 + (((q & 7) ^ (r & 7)) << 4),
                    in ? qb + static_cast<size_t>(gr) * D_QK + q * 8 : p.q, in ? 16 : 0);
       }
-      tc::cp_async_arrive_noinc(mbar(MB_Q));
+      for (int g = 0; g < 5; ++g) {
+        gather_group(p, s_slot, sbase, g, li);
+        tc::cp_async_arrive_noinc(mbar(MB_CHUNK + g));
+      }
     }
 #pragma unroll 1
     for (int it = 0; it < nb; ++it) {
+      const int kb = kb0 + it;
+      const int cur = it & 1;
       const uint32_t par = static_cast<uint32_t>(it & 1);
-      // Widen this block's values once S^T(k) is done with them (the TMA
-      // phases are observed first so the generic reads follow the copies).
+      // Next block's slot for key li, and its row into L2.
+      int pending = -1;
+      if (it + 1 < nb) {
+        pending = block_slot(p, rq, kb + 1, li, true);
+        if (pending >= 0) {
+          const char* row = reinterpret_cast<const char*>(p.kv + static_cast<long long>(pending) * D_QK);
+#pragma unroll
+          for (int l = 0; l < ROW_BYTES / 128; ++l)
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + l * 128));
+        }
+      }
+      // Widen this block's values once S^T(k) is done with them.
       wait_warp(mbar(MB_S), par, s_abort, p.err, lane);
-      for (int g = 0; g < 4; ++g) wait_warp(mbar(MB_CHUNK + g), par, s_abort, p.err, lane);
 #pragma unroll 1
       for (int e0 = li; e0 < 8 * KV_CHUNK / 16; e0 += 8 * 128) {
         uint4 v[8];
@@ -271,43 +302,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc::fence_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(mbar(MB_CONV));
-    }
-  } else if (warp == TMA_WARP) {
-    // ============================ TMA producer ==============================
-    int sl[4];
-    auto slots_of = [&](int kb) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int s = block_slot(p, rq, kb, lane * 4 + i, true);
-        sl[i] = s >= 0 ? s : static_cast<int>(p.num_slots);   // past the last row: zeros
+      s_slot[(cur ^ 1) * BN + li] = pending;
+      named_sync(2, 128);
+      if (it + 1 < nb) {
+        const int* slots = s_slot + (cur ^ 1) * BN;
+        for (int g = 0; g < 4; ++g) {
+          wait_warp(mbar(MB_OT + g), par, s_abort, p.err, lane);
+          tc::fence_async_smem();
+          gather_group(p, slots, sbase, g, li);
+          tc::cp_async_arrive_noinc(mbar(MB_CHUNK + g));
+        }
+        gather_group(p, slots, sbase, 4, li);   // rope chunk: P^T(k) is no longer read
+        tc::cp_async_arrive_noinc(mbar(MB_CHUNK + 4));
       }
-    };
-    if (nb > 0) slots_of(kb0);
-#pragma unroll 1
-    for (int it = 0; it < nb; ++it) {
-      const uint32_t prev = static_cast<uint32_t>((it - 1) & 1);
-      for (int g = 0; g < 5; ++g) {
-        // Chunk pair g of this block overwrites the previous block's pair g
-        // (and the rope chunk its P^T): wait until O^T(k-1) has read them.
-        if (it > 0 && g < 4) wait_warp(mbar(MB_OT + g), prev, s_abort, p.err, lane);
-        if (lane == 0) tc::mbar_arrive_expect_tx(mbar(MB_CHUNK + g), g < 4 ? 2 * KV_CHUNK : KV_CHUNK);
-        __syncwarp();
-        tma_group(&kv_map, sbase, mbar(MB_CHUNK + g), g, lane, sl);
-      }
-      if (it + 1 < nb) slots_of(kb0 + it + 1);
     }
   } else if (warp == MMA_WARP) {
     // ============================ MMA issuer ===============================
-    if (lane == 0 && nb > 0) {
-      wait_phase(mbar(MB_Q), 0, s_abort, p.err);
-      tc::fence_async_smem();   // the Q tile was written by cp.async (generic proxy)
-    }
     if (lane == 0) {
 #pragma unroll 1
       for (int it = 0; it < nb; ++it) {
         const uint32_t par = static_cast<uint32_t>(it & 1);
         for (int g = 0; g < 5; ++g) {
           wait_phase(mbar(MB_CHUNK + g), par, s_abort, p.err);
+          tc::fence_async_smem();
           tc::fence_after_sync();
           const int k0 = g < 4 ? 8 * g : 32, k1 = g < 4 ? k0 + 8 : 36;
           for (int k = k0; k < k1; ++k) {
@@ -516,40 +533,10 @@ cudaError_t partial_tc_prepare() {
                               SMEM_TOTAL);
 }
 
-cudaError_t launch_partial_tc(const Params& p, const CUtensorMap& kv_map, cudaStream_t stream) {
+cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream) {
   const dim3 grid(p.nsplit, (p.R + BM - 1) / BM, p.batch);
-  partial_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(p, kv_map);
+  partial_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(p);
   return cudaGetLastError();
-}
-
-}  // namespace mlav
-
-namespace mlav {
-
-cudaError_t encode_kv_map(CUtensorMap* map, const void* kv_cache, long long num_slots) {
-  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                              CUtensorMapFloatOOBfill);
-  static Encode encode = nullptr;
-  if (!encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return cudaErrorNotSupported;
-    encode = reinterpret_cast<Encode>(fn);
-  }
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_QK), static_cast<cuuint64_t>(num_slots)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ROW_BYTES)};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache), dims,
-                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace mlav

@@ -138,26 +138,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t mbar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
 }
 
-// Arrive once and add `bytes` to the barrier's expected transaction count.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes)
-               : "memory");
-}
-
-// ---- TMA --------------------------------------------------------------------
-// Four rows (row0..row3, any order, out-of-range rows read as zero) of a 2-D
-// tensor, columns col .. col + box width, into four consecutive box rows at
-// dst; completion is signalled to `mbar` as transaction bytes.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int col, int row0,
-                                            int row1, int row2, int row3, uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(col), "r"(row0), "r"(row1), "r"(row2), "r"(row3),
-      "r"(mbar)
-      : "memory");
-}
-
 __device__ __forceinline__ float warp_max(float v) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(v));
