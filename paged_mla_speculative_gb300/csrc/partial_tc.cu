@@ -75,6 +75,7 @@ constexpr int MB_S = 5;       // S^T done (tcgen05.commit)
 constexpr int MB_P = 6;       // P^T written, O^T rescaled (one arrival per softmax warp)
 constexpr int MB_CONV = 7;    // values widened to fp16 (one arrival per loader warp)
 constexpr int MB_OT = 8;      // [4] O^T tile d done (tcgen05.commit)
+constexpr int MB_SG = 12;     // [4] S^T over chunk pair g done (tcgen05.commit)
 
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t TM_S = 256;                  // S^T columns; O^T tile d at d * 64
@@ -108,11 +109,11 @@ __device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t parity, volat
   }
 }
 
-// Warp-wide wait: lane 0 polls (keeping shared-memory traffic away from the
-// tensor core's operand reads), then the warp reconverges behind it.
+// Warp-wide wait.  Every lane polls: measured faster here than one polling
+// lane with the rest of the warp parked at __syncwarp.
 __device__ __forceinline__ void wait_warp(uint32_t mbar, uint32_t parity, volatile int* abort,
-                                          int* err, int lane) {
-  if (lane == 0) wait_phase(mbar, parity, abort, err);
+                                          int* err) {
+  wait_phase(mbar, parity, abort, err);
   __syncwarp();
 }
 
@@ -237,6 +238,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     tc::mbar_init(mbar(MB_P), 8);
     tc::mbar_init(mbar(MB_CONV), 4);
     for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_OT + i), 1);
+    for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_SG + i), 1);
     tc::mbar_fence_init();
     s_flag[0] = 0;
     s_flag[1] = 0;
@@ -283,20 +285,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
             asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + l * 128));
         }
       }
-      // Widen this block's values once S^T(k) is done with them.
-      wait_warp(mbar(MB_S), par, s_abort, p.err, lane);
+      // Widen this block's value chunks to fp16 pair by pair, each as soon as
+      // the S^T MMAs that read it are done (this hides under S^T, which waits
+      // for the gathers anyway).
 #pragma unroll 1
-      for (int e0 = li; e0 < 8 * KV_CHUNK / 16; e0 += 8 * 128) {
-        uint4 v[8];
+      for (int g = 0; g < 4; ++g) {
+        wait_warp(mbar(MB_SG + g), par, s_abort, p.err);
+        uint8_t* pair = smem + OFF_KV + 2 * g * KV_CHUNK;
+#pragma unroll 1
+        for (int e0 = li; e0 < 2 * KV_CHUNK / 16; e0 += 8 * 128) {
+          uint4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(smem + OFF_KV + (e0 + u * 128) * 16);
+          for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(pair + (e0 + u * 128) * 16);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          v[u].x = widen_word(v[u].x);
-          v[u].y = widen_word(v[u].y);
-          v[u].z = widen_word(v[u].z);
-          v[u].w = widen_word(v[u].w);
-          *reinterpret_cast<uint4*>(smem + OFF_KV + (e0 + u * 128) * 16) = v[u];
+          for (int u = 0; u < 8; ++u) {
+            v[u].x = widen_word(v[u].x);
+            v[u].y = widen_word(v[u].y);
+            v[u].z = widen_word(v[u].z);
+            v[u].w = widen_word(v[u].w);
+            *reinterpret_cast<uint4*>(pair + (e0 + u * 128) * 16) = v[u];
+          }
         }
       }
       tc::fence_async_smem();
@@ -307,7 +315,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       if (it + 1 < nb) {
         const int* slots = s_slot + (cur ^ 1) * BN;
         for (int g = 0; g < 4; ++g) {
-          wait_warp(mbar(MB_OT + g), par, s_abort, p.err, lane);
+          wait_warp(mbar(MB_OT + g), par, s_abort, p.err);
           tc::fence_async_smem();
           gather_group(p, slots, sbase, g, li);
           tc::cp_async_arrive_noinc(mbar(MB_CHUNK + g));
@@ -332,6 +340,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
             const uint64_t bq = tc::desc_sw128(sbase + OFF_Q + (k >> 2) * Q_CHUNK + (k & 3) * 32, 16, 1024);
             tc::mma_ss(tmem + TM_S, a, bq, IDESC_S, k > 0);
           }
+          if (g < 4) tc::commit(mbar(MB_SG + g));   // the pair may now be widened
         }
         tc::commit(mbar(MB_S));
         wait_phase(mbar(MB_P), par, s_abort, p.err);
@@ -367,7 +376,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       const bool key_ok = next_ok;
       if (it + 1 < nb) next_ok = block_slot(p, rq, kb + 1, j, false) >= 0;
       const int jg = kb * BN + j;
-      wait_warp(mbar(MB_S), par, s_abort, p.err, lane);
+      wait_warp(mbar(MB_S), par, s_abort, p.err);
       tc::fence_after_sync();
       uint32_t sr[HALF];
       tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + TM_S + c0, sr);
@@ -459,7 +468,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       if (lane == 0) tc::mbar_arrive(mbar(MB_P));
     }
     if (nb > 0) {
-      wait_warp(mbar(MB_OT + 3), static_cast<uint32_t>((nb - 1) & 1), s_abort, p.err, lane);
+      wait_warp(mbar(MB_OT + 3), static_cast<uint32_t>((nb - 1) & 1), s_abort, p.err);
       tc::fence_after_sync();
     }
     // Row sums over all keys: this warp's 32 keys, then 4 quads.
