@@ -41,6 +41,9 @@ struct mla_verify_plan {
   float* st_lse;
   long long st_idx_cap;
   cudaEvent_t profile_event;  // recorded after the partial kernel, or null
+  // Packed fp16 key blocks for the TC kernel: max_batch x pack_blocks blocks.
+  void* packed;
+  int pack_blocks;
 };
 
 namespace {
@@ -88,7 +91,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_all(mla_verify_plan* p) {
   void* bufs[] = {p->ws_o, p->ws_lse, p->err, p->st_q, p->st_idx, p->st_indptr,
-                  p->st_lens, p->st_parent, p->st_out, p->st_lse};
+                  p->st_lens, p->st_parent, p->st_out, p->st_lse, p->packed};
   for (void* b : bufs)
     if (b) cudaFree(b);
 }
@@ -180,13 +183,17 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
             cudaMalloc(&pl->st_parent, static_cast<size_t>(max_batch) * num_drafts * 4) == cudaSuccess &&
             cudaMalloc(&pl->st_out, qrows * mlav::D_V * out_elt) == cudaSuccess &&
             cudaMalloc(&pl->st_lse, qrows * sizeof(float)) == cudaSuccess;
+  pl->pack_blocks = static_cast<int>(ceil_div(max_kv_len, 128));
+  const size_t packed_bytes =
+      static_cast<size_t>(max_batch) * pl->pack_blocks * mlav::packed_block_bytes();
+  ok = ok && cudaMalloc(&pl->packed, packed_bytes) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_all(pl);
     delete pl;
     return MLA_VERIFY_ERR_OOM;
   }
-  pl->ws_bytes = rows * (mlav::D_V + 1) * sizeof(float) + 256;
+  pl->ws_bytes = rows * (mlav::D_V + 1) * sizeof(float) + 256 + packed_bytes;
   if (cudaMemset(pl->err, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     free_all(pl);
     delete pl;
@@ -276,10 +283,17 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   p.lse = lse;
   p.out_bf16 = pl->out_dtype == MLA_VERIFY_OUT_BF16;
   p.err = pl->err;
+  p.packed = static_cast<const uint8_t*>(pl->packed);
+  p.packed_max_blocks = pl->pack_blocks;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
-                                                             : mlav::launch_partial_tc(p, s);
+  cudaError_t le;
+  if (pl->kernel == MLA_VERIFY_KERNEL_MMA) {
+    le = mlav::launch_partial_mma(p, s);
+  } else {
+    le = mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
+    if (le == cudaSuccess) le = mlav::launch_partial_tc(p, s);
+  }
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   if (pl->profile_event && cudaEventRecord(pl->profile_event, s) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;

@@ -44,6 +44,8 @@ struct Params {
   float* lse;                   // [B, R]
   int out_bf16;
   int* err;                     // sticky device error word
+  const uint8_t* packed;        // packed fp16 key blocks (TC kernel), see pack_kv.cu
+  int packed_max_blocks;        // 128-key blocks reserved per request in `packed`
 };
 
 // Per-request facts every CTA of the request derives the same way.

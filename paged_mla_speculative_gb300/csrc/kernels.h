@@ -16,6 +16,10 @@ cudaError_t launch_partial_mma(const Params& p, cudaStream_t stream);
 cudaError_t partial_tc_prepare();
 cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream);
 
+// Per-call gather of the key rows into packed fp16 operand tiles.
+size_t packed_block_bytes();
+cudaError_t launch_pack_kv(const Params& p, void* packed, int max_blocks, cudaStream_t stream);
+
 // LSE combine of the split partials into out/lse.
 cudaError_t launch_combine(const Params& p, cudaStream_t stream);
 

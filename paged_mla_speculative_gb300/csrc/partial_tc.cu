@@ -8,7 +8,7 @@
 // split for occupancy, 128-bit vector loads of scattered page_size=1 rows).
 //
 // The products are taken transposed so that every MMA has M = 128:
-//     S^T[key, row] = K_block[128 x 576] . Q_tile[64 x 576]^T          (bf16)
+//     S^T[key, row] = K_block[128 x 576] . Q_tile[64 x 576]^T          (fp16)
 //     O^T[dim, row] += V_block^T[512 x 128] . P^T[128 x 64]              (fp16)
 // O^T lives in tensor memory for the whole split (4 tiles of 128 dims x 64
 // rows = columns 0..255) and S^T in columns 256..319.  With one thread per
@@ -18,22 +18,24 @@
 // lazily moved max would round the dominant key's weight too, which doubles
 // the worst-case output error on spiky keys); O^T columns are rescaled in
 // TMEM only for the 32-row groups whose max moved.  P is fp16 and the values
-// are widened to fp16 in shared memory, because P in bf16 costs more than the
-// 1e-2 output tolerance allows.
+// are fp16 (widened by the pack), because P in bf16 costs more than the 1e-2
+// output tolerance allows.
 //
-// Roles (13 warps):
+// The key blocks come from the per-call pack (pack_kv.cu): 147456 contiguous
+// bytes per 128-key block, already fp16 and already in the 128-byte-swizzled
+// operand layout, so each chunk pair arrives with one 32 KB bulk copy.
+//
+// Roles (10 warps):
 //   warps 0-7  softmax: one thread per (key of the block, half of the 64 query
-//              rows); warps w and w+4 share TMEM lane quadrant w;
-//   warps 8-11 loaders: gather the block's 128 scattered 1152-byte rows with
-//              16-byte cp.async vectors into nine 128-byte-swizzled 16 KB
-//              chunk tiles (the MMA operand layout), then widen the value
-//              chunks 0-7 to fp16 in place once S^T no longer reads them;
-//   warp 12    lane 0 issues the MMAs; the warp owns the TMEM allocation.
+//              rows); warps w and w+4 share TMEM lane quadrant w.  First they
+//              load the Q tile and widen it to fp16;
+//   warp 8     lane 0 issues the MMAs; the warp owns the TMEM allocation;
+//   warp 9     lane 0 streams the packed blocks with cp.async.bulk.
 // Pipeline over 128-key blocks k (mbarriers, all waits bounded):
-//   loaders:  chunk pair d of block k+1 is gathered as soon as O^T(k) tile d
-//             has finished with it; the rope chunk (which holds P^T(k)) last;
+//   producer: chunk pair d of block k+1 is copied as soon as O^T(k) tile d has
+//             finished with it; the rope chunk (which holds P^T(k)) last;
 //   MMA:      S^T(k) chunk pair by chunk pair as the pairs land, then, once
-//             softmax(k) and the widening are done, O^T(k) tile by tile;
+//             softmax(k) is done, O^T(k) tile by tile;
 //   softmax:  after S^T(k): mask, max, P^T(k) into the rope chunk tile.
 #include "common.cuh"
 #include "kernels.h"
@@ -47,12 +49,13 @@ namespace {
 
 constexpr int BM = 64;          // query rows per CTA: MMA N
 constexpr int BN = 128;         // keys per block: MMA M of S^T
-constexpr int NWARPS = 13;
+constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
-constexpr int LOADER_WARP0 = 8, MMA_WARP = 12;
+constexpr int SOFTMAX_WARPS = 8, MMA_WARP = 8, COPY_WARP = 9;
 constexpr int HALF = BM / 2;    // query-row columns per softmax thread
 constexpr int Q_CHUNK = BM * 128;   // one 64-dim chunk of the Q tile
 constexpr int KV_CHUNK = BN * 128;  // one 64-dim chunk of the key block
+constexpr int PACKED_BLOCK = 9 * KV_CHUNK;       // one packed 128-key block
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + 9 * Q_CHUNK;
 constexpr int OFF_P = OFF_KV + 8 * KV_CHUNK;   // rope chunk tile, reused for P^T
@@ -60,8 +63,7 @@ constexpr int OFF_RED = OFF_KV + 9 * KV_CHUNK;  // float [4][64] per-warp column
 constexpr int OFF_MREF = OFF_RED + 4 * 64 * 4;  // float [64] running row max (base 2)
 constexpr int OFF_ALPHA = OFF_MREF + 64 * 4;    // float [64] rescale factor of this block
 constexpr int OFF_L = OFF_ALPHA + 64 * 4;       // float [64] final row sums
-constexpr int OFF_SLOT = OFF_L + 64 * 4;        // int [2][128] slots of this / next block
-constexpr int OFF_MASK = OFF_SLOT + 2 * BN * 4; // uint32 [32] ancestor masks
+constexpr int OFF_MASK = OFF_L + 64 * 4;        // uint32 [32] ancestor masks
 constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -1 past R
 constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [16] mbarriers
 constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, rescale flags [2], abort flag
@@ -70,18 +72,17 @@ static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
 // mbarrier indices
-constexpr int MB_CHUNK = 0;   // [5] chunk pairs 0..3 and the rope chunk landed (count 128)
+constexpr int MB_CHUNK = 0;   // [5] chunk pairs 0..3 and the rope chunk landed (copy bytes)
 constexpr int MB_S = 5;       // S^T done (tcgen05.commit)
 constexpr int MB_P = 6;       // P^T written, O^T rescaled (one arrival per softmax warp)
-constexpr int MB_CONV = 7;    // values widened to fp16 (one arrival per loader warp)
+constexpr int MB_Q = 7;       // Q tile in fp16 (one arrival per softmax warp)
 constexpr int MB_OT = 8;      // [4] O^T tile d done (tcgen05.commit)
-constexpr int MB_SG = 12;     // [4] S^T over chunk pair g done (tcgen05.commit)
 
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t TM_S = 256;                  // S^T columns; O^T tile d at d * 64
 constexpr long long WAIT_LIMIT = 1LL << 31;     // cycles before a wait gives up
 
-constexpr uint32_t IDESC_S = tc::idesc_f16(128, BM, 1, 0, 0);   // bf16, both K-major
+constexpr uint32_t IDESC_S = tc::idesc_f16(128, BM, 0, 0, 0);   // fp16, both K-major
 constexpr uint32_t IDESC_O = tc::idesc_f16(128, BM, 0, 1, 1);   // fp16, both MN-major
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
@@ -154,34 +155,11 @@ __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split
   }
 }
 
-// Loader: gather chunk group g of a key block (g < 4: value chunks 2g, 2g+1;
-// g == 4: the rope chunk 8) for the keys whose slots are given; rows without
-// a slot are zero-filled.  Two rows per warp instruction, 16 lanes per
-// 256-byte row segment.
-__device__ __forceinline__ void gather_group(const Params& p, const int* slots, uint32_t sbase,
-                                             int g, int li) {
-  if (g < 4) {
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-      const int e = li + 128 * i;
-      const int j = e >> 4, gq = e & 15;
-      const int c = 2 * g + (gq >> 3), gr = gq & 7;
-      const int slot = slots[j];
-      cp_async16(sbase + OFF_KV + c * KV_CHUNK + j * 128 + ((gr ^ (j & 7)) << 4),
-                 slot >= 0 ? p.kv + static_cast<long long>(slot) * D_QK + c * 64 + gr * 8 : p.kv,
-                 slot >= 0 ? 16 : 0);
-    }
-  } else {
-#pragma unroll 4
-    for (int i = 0; i < 8; ++i) {
-      const int e = li + 128 * i;
-      const int j = e >> 3, gr = e & 7;
-      const int slot = slots[j];
-      cp_async16(sbase + OFF_KV + 8 * KV_CHUNK + j * 128 + ((gr ^ (j & 7)) << 4),
-                 slot >= 0 ? p.kv + static_cast<long long>(slot) * D_QK + 512 + gr * 8 : p.kv,
-                 slot >= 0 ? 16 : 0);
-    }
-  }
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p) {
@@ -195,7 +173,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   float* s_mref = reinterpret_cast<float*>(smem + OFF_MREF);
   float* s_alpha = reinterpret_cast<float*>(smem + OFF_ALPHA);
   float* s_l = reinterpret_cast<float*>(smem + OFF_L);
-  int* s_slot = reinterpret_cast<int*>(smem + OFF_SLOT);
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
   int* s_tofr = reinterpret_cast<int*>(smem + OFF_TOFR);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -228,17 +205,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
     s_mref[tid] = -INFINITY;
   }
-  if (warp >= LOADER_WARP0 && warp < MMA_WARP && nb > 0) {
-    const int li = tid - LOADER_WARP0 * 32;
-    s_slot[li] = block_slot(p, rq, kb0, li, true);
-  }
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 128);
+    for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 1);
     tc::mbar_init(mbar(MB_S), 1);
-    tc::mbar_init(mbar(MB_P), 8);
-    tc::mbar_init(mbar(MB_CONV), 4);
+    tc::mbar_init(mbar(MB_P), SOFTMAX_WARPS);
+    tc::mbar_init(mbar(MB_Q), SOFTMAX_WARPS);
     for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_OT + i), 1);
-    for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_SG + i), 1);
     tc::mbar_fence_init();
     s_flag[0] = 0;
     s_flag[1] = 0;
@@ -250,89 +222,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
 
-  if (warp >= LOADER_WARP0 && warp < MMA_WARP) {
-    // =========================== loaders ===================================
-    const int li = tid - LOADER_WARP0 * 32;
-    if (nb > 0) {
-      // Q tile (64 rows x 9 chunks, rows beyond R zero) rides on group 0.
-      const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
+  if (warp == COPY_WARP) {
+    // ======================= packed-block producer ==========================
+    if (lane == 0) {
+      const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PACKED_BLOCK;
 #pragma unroll 1
-      for (int e = li; e < BM * ROW_CHUNKS; e += 128) {
-        const int r = e / ROW_CHUNKS, q = e - r * ROW_CHUNKS;
-        const int gr = row0 + r;
-        const bool in = gr < p.R;
-        cp_async16(sbase + OFF_Q + (q >> 3) * Q_CHUNK + r * 128 + (((q & 7) ^ (r & 7)) << 4),
-                   in ? qb + static_cast<size_t>(gr) * D_QK + q * 8 : p.q, in ? 16 : 0);
-      }
-      for (int g = 0; g < 5; ++g) {
-        gather_group(p, s_slot, sbase, g, li);
-        tc::cp_async_arrive_noinc(mbar(MB_CHUNK + g));
-      }
-    }
-#pragma unroll 1
-    for (int it = 0; it < nb; ++it) {
-      const int kb = kb0 + it;
-      const int cur = it & 1;
-      const uint32_t par = static_cast<uint32_t>(it & 1);
-      // Next block's slot for key li, and its row into L2.
-      int pending = -1;
-      if (it + 1 < nb) {
-        pending = block_slot(p, rq, kb + 1, li, true);
-        if (pending >= 0) {
-          const char* row = reinterpret_cast<const char*>(p.kv + static_cast<long long>(pending) * D_QK);
-#pragma unroll
-          for (int l = 0; l < ROW_BYTES / 128; ++l)
-            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + l * 128));
+      for (int it = 0; it < nb; ++it) {
+        const uint8_t* src = blocks + static_cast<size_t>(kb0 + it) * PACKED_BLOCK;
+        const uint32_t prev = static_cast<uint32_t>((it - 1) & 1);
+        for (int g = 0; g < 5; ++g) {
+          // Pair g of this block overwrites pair g of the previous one (and
+          // the rope chunk its P^T): wait until O^T(k-1) has read them.
+          if (it > 0 && g < 4) wait_phase(mbar(MB_OT + g), prev, s_abort, p.err);
+          const uint32_t bytes = g < 4 ? 2 * KV_CHUNK : KV_CHUNK;
+          const uint32_t off = g < 4 ? 2 * g * KV_CHUNK : 8 * KV_CHUNK;
+          tc::mbar_arrive_expect_tx(mbar(MB_CHUNK + g), bytes);
+          bulk_copy(sbase + OFF_KV + off, src + off, bytes, mbar(MB_CHUNK + g));
         }
-      }
-      // Widen this block's value chunks to fp16 pair by pair, each as soon as
-      // the S^T MMAs that read it are done (this hides under S^T, which waits
-      // for the gathers anyway).
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        wait_warp(mbar(MB_SG + g), par, s_abort, p.err);
-        uint8_t* pair = smem + OFF_KV + 2 * g * KV_CHUNK;
-#pragma unroll 1
-        for (int e0 = li; e0 < 2 * KV_CHUNK / 16; e0 += 8 * 128) {
-          uint4 v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(pair + (e0 + u * 128) * 16);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            v[u].x = widen_word(v[u].x);
-            v[u].y = widen_word(v[u].y);
-            v[u].z = widen_word(v[u].z);
-            v[u].w = widen_word(v[u].w);
-            *reinterpret_cast<uint4*>(pair + (e0 + u * 128) * 16) = v[u];
-          }
-        }
-      }
-      tc::fence_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(mbar(MB_CONV));
-      s_slot[(cur ^ 1) * BN + li] = pending;
-      named_sync(2, 128);
-      if (it + 1 < nb) {
-        const int* slots = s_slot + (cur ^ 1) * BN;
-        for (int g = 0; g < 4; ++g) {
-          wait_warp(mbar(MB_OT + g), par, s_abort, p.err);
-          tc::fence_async_smem();
-          gather_group(p, slots, sbase, g, li);
-          tc::cp_async_arrive_noinc(mbar(MB_CHUNK + g));
-        }
-        gather_group(p, slots, sbase, 4, li);   // rope chunk: P^T(k) is no longer read
-        tc::cp_async_arrive_noinc(mbar(MB_CHUNK + 4));
       }
     }
   } else if (warp == MMA_WARP) {
     // ============================ MMA issuer ===============================
-    if (lane == 0) {
+    if (lane == 0 && nb > 0) {
+      wait_phase(mbar(MB_Q), 0, s_abort, p.err);
+      tc::fence_after_sync();
 #pragma unroll 1
       for (int it = 0; it < nb; ++it) {
         const uint32_t par = static_cast<uint32_t>(it & 1);
         for (int g = 0; g < 5; ++g) {
           wait_phase(mbar(MB_CHUNK + g), par, s_abort, p.err);
-          tc::fence_async_smem();
           tc::fence_after_sync();
           const int k0 = g < 4 ? 8 * g : 32, k1 = g < 4 ? k0 + 8 : 36;
           for (int k = k0; k < k1; ++k) {
@@ -340,12 +258,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
             const uint64_t bq = tc::desc_sw128(sbase + OFF_Q + (k >> 2) * Q_CHUNK + (k & 3) * 32, 16, 1024);
             tc::mma_ss(tmem + TM_S, a, bq, IDESC_S, k > 0);
           }
-          if (g < 4) tc::commit(mbar(MB_SG + g));   // the pair may now be widened
         }
         tc::commit(mbar(MB_S));
         wait_phase(mbar(MB_P), par, s_abort, p.err);
-        wait_phase(mbar(MB_CONV), par, s_abort, p.err);
-        tc::fence_async_smem();
         tc::fence_after_sync();
         for (int d = 0; d < 4; ++d) {
 #pragma unroll
@@ -360,6 +275,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     }
   } else {
     // ============================= softmax =================================
+    // Q tile: 64 rows x 9 swizzled chunks (rows beyond R zero), then fp16.
+    if (nb > 0) {
+      const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
+#pragma unroll 1
+      for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
+        const int r = e / ROW_CHUNKS, q = e - r * ROW_CHUNKS;
+        const int gr = row0 + r;
+        const bool in = gr < p.R;
+        cp_async16(sbase + OFF_Q + (q >> 3) * Q_CHUNK + r * 128 + (((q & 7) ^ (r & 7)) << 4),
+                   in ? qb + static_cast<size_t>(gr) * D_QK + q * 8 : p.q, in ? 16 : 0);
+      }
+      asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+      named_sync(1, SOFTMAX_WARPS * 32);
+#pragma unroll 1
+      for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
+        uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_Q + e * 16);
+        uint4 v = *ptr;
+        *ptr = make_uint4(widen_word(v.x), widen_word(v.y), widen_word(v.z), widen_word(v.w));
+      }
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(mbar(MB_Q));
+    }
     const int j = quad * 32 + lane;     // key of this thread = TMEM lane
     const int hc = warp >> 2;           // query-row columns hc*32 .. +32
     const int c0 = hc * HALF;
@@ -498,7 +436,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   tc::fence_after_sync();
   if (*s_abort != 0) {
     write_nan_rows(p, b, split, row0, tid);
-  } else if (warp < LOADER_WARP0) {
+  } else if (warp < SOFTMAX_WARPS) {
     // Softmax warp (quad, half): the half's 32 rows of every O^T tile.
     const int h = warp >> 2;
     const int nrows = min(BM, p.R - row0);
