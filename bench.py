@@ -307,9 +307,10 @@ def run_gb300(args):
 
     K = args.steps
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_k = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for e in ev_m:
+    for e in ev_k + ev_m:
         e.record(stream)
     torch.cuda.synchronize()
     uuid = None
@@ -324,19 +325,21 @@ def run_gb300(args):
         t0 = time.perf_counter()
         for i in range(K):
             flush.zero_()
-            plan.set_profile_event(ev_m[i])
+            plan.set_profile_events(ev_k[i], ev_m[i])
             ev_a[i].record(stream)
             call()
             ev_b[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     barrier(ws)
-    plan.set_profile_event(None)
+    plan.set_profile_events(None, None)
 
     call_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
-    part_ms = [a.elapsed_time(m) for a, m in zip(ev_a, ev_m)]
+    pack_ms = [a.elapsed_time(k) for a, k in zip(ev_a, ev_k)]
+    part_ms = [k.elapsed_time(m) for k, m in zip(ev_k, ev_m)]
     comb_ms = [m.elapsed_time(b) for m, b in zip(ev_m, ev_b)]
     mean_call = max_over_ranks(ws, statistics.fmean(call_ms))
+    mean_pack = max_over_ranks(ws, statistics.fmean(pack_ms))
     mean_part = max_over_ranks(ws, statistics.fmean(part_ms))
     mean_comb = max_over_ranks(ws, statistics.fmean(comb_ms))
     us_per_call = mean_call * 1e3 / ws          # whole job: ws replicas in parallel
@@ -398,16 +401,16 @@ def run_gb300(args):
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     t_roof_us = max(work["bytes"] / (hbm * 1e9), flops / (peak * 1e12)) * 1e6
     clocks = clk.summary()
-    launches = K * (2 if ns > 1 else 1)
+    launches = K * (3 if ns > 1 else 2)
 
     line = {
         "metric": "verify_attn_us_per_call", "value": us_per_call, "unit": "us/call",
         "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": mean_call,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded), bf16 inputs resident in HBM",
-        "config": config_of(w, {"nsplit": ns, "kernel": "partial_tc_kernel + combine_kernel"}),
+        "config": config_of(w, {"nsplit": ns, "kernels": "pack_kv_kernel + partial_tc_kernel + combine_kernel"}),
         "us_per_call_p10_p50_p90": [q[0] * 1e3, statistics.median(call_ms) * 1e3, q[-1] * 1e3],
-        "partial_us": mean_part * 1e3, "combine_us": mean_comb * 1e3,
+        "pack_us": mean_pack * 1e3, "partial_us": mean_part * 1e3, "combine_us": mean_comb * 1e3,
         "graph_replay_us_per_call": graph_us,
         "kv_gbs": kv_gbs, "kv_frac_of_hbm": kv_gbs / hbm,
         "roofline_time_us": t_roof_us, "frac_of_roofline": t_roof_us / (mean_call * 1e3),

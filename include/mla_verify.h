@@ -134,15 +134,17 @@ int mla_verify_plan_get_nsplit(const mla_verify_plan* plan, int batch);
 int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
 
 /*
- * Profiling hook.  When `event` (a cudaEvent_t created with timing enabled)
- * is not NULL, every later mla_verify_attn call records it on the call's
- * stream right after the split-KV partial kernel, so the time from an event
- * recorded just before the call measures that kernel alone, and the time to
- * an event recorded just after the call measures the combine.  The record
- * is an ordinary stream operation and is captured into graphs like the
- * kernels.  Pass NULL to stop.
+ * Profiling hook.  Later mla_verify_attn calls record `after_pack` (if not
+ * NULL) on the call's stream right after the key-gather/pack kernel (right
+ * at the start for the MMA family, which has none) and `after_partial` (if
+ * not NULL) right after the split-KV partial kernel.  With events recorded
+ * just before and just after the call, the differences time the pack, the
+ * partial kernel and the combine separately.  Both must be cudaEvent_t
+ * created with timing enabled; the records are ordinary stream operations and
+ * are captured into graphs like the kernels.  Pass NULLs to stop.
  */
-int mla_verify_plan_set_profile_event(mla_verify_plan* plan, void* event);
+int mla_verify_plan_set_profile_events(mla_verify_plan* plan, void* after_pack,
+                                       void* after_partial);
 
 /* Bytes of device workspace the plan holds (partials + error word). */
 size_t mla_verify_plan_workspace_bytes(const mla_verify_plan* plan);

@@ -44,7 +44,7 @@ SIGNATURES = {
     "mla_verify_plan_get_nsplit": (_I, [_P, _I]),
     "mla_verify_plan_set_kernel": (_I, [_P, _I]),
     "mla_verify_plan_workspace_bytes": (ctypes.c_size_t, [_P]),
-    "mla_verify_plan_set_profile_event": (_I, [_P, _P]),
+    "mla_verify_plan_set_profile_events": (_I, [_P, _P, _P]),
     "mla_verify_attn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "mla_verify_attn_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "mla_verify_get_error": (_I, [_P, ctypes.POINTER(_I), _I]),
@@ -150,18 +150,21 @@ class Plan:
     def set_kernel(self, kernel: int):
         _check(load_library().mla_verify_plan_set_kernel(self.handle, kernel), "set_kernel")
 
-    def set_profile_event(self, event):
-        """Record ``event`` (a torch.cuda.Event with timing, or None) after
-        the partial kernel of every later call."""
-        ptr = None
-        if event is not None:
-            if int(event.cuda_event) == 0:   # torch creates the event on first record
-                event.record()
-                event.synchronize()
-            ptr = int(event.cuda_event)
-        _check(load_library().mla_verify_plan_set_profile_event(self.handle, ptr),
-               "set_profile_event")
-        self._profile_event = event
+    def set_profile_events(self, after_pack=None, after_partial=None):
+        """Record torch.cuda.Events (timing enabled) after the pack kernel and
+        after the partial kernel of every later call; None stops either."""
+        ptrs = []
+        for ev in (after_pack, after_partial):
+            if ev is None:
+                ptrs.append(None)
+                continue
+            if int(ev.cuda_event) == 0:   # torch creates the event on first record
+                ev.record()
+                ev.synchronize()
+            ptrs.append(int(ev.cuda_event))
+        _check(load_library().mla_verify_plan_set_profile_events(self.handle, *ptrs),
+               "set_profile_events")
+        self._profile_events = (after_pack, after_partial)
 
     def workspace_bytes(self) -> int:
         return int(load_library().mla_verify_plan_workspace_bytes(self.handle))

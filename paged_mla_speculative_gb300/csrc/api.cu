@@ -40,7 +40,8 @@ struct mla_verify_plan {
   void* st_out;
   float* st_lse;
   long long st_idx_cap;
-  cudaEvent_t profile_event;  // recorded after the partial kernel, or null
+  cudaEvent_t ev_after_pack;     // profiling: recorded after the pack kernel, or null
+  cudaEvent_t ev_after_partial;  // profiling: recorded after the partial kernel, or null
   // Packed fp16 key blocks for the TC kernel: max_batch x pack_blocks blocks.
   void* packed;
   int pack_blocks;
@@ -236,9 +237,10 @@ int mla_verify_plan_set_kernel(mla_verify_plan* pl, int kernel) {
   return MLA_VERIFY_OK;
 }
 
-int mla_verify_plan_set_profile_event(mla_verify_plan* pl, void* event) {
+int mla_verify_plan_set_profile_events(mla_verify_plan* pl, void* after_pack, void* after_partial) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
-  pl->profile_event = static_cast<cudaEvent_t>(event);
+  pl->ev_after_pack = static_cast<cudaEvent_t>(after_pack);
+  pl->ev_after_partial = static_cast<cudaEvent_t>(after_partial);
   return MLA_VERIFY_OK;
 }
 
@@ -287,16 +289,14 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   p.packed_max_blocks = pl->pack_blocks;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t le;
-  if (pl->kernel == MLA_VERIFY_KERNEL_MMA) {
-    le = mlav::launch_partial_mma(p, s);
-  } else {
+  cudaError_t le = cudaSuccess;
+  if (pl->kernel != MLA_VERIFY_KERNEL_MMA)
     le = mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
-    if (le == cudaSuccess) le = mlav::launch_partial_tc(p, s);
-  }
+  if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
+  if (le == cudaSuccess)
+    le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s) : mlav::launch_partial_tc(p, s);
+  if (le == cudaSuccess && pl->ev_after_partial) le = cudaEventRecord(pl->ev_after_partial, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
-  if (pl->profile_event && cudaEventRecord(pl->profile_event, s) != cudaSuccess)
-    return MLA_VERIFY_ERR_CUDA;
   if (ns > 1 && mlav::launch_combine(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   return MLA_VERIFY_OK;
 }
