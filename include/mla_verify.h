@@ -79,6 +79,7 @@ extern "C" {
 #define MLA_VERIFY_ERR_DEVICE        -7   /* current device is not the plan's      */
 #define MLA_VERIFY_ERR_OOM           -8   /* device or pinned allocation failed    */
 #define MLA_VERIFY_ERR_ARG           -9   /* other invalid argument                */
+#define MLA_VERIFY_ERR_SCRATCH      -10   /* call needs more than the static scratch */
 
 /* Bits of the device error word (mla_verify_get_error). */
 #define MLA_VERIFY_DEV_BAD_SLOT       1   /* slot or page id outside the cache     */
@@ -185,6 +186,39 @@ int mla_verify_attn_host(mla_verify_plan* plan, int batch, const void* q_host,
  * plan's device: call outside graph capture.
  */
 int mla_verify_get_error(mla_verify_plan* plan, int* device_status, int clear);
+
+/*
+ * Allocation-free verify attention, for callers that cannot allocate device
+ * memory: code running inside a memory pool that owns the whole device, a
+ * serving loop that must not allocate after start-up, or a layer that is only
+ * handed pointers by an outer framework.  The pages have no counterpart; it
+ * is an integration convenience.
+ *
+ * Runs the MMA family (mma.sync partial kernel + LSE combine, out in fp32)
+ * with `nsplit` key splits (1..MLA_VERIFY_MAX_NSPLIT, no automatic choice).
+ * The split partials live in a file-scope device array of
+ * MLA_VERIFY_STATIC_SCRATCH_BYTES held by every GPU that loads the library
+ * until the process exits; a call needing more (batch * nsplit * T * H * 2052
+ * bytes + 256 when nsplit > 1) returns MLA_VERIFY_ERR_SCRATCH.  Arguments,
+ * layouts and device-side error behaviour are those of mla_verify_attn, with
+ * the shape given per call; `device_status` is an optional device int the
+ * kernels OR their MLA_VERIFY_DEV_* bits into (the caller clears it); when it
+ * is NULL the bits go to a word inside the array, cleared at every call and
+ * not readable.  Calls nothing that allocates (no cudaMalloc or cudaFree).
+ *
+ * The first call on each device looks up the array's device address and sets
+ * a kernel attribute for that device: make it before any stream capture.
+ * Every call on a device shares the one array, so calls that overlap on the
+ * GPU (different streams, or different host threads without ordering) race
+ * on it and corrupt each other's results; serialise them.
+ */
+#define MLA_VERIFY_STATIC_SCRATCH_BYTES (32u << 20)
+int mla_verify_attn_static(int batch, int num_drafts, int num_heads, int page_size,
+                           int64_t num_slots, int max_kv_len, int nsplit, const void* q,
+                           const void* kv_cache, const int32_t* kv_indices,
+                           const int32_t* kv_indptr, const int32_t* kv_lens,
+                           const int32_t* draft_parent, float scale, float* out, float* lse,
+                           int* device_status, void* stream);
 
 /* Static text for a status code. */
 const char* mla_verify_strerror(int status);

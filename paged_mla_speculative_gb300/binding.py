@@ -32,7 +32,9 @@ DEV_TIMEOUT = 16
 DEV_INTERNAL = 32
 
 STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_ALIGN", -3: "ERR_SHAPE", -4: "ERR_BATCH",
-          -5: "ERR_SCALE", -6: "ERR_CUDA", -7: "ERR_DEVICE", -8: "ERR_OOM", -9: "ERR_ARG"}
+          -5: "ERR_SCALE", -6: "ERR_CUDA", -7: "ERR_DEVICE", -8: "ERR_OOM", -9: "ERR_ARG",
+          -10: "ERR_SCRATCH"}
+STATIC_SCRATCH_BYTES = 32 << 20
 
 # name -> (restype, argtypes): every entry point the header declares.
 _P = ctypes.c_void_p
@@ -48,6 +50,8 @@ SIGNATURES = {
     "mla_verify_attn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "mla_verify_attn_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "mla_verify_get_error": (_I, [_P, ctypes.POINTER(_I), _I]),
+    "mla_verify_attn_static": (_I, [_I, _I, _I, _I, ctypes.c_int64, _I, _I, _P, _P, _P, _P, _P, _P,
+                                    ctypes.c_float, _P, _P, _P, _P]),
     "mla_verify_strerror": (ctypes.c_char_p, [_I]),
     "mla_verify_version": (_I, []),
 }

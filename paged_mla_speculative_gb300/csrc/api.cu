@@ -121,6 +121,7 @@ const char* mla_verify_strerror(int status) {
     case MLA_VERIFY_ERR_DEVICE: return "the current CUDA device is not the plan's device";
     case MLA_VERIFY_ERR_OOM: return "device memory allocation failed";
     case MLA_VERIFY_ERR_ARG: return "invalid argument";
+    case MLA_VERIFY_ERR_SCRATCH: return "the call needs more scratch than the static array holds";
     default: return "unknown status";
   }
 }
