@@ -35,16 +35,22 @@ __device__ __forceinline__ uint32_t widen(uint32_t w) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+constexpr int QUARTER = BN / 4;   // keys per CTA
+
+// One CTA packs a quarter block (32 keys x 72 granules): every thread has
+// its nine 16-byte loads in flight at once, and four CTAs per block keep
+// enough bytes in flight per SM to cover DRAM latency.
 __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8_t* packed,
                                                            int max_blocks) {
-  __shared__ int s_slot[BN];
-  const int kb = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  __shared__ int s_slot[QUARTER];
+  const int kb = blockIdx.x >> 2, quarter = blockIdx.x & 3, b = blockIdx.y, tid = threadIdx.x;
   const Request rq = load_request(p, b);
   if (!rq.ok) return;                      // the attention kernel reports the request
   const int nblk = (rq.n + BN - 1) / BN;
   if (kb >= nblk) return;
-  if (tid < BN) {
-    const int j = kb * BN + tid;
+  const int key0 = quarter * QUARTER;      // first key of this quarter within the block
+  if (tid < QUARTER) {
+    const int j = kb * BN + key0 + tid;
     long long s = -1;
     if (j < rq.n) {
       s = key_slot(p, rq.ip0, j);
@@ -54,32 +60,24 @@ __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8
   }
   __syncthreads();
   uint8_t* dst = packed + (static_cast<size_t>(b) * max_blocks + kb) * BLOCK_BYTES;
-  // 128 rows x 72 granules; consecutive threads take consecutive granules of
-  // a row (coalesced 16-byte loads), eight loads in flight per thread.
-#pragma unroll 1
-  for (int e0 = tid; e0 < BN * ROW_CHUNKS; e0 += 8 * NTHREADS) {
-    uint4 v[8];
-    int off[8];
+  constexpr int PER_THREAD = QUARTER * ROW_CHUNKS / NTHREADS;   // 9
+  static_assert(QUARTER * ROW_CHUNKS == PER_THREAD * NTHREADS, "even split");
+  uint4 v[PER_THREAD];
+  int off[PER_THREAD];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = e0 + u * NTHREADS;
-      off[u] = -1;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (e < BN * ROW_CHUNKS) {
-        const int j = e / ROW_CHUNKS, q = e - j * ROW_CHUNKS;
-        const int slot = s_slot[j];
-        off[u] = (q >> 3) * (BN * 128) + j * 128 + (((q & 7) ^ (j & 7)) << 4);
-        if (slot >= 0)
-          v[u] = __ldg(reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(slot) * D_QK) + q);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (off[u] < 0) continue;
-      const uint4 w = make_uint4(widen(v[u].x), widen(v[u].y), widen(v[u].z), widen(v[u].w));
-      *reinterpret_cast<uint4*>(dst + off[u]) = w;
-    }
+  for (int u = 0; u < PER_THREAD; ++u) {
+    const int e = tid + u * NTHREADS;
+    const int jl = e / ROW_CHUNKS, q = e - jl * ROW_CHUNKS;
+    const int j = key0 + jl;                // key within the block
+    const int slot = s_slot[jl];
+    off[u] = (q >> 3) * (BN * 128) + j * 128 + (((q & 7) ^ (j & 7)) << 4);
+    v[u] = slot >= 0 ? __ldg(reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(slot) * D_QK) + q)
+                     : make_uint4(0, 0, 0, 0);
   }
+#pragma unroll
+  for (int u = 0; u < PER_THREAD; ++u)
+    *reinterpret_cast<uint4*>(dst + off[u]) =
+        make_uint4(widen(v[u].x), widen(v[u].y), widen(v[u].z), widen(v[u].w));
 }
 
 }  // namespace
@@ -87,7 +85,7 @@ __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8
 size_t packed_block_bytes() { return BLOCK_BYTES; }
 
 cudaError_t launch_pack_kv(const Params& p, void* packed, int max_blocks, cudaStream_t stream) {
-  const dim3 grid(max_blocks, p.batch);
+  const dim3 grid(4 * max_blocks, p.batch);
   pack_kv_kernel<<<grid, NTHREADS, 0, stream>>>(p, static_cast<uint8_t*>(packed), max_blocks);
   return cudaGetLastError();
 }
