@@ -29,8 +29,9 @@
 //   warps 0-7  softmax: one thread per (key of the block, half of the 64 query
 //              rows); warps w and w+4 share TMEM lane quadrant w.  First they
 //              load the Q tile and widen it to fp16;
-//   warp 8     lane 0 issues the MMAs; the warp owns the TMEM allocation;
-//   warp 9     lane 0 streams the packed blocks with cp.async.bulk.
+//   warp 8     issues the MMAs (one elected lane of the converged warp); it
+//              owns the TMEM allocation;
+//   warp 9     streams the packed blocks with cp.async.bulk (elected lane).
 // Pipeline over 128-key blocks k (mbarriers, all waits bounded):
 //   producer: chunk pair d of block k+1 is copied as soon as O^T(k) tile d has
 //             finished with it; the rope chunk (which holds P^T(k)) last;
@@ -155,13 +156,6 @@ __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split
   }
 }
 
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(mbar)
-      : "memory");
-}
-
 __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int split = blockIdx.x, rt = blockIdx.y, b = blockIdx.z;
@@ -224,33 +218,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
 
   if (warp == COPY_WARP) {
     // ======================= packed-block producer ==========================
-    if (lane == 0) {
-      const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PACKED_BLOCK;
+    // The whole warp runs the loop; one elected lane issues each copy.
+    const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PACKED_BLOCK;
 #pragma unroll 1
-      for (int it = 0; it < nb; ++it) {
-        const uint8_t* src = blocks + static_cast<size_t>(kb0 + it) * PACKED_BLOCK;
-        const uint32_t prev = static_cast<uint32_t>((it - 1) & 1);
-        for (int g = 0; g < 5; ++g) {
-          // Pair g of this block overwrites pair g of the previous one (and
-          // the rope chunk its P^T): wait until O^T(k-1) has read them.
-          if (it > 0 && g < 4) wait_phase(mbar(MB_OT + g), prev, s_abort, p.err);
-          const uint32_t bytes = g < 4 ? 2 * KV_CHUNK : KV_CHUNK;
-          const uint32_t off = g < 4 ? 2 * g * KV_CHUNK : 8 * KV_CHUNK;
-          tc::mbar_arrive_expect_tx(mbar(MB_CHUNK + g), bytes);
-          bulk_copy(sbase + OFF_KV + off, src + off, bytes, mbar(MB_CHUNK + g));
-        }
+    for (int it = 0; it < nb; ++it) {
+      const uint8_t* src = blocks + static_cast<size_t>(kb0 + it) * PACKED_BLOCK;
+      const uint32_t prev = static_cast<uint32_t>((it - 1) & 1);
+      for (int g = 0; g < 5; ++g) {
+        // Pair g of this block overwrites pair g of the previous one (and
+        // the rope chunk its P^T): wait until O^T(k-1) has read them.
+        if (it > 0 && g < 4) wait_warp(mbar(MB_OT + g), prev, s_abort, p.err);
+        const uint32_t bytes = g < 4 ? 2 * KV_CHUNK : KV_CHUNK;
+        const uint32_t off = g < 4 ? 2 * g * KV_CHUNK : 8 * KV_CHUNK;
+        tc::bulk_copy_expect(sbase + OFF_KV + off, src + off, bytes, mbar(MB_CHUNK + g));
       }
     }
   } else if (warp == MMA_WARP) {
     // ============================ MMA issuer ===============================
-    if (lane == 0 && nb > 0) {
-      wait_phase(mbar(MB_Q), 0, s_abort, p.err);
+    // The whole warp runs the loop (warp-uniform operands); one elected lane
+    // issues each MMA and commit.
+    if (nb > 0) {
+      wait_warp(mbar(MB_Q), 0, s_abort, p.err);
       tc::fence_after_sync();
 #pragma unroll 1
       for (int it = 0; it < nb; ++it) {
         const uint32_t par = static_cast<uint32_t>(it & 1);
         for (int g = 0; g < 5; ++g) {
-          wait_phase(mbar(MB_CHUNK + g), par, s_abort, p.err);
+          wait_warp(mbar(MB_CHUNK + g), par, s_abort, p.err);
           tc::fence_after_sync();
           const int k0 = g < 4 ? 8 * g : 32, k1 = g < 4 ? k0 + 8 : 36;
           for (int k = k0; k < k1; ++k) {
@@ -260,7 +254,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
           }
         }
         tc::commit(mbar(MB_S));
-        wait_phase(mbar(MB_P), par, s_abort, p.err);
+        wait_warp(mbar(MB_P), par, s_abort, p.err);
         tc::fence_after_sync();
         for (int d = 0; d < 4; ++d) {
 #pragma unroll

@@ -30,18 +30,44 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16, int 
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The MMA, commit and bulk-copy wrappers below are warp-collective: all 32
+// lanes of a converged warp execute them and the lane chosen by elect.sync
+// issues the instruction.  elect.sync picks the same lane every time for the
+// same member mask, so the commits track exactly the MMAs issued before them.
+// Issuing from one lane inside a divergent branch measured about twice as
+// slow per MMA (the operands are then not warp-uniform).
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n.reg .pred p;\n.reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
-// Arrive once on the mbarrier when every MMA this thread issued so far is done.
+// Arrive once on the mbarrier when every MMA the elected lane issued so far
+// is done.
 __device__ __forceinline__ void commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
-      mbar));
+  asm volatile(
+      "{\n.reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+          mbar));
+}
+
+// Announce `bytes` on the mbarrier (one arrival) and start one bulk copy of
+// that many bytes from global memory into shared memory that completes on it.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_expect(uint32_t dst, const void* src, uint32_t bytes,
+                                                 uint32_t mbar) {
+  asm volatile(
+      "{\n.reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %2;\n"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
 }
 
 __device__ __forceinline__ void fence_before_sync() {
