@@ -60,14 +60,14 @@ constexpr int PACKED_BLOCK = 9 * KV_CHUNK;       // one packed 128-key block
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + 9 * Q_CHUNK;
 constexpr int OFF_P = OFF_KV + 8 * KV_CHUNK;   // rope chunk tile, reused for P^T
-constexpr int OFF_RED = OFF_KV + 9 * KV_CHUNK;  // float [4][64] per-warp column max / sums
-constexpr int OFF_MREF = OFF_RED + 4 * 64 * 4;  // float [64] running row max (base 2)
-constexpr int OFF_ALPHA = OFF_MREF + 64 * 4;    // float [64] rescale factor of this block
-constexpr int OFF_L = OFF_ALPHA + 64 * 4;       // float [64] final row sums
+constexpr int OFF_RED = OFF_KV + 9 * KV_CHUNK;  // float [64][4] column max per quad; [4][64] sums
+constexpr int OFF_MREF = OFF_RED + 4 * 64 * 4;  // float [64] final running row max (base 2)
+constexpr int OFF_WARP = OFF_MREF + 64 * 4;     // float [8][2][32] per-warp row max / rescale factor
+constexpr int OFF_L = OFF_WARP + 8 * 64 * 4;    // float [64] reciprocal of the final row sums (0: none)
 constexpr int OFF_MASK = OFF_L + 64 * 4;        // uint32 [32] ancestor masks
 constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -1 past R
 constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [16] mbarriers
-constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, rescale flags [2], abort flag
+constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, abort flag
 constexpr int SMEM_TOTAL = OFF_MISC + 16;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -119,6 +119,18 @@ __device__ __forceinline__ void wait_warp(uint32_t mbar, uint32_t parity, volati
   __syncwarp();
 }
 
+// Bounded wait that ignores the abort flag: used to let this CTA's own
+// copies land before it exits.
+__device__ __forceinline__ void wait_drain(uint32_t mbar, uint32_t parity, int* err) {
+  const long long t0 = clock64();
+  while (!tc::mbar_try(mbar, parity)) {
+    if (clock64() - t0 > WAIT_LIMIT) {
+      atomicOr(err, ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
 // Slot of key r of 128-key block kb, or -1 past the end of the request or
 // when the table points outside the cache (reported when `report`).
 __device__ __forceinline__ int block_slot(const Params& p, const Request& rq, int kb, int r,
@@ -135,6 +147,23 @@ __device__ __forceinline__ uint32_t widen_word(uint32_t w) {
   const float hi = __uint_as_float(w & 0xffff0000u);
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Column maxima of a warp's 32 x 32 tile (lane = key, v[c] = column c) in 31
+// shuffles: each step halves the columns a lane holds and swaps the other
+// half with the partner lane, so lane l ends with the maximum of column l
+// over all 32 lanes in v[0].
+__device__ __forceinline__ void transpose_max32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+    }
+  }
 }
 
 __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split, int row0, int tid) {
@@ -165,12 +194,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
 
   float* s_red = reinterpret_cast<float*>(smem + OFF_RED);
   float* s_mref = reinterpret_cast<float*>(smem + OFF_MREF);
-  float* s_alpha = reinterpret_cast<float*>(smem + OFF_ALPHA);
   float* s_l = reinterpret_cast<float*>(smem + OFF_L);
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
   int* s_tofr = reinterpret_cast<int*>(smem + OFF_TOFR);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* s_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t mbar0 = sbase + OFF_MBAR;
@@ -195,10 +222,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   const int nb = kb1 - kb0;
 
   if (tid < p.T) s_mask[tid] = ancestor_mask(p.draft_parent + b * p.T, tid, p.err);
-  if (tid < BM) {
-    s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
-    s_mref[tid] = -INFINITY;
-  }
+  if (tid < BM) s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
   if (tid == 0) {
     for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 1);
     tc::mbar_init(mbar(MB_S), 1);
@@ -206,8 +230,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     tc::mbar_init(mbar(MB_Q), SOFTMAX_WARPS);
     for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_OT + i), 1);
     tc::mbar_fence_init();
-    s_flag[0] = 0;
-    s_flag[1] = 0;
     *s_abort = 0;
   }
   if (warp == MMA_WARP) tc::tmem_alloc<TMEM_COLS>(smem_u32(s_tmem));
@@ -220,6 +242,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     // ======================= packed-block producer ==========================
     // The whole warp runs the loop; one elected lane issues each copy.
     const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PACKED_BLOCK;
+    int issued = 0;   // copies issued, in (block, g) order
 #pragma unroll 1
     for (int it = 0; it < nb; ++it) {
       const uint8_t* src = blocks + static_cast<size_t>(kb0 + it) * PACKED_BLOCK;
@@ -228,10 +251,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         // Pair g of this block overwrites pair g of the previous one (and
         // the rope chunk its P^T): wait until O^T(k-1) has read them.
         if (it > 0 && g < 4) wait_warp(mbar(MB_OT + g), prev, s_abort, p.err);
+        if (*s_abort) break;
         const uint32_t bytes = g < 4 ? 2 * KV_CHUNK : KV_CHUNK;
         const uint32_t off = g < 4 ? 2 * g * KV_CHUNK : 8 * KV_CHUNK;
         tc::bulk_copy_expect(sbase + OFF_KV + off, src + off, bytes, mbar(MB_CHUNK + g));
+        ++issued;
       }
+      if (*s_abort) break;
+    }
+    // After an abort the last copy into each slot may still be in flight:
+    // let it land before shared memory is reused or released.
+    if (*s_abort) {
+      for (int g = 0; g < 5 && g < issued; ++g)
+        wait_drain(mbar(MB_CHUNK + g), static_cast<uint32_t>(((issued - 1 - g) / 5) & 1), p.err);
+      __syncwarp();
     }
   } else if (warp == MMA_WARP) {
     // ============================ MMA issuer ===============================
@@ -297,6 +330,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     const int c0 = hc * HALF;
     const bool all_rows = row0 + BM <= p.R;
     const float scale2 = p.scale_log2;
+    float mrow = -INFINITY;             // running max (base 2) of row c0 + lane
+    float* w_m = reinterpret_cast<float*>(smem + OFF_WARP) + warp * 64;   // [32] row max, fully masked -> 0
+    float* w_a = w_m + 32;                                                // [32] rescale factor
     float lpart[HALF];                  // this key's share of its rows' sums
 #pragma unroll
     for (int c = 0; c < HALF; ++c) lpart[c] = 0.f;
@@ -330,41 +366,56 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
           s[c] = vis ? __uint_as_float(sr[c]) * scale2 : -INFINITY;
         }
       }
-      // Column (query row) max over this warp's 32 keys, then over 4 quads.
+      // Column (query row) max: over this warp's 32 keys (lane l ends with
+      // column c0 + l), then over the four quads.  Lane l keeps the running
+      // max of column c0 + l in a register.
+      {
+        float v[HALF];
 #pragma unroll
-      for (int c = 0; c < HALF; ++c) {
-        const float m = tc::warp_max(s[c]);
-        if (c == lane) s_red[quad * BM + c0 + c] = m;
+        for (int c = 0; c < HALF; ++c) v[c] = s[c];
+        transpose_max32(v, lane);
+        s_red[(c0 + lane) * 4 + quad] = v[0];
       }
       named_sync(1, 256);
-      if (tid < BM) {
-        const float bm = fmaxf(fmaxf(s_red[tid], s_red[BM + tid]),
-                               fmaxf(s_red[2 * BM + tid], s_red[3 * BM + tid]));
-        const float old = s_mref[tid];
+      bool moved;
+      {
+        const float4 q4 = *reinterpret_cast<const float4*>(s_red + (c0 + lane) * 4);
+        const float bm = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
         float alpha = 1.f;
-        if (bm > old) {
-          s_mref[tid] = bm;
-          if (old != -INFINITY) alpha = ex2(old - bm);
+        if (bm > mrow) {
+          if (mrow != -INFINITY) alpha = ex2(mrow - bm);
+          mrow = bm;
         }
-        s_alpha[tid] = alpha;
-        const bool moved = __any_sync(0xffffffffu, alpha != 1.f);
-        if (lane == 0) s_flag[warp] = moved;
+        moved = __any_sync(0xffffffffu, alpha != 1.f);
+        w_m[lane] = mrow == -INFINITY ? 0.f : mrow;   // a fully masked row: every p = ex2(-inf) = 0
+        w_a[lane] = alpha;
+        __syncwarp();
       }
-      named_sync(1, 256);
       // This key's P^T entries for the half's 32 query rows as fp16 (four
       // 16-byte granules of the key's 128-byte swizzled row), into the rope
       // chunk tile (S^T(k) no longer reads it).
       uint32_t pk[HALF / 2];
+      if (moved) {
 #pragma unroll
-      for (int c = 0; c < HALF; c += 2) {
-        const float2 m = *reinterpret_cast<const float2*>(s_mref + c0 + c);
-        const float2 al = *reinterpret_cast<const float2*>(s_alpha + c0 + c);
-        const float p0 = s[c] == -INFINITY ? 0.f : ex2(s[c] - m.x);
-        const float p1 = s[c + 1] == -INFINITY ? 0.f : ex2(s[c + 1] - m.y);
-        lpart[c] = lpart[c] * al.x + p0;
-        lpart[c + 1] = lpart[c + 1] * al.y + p1;
-        __half2 h = __floats2half2_rn(p0, p1);
-        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h);
+        for (int c = 0; c < HALF; c += 2) {
+          const float2 m = *reinterpret_cast<const float2*>(w_m + c);
+          const float2 al = *reinterpret_cast<const float2*>(w_a + c);
+          const float p0 = ex2(s[c] - m.x), p1 = ex2(s[c + 1] - m.y);
+          lpart[c] = lpart[c] * al.x + p0;
+          lpart[c + 1] = lpart[c + 1] * al.y + p1;
+          __half2 h = __floats2half2_rn(p0, p1);
+          pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < HALF; c += 2) {
+          const float2 m = *reinterpret_cast<const float2*>(w_m + c);
+          const float p0 = ex2(s[c] - m.x), p1 = ex2(s[c + 1] - m.y);
+          lpart[c] += p0;
+          lpart[c + 1] += p1;
+          __half2 h = __floats2half2_rn(p0, p1);
+          pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h);
+        }
       }
       uint8_t* prow = smem + OFF_P + j * 128;
 #pragma unroll
@@ -375,7 +426,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       }
       // Rescale this half's O^T columns if any of its rows' max moved (O^T(k-1)
       // is complete: S^T(k) finished after it on the in-order tensor pipe).
-      if (s_flag[hc] != 0) {
+      if (moved) {
 #pragma unroll 1
         for (int d = 0; d < 4; d += 2) {
           const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + c0;
@@ -385,7 +436,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
           tc::tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < HALF; ++c) {
-            const float al = s_alpha[c0 + c];
+            const float al = w_a[c];
             v0[c] = __float_as_uint(__uint_as_float(v0[c]) * al);
             v1[c] = __float_as_uint(__uint_as_float(v1[c]) * al);
           }
@@ -403,6 +454,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       wait_warp(mbar(MB_OT + 3), static_cast<uint32_t>((nb - 1) & 1), s_abort, p.err);
       tc::fence_after_sync();
     }
+    if (quad == 0) s_mref[c0 + lane] = mrow;
     // Row sums over all keys: this warp's 32 keys, then 4 quads.
 #pragma unroll
     for (int c = 0; c < HALF; ++c) {
@@ -414,7 +466,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     named_sync(1, 256);
     if (tid < BM) {
       const float l = s_red[tid] + s_red[BM + tid] + s_red[2 * BM + tid] + s_red[3 * BM + tid];
-      s_l[tid] = l;
+      s_l[tid] = l > 0.f ? 1.f / l : 0.f;
       const int gr = row0 + tid;
       if (gr < p.R) {
         const float lse = l > 0.f ? (s_mref[tid] + log2f(l)) * kLn2 : -INFINITY;
@@ -424,20 +476,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     }
   }
 
-  // ---- all roles: normalised O out of TMEM (thread = value dim).
+  // ---- normalised O out of TMEM (thread = value dim), staged row-major in
+  // the idle key-block buffer, then one bulk store per row.
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (*s_abort != 0) {
     write_nan_rows(p, b, split, row0, tid);
-  } else if (warp < SOFTMAX_WARPS) {
-    // Softmax warp (quad, half): the half's 32 rows of every O^T tile.
-    const int h = warp >> 2;
+  } else {
     const int nrows = min(BM, p.R - row0);
+    const bool out16 = p.nsplit == 1 && p.out_bf16;
+    uint8_t* stage = smem + OFF_KV;            // [64 rows][512 dims] fp32 or bf16
+    if (warp < SOFTMAX_WARPS) {
+      // Softmax warp (quad, half): the half's 32 rows of every O^T tile.
+      const int h = warp >> 2;
 #pragma unroll 1
-    for (int d = 0; d < 4; ++d) {
-      const int dim = d * 128 + quad * 32 + lane;
-      {
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + quad * 32 + lane;
         uint32_t v[32];
         if (nb > 0) {
           tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + h * 32, v);
@@ -446,20 +501,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int r = h * 32 + c;
-          if (r >= nrows) continue;
-          const float l = s_l[r];
-          const float o = (l > 0.f && nb > 0) ? __uint_as_float(v[c]) / l : 0.f;
-          const size_t row = static_cast<size_t>(b) * p.R + row0 + r;
-          if (p.nsplit == 1) {
-            if (p.out_bf16)
-              reinterpret_cast<__nv_bfloat16*>(p.out)[row * D_V + dim] = __float2bfloat16_rn(o);
-            else
-              reinterpret_cast<float*>(p.out)[row * D_V + dim] = o;
-          } else {
-            p.ws_o[((static_cast<size_t>(b) * p.nsplit + split) * p.R + row0 + r) * D_V + dim] = o;
-          }
+          const float inv = s_l[r];
+          const float o = (inv > 0.f && nb > 0) ? __uint_as_float(v[c]) * inv : 0.f;
+          if (out16)
+            reinterpret_cast<__nv_bfloat16*>(stage)[r * D_V + dim] = __float2bfloat16_rn(o);
+          else
+            reinterpret_cast<float*>(stage)[r * D_V + dim] = o;
         }
       }
+      tc::fence_async_smem();
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t row_bytes = out16 ? D_V * 2 : D_V * 4;
+      for (int r = lane; r < nrows; r += 32) {
+        const size_t grow = static_cast<size_t>(b) * p.R + row0 + r;
+        void* dst = p.nsplit == 1
+                        ? static_cast<void*>(static_cast<uint8_t*>(p.out) + grow * row_bytes)
+                        : static_cast<void*>(p.ws_o + ((static_cast<size_t>(b) * p.nsplit + split) * p.R +
+                                                       row0 + r) * D_V);
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
+                     "r"(sbase + OFF_KV + r * row_bytes), "r"(row_bytes)
+                     : "memory");
+      }
+      asm volatile("cp.async.bulk.commit_group;\ncp.async.bulk.wait_group 0;\n" ::: "memory");
     }
   }
   tc::fence_before_sync();
