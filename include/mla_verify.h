@@ -142,7 +142,10 @@ int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
  * just before and just after the call, the differences time the pack, the
  * partial kernel and the combine separately.  Both must be cudaEvent_t
  * created with timing enabled; the records are ordinary stream operations and
- * are captured into graphs like the kernels.  Pass NULLs to stop.
+ * are captured into graphs like the kernels.  Pass NULLs to stop.  Without
+ * events each kernel of a call may start while the previous one finishes
+ * (programmatic dependent launch); with events they run back to back, so the
+ * split times each kernel alone and the call as a whole is a little slower.
  */
 int mla_verify_plan_set_profile_events(mla_verify_plan* plan, void* after_pack,
                                        void* after_partial);

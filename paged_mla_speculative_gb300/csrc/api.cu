@@ -290,15 +290,20 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   p.packed_max_blocks = pl->pack_blocks;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Each kernel may start while the one before it finishes (programmatic
+  // dependent launch), except when profiling events sit between them: then
+  // the kernels run back to back so that each event brackets one kernel.
+  const bool overlap = !pl->ev_after_pack && !pl->ev_after_partial;
   cudaError_t le = cudaSuccess;
   if (pl->kernel != MLA_VERIFY_KERNEL_MMA)
     le = mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)
-    le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s) : mlav::launch_partial_tc(p, s);
+    le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
+                                             : mlav::launch_partial_tc(p, s, overlap);
   if (le == cudaSuccess && pl->ev_after_partial) le = cudaEventRecord(pl->ev_after_partial, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
-  if (ns > 1 && mlav::launch_combine(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (ns > 1 && mlav::launch_combine(p, s, overlap) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   return MLA_VERIFY_OK;
 }
 

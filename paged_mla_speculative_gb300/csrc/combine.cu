@@ -19,6 +19,9 @@ namespace {
 constexpr int WARPS = 8;
 
 __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
+  // The split partials come from the kernel just before this one on the
+  // stream (a no-op when launched without overlap).
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
   if (row >= static_cast<long long>(p.batch) * p.R) return;
@@ -81,11 +84,18 @@ __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
 
 }  // namespace
 
-cudaError_t launch_combine(const Params& p, cudaStream_t stream) {
+cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool overlap) {
   const long long rows = static_cast<long long>(p.batch) * p.R;
-  const unsigned grid = static_cast<unsigned>((rows + WARPS - 1) / WARPS);
-  combine_kernel<<<grid, WARPS * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + WARPS - 1) / WARPS));
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 }  // namespace mlav

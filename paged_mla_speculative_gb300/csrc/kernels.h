@@ -14,13 +14,17 @@ cudaError_t launch_partial_mma(const Params& p, cudaStream_t stream);
 
 // Split-KV partial kernel on tcgen05 tensor cores with TMEM accumulators.
 cudaError_t partial_tc_prepare();
-cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream);
+// `overlap`: launch with programmatic stream serialisation, so the kernel's
+// CTAs may start while the previous kernel on the stream (the pack, the
+// partial kernel) finishes; the kernel waits for that kernel's results with
+// griddepcontrol.wait before reading them.
+cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap);
 
 // Per-call gather of the key rows into packed fp16 operand tiles.
 size_t packed_block_bytes();
 cudaError_t launch_pack_kv(const Params& p, void* packed, int max_blocks, cudaStream_t stream);
 
 // LSE combine of the split partials into out/lse.
-cudaError_t launch_combine(const Params& p, cudaStream_t stream);
+cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool overlap);
 
 }  // namespace mlav

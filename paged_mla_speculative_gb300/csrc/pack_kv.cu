@@ -43,6 +43,9 @@ constexpr int QUARTER = BN / 4;   // keys per CTA
 __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8_t* packed,
                                                            int max_blocks) {
   __shared__ int s_slot[QUARTER];
+  // The attention kernel may be scheduled as soon as every pack CTA runs:
+  // only its copy warp reads the packed blocks, after griddepcontrol.wait.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int kb = blockIdx.x >> 2, quarter = blockIdx.x & 3, b = blockIdx.y, tid = threadIdx.x;
   const Request rq = load_request(p, b);
   if (!rq.ok) return;                      // the attention kernel reports the request

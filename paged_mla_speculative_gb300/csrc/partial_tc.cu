@@ -242,6 +242,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     // ======================= packed-block producer ==========================
     // The whole warp runs the loop; one elected lane issues each copy.
     const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PACKED_BLOCK;
+    // The packed blocks come from the pack kernel just before this one on
+    // the stream: wait for it (a no-op when launched without overlap).
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     int issued = 0;   // copies issued, in (block, g) order
 #pragma unroll 1
     for (int it = 0; it < nb; ++it) {
@@ -480,6 +483,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   // the idle key-block buffer, then one bulk store per row.
   tc::fence_before_sync();
   __syncthreads();
+  // The combine may be scheduled now; it waits for this grid to complete.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   tc::fence_after_sync();
   if (*s_abort != 0) {
     write_nan_rows(p, b, split, row0, tid);
@@ -488,25 +493,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     const bool out16 = p.nsplit == 1 && p.out_bf16;
     uint8_t* stage = smem + OFF_KV;            // [64 rows][512 dims] fp32 or bf16
     if (warp < SOFTMAX_WARPS) {
-      // Softmax warp (quad, half): the half's 32 rows of every O^T tile.
+      // Softmax warp (quad, half): the half's 32 rows of every O^T tile, two
+      // tiles per TMEM wait, the row reciprocals four at a time.
       const int h = warp >> 2;
 #pragma unroll 1
-      for (int d = 0; d < 4; ++d) {
-        const int dim = d * 128 + quad * 32 + lane;
-        uint32_t v[32];
+      for (int d = 0; d < 4; d += 2) {
+        uint32_t v0[32], v1[32];
         if (nb > 0) {
-          tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + h * 32, v);
+          const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + h * 32;
+          tc::tmem_ld32(ta, v0);
+          tc::tmem_ld32(ta + BM, v1);
           tc::tmem_wait_ld();
         }
+        const int dim0 = d * 128 + quad * 32 + lane, dim1 = dim0 + 128;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int r = h * 32 + c;
-          const float inv = s_l[r];
-          const float o = (inv > 0.f && nb > 0) ? __uint_as_float(v[c]) * inv : 0.f;
-          if (out16)
-            reinterpret_cast<__nv_bfloat16*>(stage)[r * D_V + dim] = __float2bfloat16_rn(o);
-          else
-            reinterpret_cast<float*>(stage)[r * D_V + dim] = o;
+        for (int c = 0; c < 32; c += 4) {
+          const float4 inv4 = *reinterpret_cast<const float4*>(s_l + h * 32 + c);
+          const float inv[4] = {inv4.x, inv4.y, inv4.z, inv4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = h * 32 + c + e;
+            const bool ok = inv[e] > 0.f && nb > 0;
+            const float o0 = ok ? __uint_as_float(v0[c + e]) * inv[e] : 0.f;
+            const float o1 = ok ? __uint_as_float(v1[c + e]) * inv[e] : 0.f;
+            if (out16) {
+              reinterpret_cast<__nv_bfloat16*>(stage)[r * D_V + dim0] = __float2bfloat16_rn(o0);
+              reinterpret_cast<__nv_bfloat16*>(stage)[r * D_V + dim1] = __float2bfloat16_rn(o1);
+            } else {
+              reinterpret_cast<float*>(stage)[r * D_V + dim0] = o0;
+              reinterpret_cast<float*>(stage)[r * D_V + dim1] = o1;
+            }
+          }
         }
       }
       tc::fence_async_smem();
@@ -539,10 +556,18 @@ cudaError_t partial_tc_prepare() {
                               SMEM_TOTAL);
 }
 
-cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream) {
-  const dim3 grid(p.nsplit, (p.R + BM - 1) / BM, p.batch);
-  partial_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nsplit, (p.R + BM - 1) / BM, p.batch);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, partial_tc_kernel, p);
 }
 
 }  // namespace mlav

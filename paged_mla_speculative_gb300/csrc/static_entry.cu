@@ -123,6 +123,6 @@ extern "C" int mla_verify_attn_static(int batch, int num_drafts, int num_heads, 
   p.out_bf16 = 0;
   p.err = err;
   if (mlav::launch_partial_mma(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
-  if (nsplit > 1 && mlav::launch_combine(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (nsplit > 1 && mlav::launch_combine(p, s, false) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   return MLA_VERIFY_OK;
 }

@@ -84,6 +84,30 @@ def test_split_counts(nsplit):
     check_full(W.make_inputs(w), nsplit=nsplit)
 
 
+@pytest.mark.parametrize("nsplit", [2, 7])
+def test_split_merge_repeats_bit_for_bit(nsplit):
+    """Split partials and their LSE combine are deterministic: calls in a row
+    on one plan give the same bits, also after a call with a rejected request
+    (whose NaN rows must not leak into the next call), and match the oracle."""
+    import dataclasses
+    raw = W.make_inputs(small(batch=3, prefix=(900, 300, 1500), seed=111))
+    inp = G.to_cuda(raw)
+    lens = inp.kv_lens.clone()
+    lens[1] = 2                      # fewer rows than drafts: request 1 rejected
+    bad = dataclasses.replace(inp, kv_lens=lens)
+    with G.make_plan(inp, nsplit=nsplit) as plan:
+        o0, l0 = G.run(plan, inp)
+        for i in range(4):
+            if i == 2:
+                G.run(plan, bad)
+                assert plan.get_error() & mb.DEV_BAD_LEN
+            o, l = G.run(plan, inp)
+            assert torch.equal(o, o0) and torch.equal(l, l0)
+        assert plan.get_error() == 0
+    ref_o, ref_l = G.oracle_full(raw)
+    G.assert_parity(o0.float().cpu().numpy(), l0.cpu().numpy(), ref_o, ref_l)
+
+
 @pytest.mark.parametrize("tree", ["chain", "star", "random"])
 def test_tree_shapes(tree):
     w = small(num_drafts=16, num_heads=8, tree=tree, prefix=(200, 90), seed=500)
