@@ -30,6 +30,10 @@ reading of MLA decode attention with absorbed queries (one shared latent KV
 head, values = the 512 latent dims of each key row) plus a causal-prefix and
 tree mask.
 
+``index_builder_ref.build_indices`` restates the per-step index builder (the
+request-to-token table turned into the slot or page table the attention
+reads); its pins are in tests/test_index_builder_pins.py.
+
 Pins (tests/test_oracle_pins.py): pure-Python brute force on tiny inputs, a
 hand-derived closed-form fixture (tests/golden/), one-visible-key, identical
 keys/scores, slot-permutation and page-size invariance, chain == causal,
