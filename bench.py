@@ -85,6 +85,72 @@ def profiled_traffic(workload):
     return None
 
 
+def index_builder_timing(mb, plan, inp, w, flush, stream, steps):
+    """Mean µs of mla_verify_build_indices for this step's requests (L2
+    flushed before each build), its algorithmic bytes and GB/s."""
+    import torch
+    B = w.batch
+    lens = inp.kv_lens.to(torch.int64)
+    ptr = inp.kv_indptr.to(torch.int64)
+    stride = plan.max_kv_len
+    gen = torch.Generator().manual_seed(w.seed + 29)
+    pool_of = torch.randperm(B + 5, generator=gen)[:B]
+    table = torch.full((B + 5, stride), -1, dtype=torch.int32, device="cuda")
+    if inp.page_size == 1:
+        for b in range(B):
+            table[pool_of[b], :int(lens[b])] = inp.kv_indices[int(ptr[b]):int(ptr[b]) + int(lens[b])]
+    else:
+        for b in range(B):
+            pages = inp.kv_indices[int(ptr[b]):int(ptr[b + 1])].to(torch.int64)
+            slots = (pages[:, None] * 64 + torch.arange(64, device="cuda")[None, :]).reshape(-1)
+            table[pool_of[b], :int(lens[b])] = slots[:int(lens[b])].to(torch.int32)
+    pools = pool_of.to(torch.int32).cuda()
+    prefix = (inp.kv_lens - w.num_drafts).to(torch.int32).cuda()
+    idx = torch.empty(int(ptr[-1]) + 64, dtype=torch.int32, device="cuda")
+    iptr = torch.empty(B + 1, dtype=torch.int32, device="cuda")
+    ilens = torch.empty(B, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        mb.build_indices(plan, table, pools, prefix, idx, iptr, ilens, stream=stream)
+    torch.cuda.synchronize()
+    assert torch.equal(iptr, inp.kv_indptr) and torch.equal(ilens, inp.kv_lens)
+    assert torch.equal(idx[:int(ptr[-1])], inp.kv_indices), "built indices differ from the workload's"
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ea[i].record(stream)
+        mb.build_indices(plan, table, pools, prefix, idx, iptr, ilens, stream=stream)
+        eb[i].record(stream)
+    torch.cuda.synchronize()
+    us = statistics.fmean(a.elapsed_time(b) for a, b in zip(ea, eb)) * 1e3
+    # Device time without host gaps: 20 builds captured in one graph, replayed.
+    g = torch.cuda.CUDAGraph()
+    gs = torch.cuda.Stream()
+    gs.wait_stream(stream)
+    with torch.cuda.graph(g, stream=gs):
+        for _ in range(20):
+            mb.build_indices(plan, table, pools, prefix, idx, iptr, ilens, stream=gs)
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g.replay()
+    torch.cuda.synchronize()
+    ga.record(stream)
+    for _ in range(10):
+        g.replay()
+    gb.record(stream)
+    torch.cuda.synchronize()
+    us_warm = ga.elapsed_time(gb) * 1e3 / 200
+    entries = int(ptr[-1])
+    # per entry: one table slot read (a page's first slot for page_size 64) and
+    # one index written; per request: pool row, prefix, kv_len; plus indptr
+    nbytes = entries * (4 + 4) + B * (4 + 4 + 4) + (B + 1) * 4
+    return {"us_per_step": us, "us_per_step_graph_warm_l2": us_warm, "entries": entries,
+            "algorithmic_bytes": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9,
+            "launches": 1 if B <= 1024 else 2,
+            "note": "us_per_step: L2 flushed before each build, launched from Python like the "
+                    "attention; us_per_step_graph_warm_l2: device time of builds replayed from "
+                    "a CUDA graph. At this size the build is bound by latency, not bandwidth"}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -360,6 +426,10 @@ def run_gb300(args):
     us_per_call = mean_call * 1e3 / ws          # whole job: ws replicas in parallel
     q = statistics.quantiles(call_ms, n=10)
 
+    # Per-step index builder on the same step: the request-to-token table
+    # holds each request's slots (pool rows permuted); time the build alone.
+    ib = index_builder_timing(mb, plan, inp, w, flush, stream, min(K, 300))
+
     # CUDA-graph replay of the same call (capture-safe path), device timed.
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -434,6 +504,7 @@ def run_gb300(args):
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "kernel": "partial_tc_kernel",
                      "peak_source": f"{peak_src} bf16 burst (fp16 has the same tensor rate)"},
+        "index_builder": ib,
         "clocks": clocks, "gpu_launches": launches,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

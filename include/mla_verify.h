@@ -88,6 +88,8 @@ extern "C" {
 #define MLA_VERIFY_DEV_BAD_INDPTR     8   /* indptr range does not match kv_len    */
 #define MLA_VERIFY_DEV_TIMEOUT       16   /* a bounded device wait gave up         */
 #define MLA_VERIFY_DEV_INTERNAL      32   /* an internal layout invariant failed   */
+#define MLA_VERIFY_DEV_BAD_POOL      64   /* index builder: pool row / prefix / length out of range */
+#define MLA_VERIFY_DEV_CAPACITY     128   /* index builder: kv_indices capacity exceeded */
 
 /* Output element type. */
 #define MLA_VERIFY_OUT_F32            0
@@ -189,6 +191,47 @@ int mla_verify_attn_host(mla_verify_plan* plan, int batch, const void* q_host,
  * plan's device: call outside graph capture.
  */
 int mla_verify_get_error(mla_verify_plan* plan, int* device_status, int clear);
+
+/*
+ * Per-step index builder: fills kv_lens, kv_indptr and kv_indices for a
+ * verify step on the GPU, in `stream`, from the serving stack's
+ * request-to-token table -- the "marshaling" work the pages see dominate at
+ * short context when it runs on the host per layer, with a kernel on the GPU
+ * named as one remedy ("The Moment of Truth: Benchmarking a Custom sm_120
+ * Verify Kernel Against Triton", sections "Interpreting the Crossover: The
+ * Marshaling Tax" and "Assumptions and Their Validity").  The outputs feed
+ * mla_verify_attn directly; both calls can be captured into one graph.
+ *
+ *   req_to_token      int32 [pool_size][stride]: cache slot of each token
+ *                     position of the request held in that pool row; stride
+ *                     >= the plan's max_kv_len.  For page_size 64 whole pages
+ *                     are allocated: a page's 64 positions hold 64 consecutive
+ *                     slots starting at a multiple of 64, and only the first
+ *                     slot of each page is read.
+ *   req_pool_indices  int32 [batch]: pool row of request b.
+ *   prefix_lens       int32 [batch]: prefix length P_b; the step reads
+ *                     positions 0 .. P_b + T - 1 (the last T are the drafts').
+ *   kv_indices        int32 [capacity] out: slots (page_size 1) or page ids.
+ *   kv_indptr         int32 [batch + 1] out, kv_lens int32 [batch] out.
+ *
+ * kv_lens[b] = P_b + T; kv_indptr is the exclusive prefix sum of each
+ * request's entry count (P_b + T slots, or ceil((P_b + T) / 64) pages).
+ * Device-side problems set sticky bits (mla_verify_get_error) and never fault:
+ * a pool row outside [0, pool_size), a negative prefix or P_b + T > max_kv_len
+ * gives kv_lens[b] = 0 and no entries (MLA_VERIFY_DEV_BAD_POOL; the attention
+ * then rejects the request); when the entries exceed `capacity` the longest
+ * leading run of requests that fits keeps them and every later request gets
+ * kv_lens 0 (MLA_VERIFY_DEV_CAPACITY); a page whose first slot is negative or
+ * not a multiple of 64 gets page id -1 (MLA_VERIFY_DEV_BAD_SLOT).  Host-side
+ * errors as for mla_verify_attn (null or misaligned pointers, batch outside
+ * [1, max_batch], stride < max_kv_len, pool_size < 1 or capacity outside
+ * [0, 2^31) give MLA_VERIFY_ERR_ARG).  Allocates nothing and does not
+ * synchronise.
+ */
+int mla_verify_build_indices(mla_verify_plan* plan, int batch, const int32_t* req_to_token,
+                             int64_t stride, int pool_size, const int32_t* req_pool_indices,
+                             const int32_t* prefix_lens, int32_t* kv_indices, int64_t capacity,
+                             int32_t* kv_indptr, int32_t* kv_lens, void* stream);
 
 /*
  * Allocation-free verify attention, for callers that cannot allocate device

@@ -30,6 +30,8 @@ DEV_BAD_PARENT = 4
 DEV_BAD_INDPTR = 8
 DEV_TIMEOUT = 16
 DEV_INTERNAL = 32
+DEV_BAD_POOL = 64
+DEV_CAPACITY = 128
 
 STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_ALIGN", -3: "ERR_SHAPE", -4: "ERR_BATCH",
           -5: "ERR_SCALE", -6: "ERR_CUDA", -7: "ERR_DEVICE", -8: "ERR_OOM", -9: "ERR_ARG",
@@ -52,6 +54,8 @@ SIGNATURES = {
     "mla_verify_get_error": (_I, [_P, ctypes.POINTER(_I), _I]),
     "mla_verify_attn_static": (_I, [_I, _I, _I, _I, ctypes.c_int64, _I, _I, _P, _P, _P, _P, _P, _P,
                                     ctypes.c_float, _P, _P, _P, _P]),
+    "mla_verify_build_indices": (_I, [_P, _I, _P, ctypes.c_int64, _I, _P, _P, _P, ctypes.c_int64,
+                                      _P, _P, _P]),
     "mla_verify_strerror": (ctypes.c_char_p, [_I]),
     "mla_verify_version": (_I, []),
 }
@@ -229,6 +233,41 @@ def mla_verify_attn(plan: Plan, q, kv_cache, kv_indices, kv_indptr, kv_lens, dra
         _stream_ptr(stream))
     _check(st, "mla_verify_attn")
     return out, lse
+
+
+def build_indices(plan: Plan, req_to_token, req_pool_indices, prefix_lens, kv_indices=None,
+                  kv_indptr=None, kv_lens=None, stream=None):
+    """Per-step index builder on the plan's device; returns (kv_indices,
+    kv_indptr, kv_lens) ready for mla_verify_attn.
+
+    req_to_token int32 [pool_size, stride >= max_kv_len] (cache slot of each
+    token position per pool row), req_pool_indices / prefix_lens int32 [B].
+    kv_indices defaults to a buffer of B * (entries of max_kv_len) int32; its
+    length is the capacity.  Enqueued on ``stream``; no sync.
+    """
+    B = req_pool_indices.shape[0]
+    dev = torch.device("cuda", plan.device)
+    _expect(req_to_token, "req_to_token", torch.int32, dev)
+    if req_to_token.dim() != 2 or req_to_token.stride(1) != 1:
+        raise ValueError("req_to_token must be a 2-D int32 tensor with unit column stride")
+    _expect(req_pool_indices, "req_pool_indices", torch.int32, dev, (B,))
+    _expect(prefix_lens, "prefix_lens", torch.int32, dev, (B,))
+    per_req = plan.max_kv_len if plan.page_size == 1 else -(-plan.max_kv_len // 64)
+    if kv_indices is None:
+        kv_indices = torch.empty(B * per_req, dtype=torch.int32, device=dev)
+    if kv_indptr is None:
+        kv_indptr = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    if kv_lens is None:
+        kv_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    _expect(kv_indices, "kv_indices", torch.int32, dev)
+    _expect(kv_indptr, "kv_indptr", torch.int32, dev, (B + 1,))
+    _expect(kv_lens, "kv_lens", torch.int32, dev, (B,))
+    st = load_library().mla_verify_build_indices(
+        plan.handle, B, _ptr(req_to_token), int(req_to_token.stride(0)), int(req_to_token.shape[0]),
+        _ptr(req_pool_indices), _ptr(prefix_lens), _ptr(kv_indices), int(kv_indices.numel()),
+        _ptr(kv_indptr), _ptr(kv_lens), _stream_ptr(stream))
+    _check(st, "mla_verify_build_indices")
+    return kv_indices, kv_indptr, kv_lens
 
 
 def mla_verify_attn_host(plan: Plan, q, kv_cache, kv_indices, kv_indptr, kv_lens,

@@ -12,6 +12,8 @@
 #include <algorithm>
 #include <new>
 
+#include <cstdint>
+
 #include "mla_verify.h"
 #include "kernels.h"
 
@@ -337,6 +339,41 @@ int mla_verify_attn_host(mla_verify_plan* pl, int batch, const void* q_host, con
        cudaMemcpyAsync(lse_host, pl->st_lse, rows * sizeof(float), d2h, s) == cudaSuccess &&
        cudaStreamSynchronize(s) == cudaSuccess;
   return ok ? MLA_VERIFY_OK : MLA_VERIFY_ERR_CUDA;
+}
+
+int mla_verify_build_indices(mla_verify_plan* pl, int batch, const int32_t* req_to_token,
+                             int64_t stride, int pool_size, const int32_t* req_pool_indices,
+                             const int32_t* prefix_lens, int32_t* kv_indices, int64_t capacity,
+                             int32_t* kv_indptr, int32_t* kv_lens, void* stream) {
+  if (!pl || !req_to_token || !req_pool_indices || !prefix_lens || !kv_indices || !kv_indptr ||
+      !kv_lens)
+    return MLA_VERIFY_ERR_NULL;
+  if (!aligned16(req_to_token) || !aligned16(req_pool_indices) || !aligned16(prefix_lens) ||
+      !aligned16(kv_indices) || !aligned16(kv_indptr) || !aligned16(kv_lens))
+    return MLA_VERIFY_ERR_ALIGN;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  if (stride < pl->max_kv_len || pool_size < 1 || capacity < 0 || capacity > INT32_MAX)
+    return MLA_VERIFY_ERR_ARG;
+  const int dev_status = check_device(pl);
+  if (dev_status != MLA_VERIFY_OK) return dev_status;
+  mlav::IndexArgs a{};
+  a.req_to_token = req_to_token;
+  a.stride = stride;
+  a.pool_size = pool_size;
+  a.req_pool_indices = req_pool_indices;
+  a.prefix_lens = prefix_lens;
+  a.batch = batch;
+  a.T = pl->T;
+  a.page_size = pl->page_size;
+  a.max_kv_len = pl->max_kv_len;
+  a.capacity = capacity;
+  a.kv_indices = kv_indices;
+  a.kv_indptr = kv_indptr;
+  a.kv_lens = kv_lens;
+  a.err = pl->err;
+  if (mlav::launch_build_indices(a, pl->max_kv_len, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_VERIFY_ERR_CUDA;
+  return MLA_VERIFY_OK;
 }
 
 int mla_verify_get_error(mla_verify_plan* pl, int* device_status, int clear) {

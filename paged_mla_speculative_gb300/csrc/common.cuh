@@ -22,6 +22,8 @@ enum : int {
   ERR_INDPTR = 8,
   ERR_TIMEOUT = 16,
   ERR_INTERNAL = 32,
+  ERR_POOL = 64,       // index builder: pool row, prefix or length out of range
+  ERR_CAPACITY = 128,  // index builder: kv_indices capacity exceeded
 };
 
 // Arguments of one verify call, shared by every kernel of the call.

@@ -27,4 +27,20 @@ cudaError_t launch_pack_kv(const Params& p, void* packed, int max_blocks, cudaSt
 // LSE combine of the split partials into out/lse.
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool overlap);
 
+// Per-step index builder (index_builder.cu).
+struct IndexArgs {
+  const int32_t* req_to_token;      // [pool_size][stride] cache slot of each token position
+  long long stride;                 // entries per table row (>= max_kv_len)
+  int pool_size;
+  const int32_t* req_pool_indices;  // [batch]
+  const int32_t* prefix_lens;       // [batch]
+  int batch, T, page_size, max_kv_len;
+  long long capacity;               // entries kv_indices holds (<= INT32_MAX)
+  int32_t* kv_indices;
+  int32_t* kv_indptr;               // [batch + 1]
+  int32_t* kv_lens;                 // [batch]
+  int* err;
+};
+cudaError_t launch_build_indices(const IndexArgs& a, int max_kv_len, cudaStream_t stream);
+
 }  // namespace mlav
