@@ -85,6 +85,57 @@ def profiled_traffic(workload):
     return None
 
 
+def small_r_timing(mb, W, name, flush, stream, steps):
+    """µs per call, KV GB/s and the fraction of the HBM roof for one of the
+    small-R workloads (L2 flushed before every call, events on the stream)."""
+    import torch
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, device="cuda")
+    work = W.algorithmic_work(inp.prefix, w.num_drafts, w.num_heads)
+    plan = mb.Plan(w.batch, w.num_drafts, w.num_heads, w.page_size, w.num_slots,
+                   max(inp.kv_lens.tolist()))
+    out, lse = plan.new_outputs(w.batch)
+
+    def call():
+        mb.mla_verify_attn(plan, inp.q, inp.kv_cache, inp.kv_indices, inp.kv_indptr,
+                           inp.kv_lens, inp.draft_parent, inp.scale, out, lse, stream=stream)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ea[i].record(stream)
+        call()
+        eb[i].record(stream)
+    torch.cuda.synchronize()
+    assert plan.get_error() == 0
+    us = statistics.fmean(a.elapsed_time(b) for a, b in zip(ea, eb)) * 1e3
+    peaks, _ = load_peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    kv_gbs = work["kv_bytes"] / (us * 1e-6) / 1e9
+    tc = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    t_hbm, t_tc = work["bytes"] / (hbm * 1e9), work["flops"] / (tc * 1e12)
+    t_roof = max(t_hbm, t_tc) * 1e6
+    res = {"us_per_call": us, "kv_gbs": kv_gbs, "kv_frac_of_hbm": kv_gbs / hbm,
+           "roofline_time_us": t_roof, "frac_of_roofline": t_roof / us,
+           "bound": "hbm" if t_hbm > t_tc else "tensor",
+           "nsplit": plan.nsplit(w.batch), "rows_per_request": w.num_drafts * w.num_heads}
+    plan.close()
+    return res
+
+
+def kernels_of(kernel, ns):
+    """The library kernels one call launches, for the JSON line."""
+    from paged_mla_speculative_gb300 import binding as mb
+    names = {mb.KERNEL_TC: ["pack_kv_kernel", "partial_tc_kernel"],
+             mb.KERNEL_MMA: ["partial_mma_kernel"]}[kernel]
+    return " + ".join(names + (["combine_kernel"] if ns > 1 else []))
+
+
 def index_builder_timing(mb, plan, inp, w, flush, stream, steps):
     """Mean µs of mla_verify_build_indices for this step's requests (L2
     flushed before each build), its algorithmic bytes and GB/s."""
@@ -430,6 +481,11 @@ def run_gb300(args):
     # holds each request's slots (pool rows permuted); time the build alone.
     ib = index_builder_timing(mb, plan, inp, w, flush, stream, min(K, 300))
 
+    # The small-R regime (a tensor-parallel head slice, one-token decode):
+    # HBM is the roof there; same call protocol, fewer calls.
+    small_r = {name: small_r_timing(mb, W, name, flush, stream, min(K, 200))
+               for name in ("decode_tp8", "decode_t1")}
+
     # CUDA-graph replay of the same call (capture-safe path), device timed.
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -486,14 +542,14 @@ def run_gb300(args):
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     t_roof_us = max(work["bytes"] / (hbm * 1e9), flops / (peak * 1e12)) * 1e6
     clocks = clk.summary()
-    launches = K * (3 if ns > 1 else 2)
+    launches = K * (len(kernels_of(plan.kernel(), ns).split(" + ")))
 
     line = {
         "metric": "verify_attn_us_per_call", "value": us_per_call, "unit": "us/call",
         "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": mean_call,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded), bf16 inputs resident in HBM",
-        "config": config_of(w, {"nsplit": ns, "kernels": "pack_kv_kernel + partial_tc_kernel + combine_kernel"}),
+        "config": config_of(w, {"nsplit": ns, "kernels": kernels_of(plan.kernel(), ns)}),
         "us_per_call_p10_p50_p90": [q[0] * 1e3, statistics.median(call_ms) * 1e3, q[-1] * 1e3],
         "pack_us": mean_pack * 1e3, "partial_us": mean_part * 1e3, "combine_us": mean_comb * 1e3,
         "serialised_us_per_call": statistics.fmean(prof_call_ms) * 1e3,
@@ -505,6 +561,7 @@ def run_gb300(args):
                      "kernel": "partial_tc_kernel",
                      "peak_source": f"{peak_src} bf16 burst (fp16 has the same tensor rate)"},
         "index_builder": ib,
+        "small_r": small_r,
         "clocks": clocks, "gpu_launches": launches,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -95,10 +95,12 @@ extern "C" {
 #define MLA_VERIFY_OUT_F32            0
 #define MLA_VERIFY_OUT_BF16           1
 
-/* Kernel family for the partial (split-KV) step. */
+/* Kernel family for the partial (split-KV) step; AUTO = TC. */
 #define MLA_VERIFY_KERNEL_AUTO        0
 #define MLA_VERIFY_KERNEL_MMA         1   /* warp-level mma.sync, O in registers   */
-#define MLA_VERIFY_KERNEL_TC          2   /* tcgen05 MMAs, O^T in tensor memory    */
+#define MLA_VERIFY_KERNEL_TC          2   /* tcgen05 MMAs, O^T in tensor memory;
+                                             key rows gathered once per call by a
+                                             pack kernel, streamed by bulk copies */
 
 typedef struct mla_verify_plan mla_verify_plan;
 
@@ -135,6 +137,9 @@ int mla_verify_plan_get_nsplit(const mla_verify_plan* plan, int batch);
 
 /* Select the partial-kernel family (MLA_VERIFY_KERNEL_*; AUTO = TC). */
 int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
+
+/* The kernel family calls will run (AUTO resolved), or < 0. */
+int mla_verify_plan_get_kernel(const mla_verify_plan* plan);
 
 /*
  * Profiling hook.  Later mla_verify_attn calls record `after_pack` (if not

@@ -47,6 +47,7 @@ SIGNATURES = {
     "mla_verify_plan_set_nsplit": (_I, [_P, _I]),
     "mla_verify_plan_get_nsplit": (_I, [_P, _I]),
     "mla_verify_plan_set_kernel": (_I, [_P, _I]),
+    "mla_verify_plan_get_kernel": (_I, [_P]),
     "mla_verify_plan_workspace_bytes": (ctypes.c_size_t, [_P]),
     "mla_verify_plan_set_profile_events": (_I, [_P, _P, _P]),
     "mla_verify_attn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
@@ -157,6 +158,13 @@ class Plan:
 
     def set_kernel(self, kernel: int):
         _check(load_library().mla_verify_plan_set_kernel(self.handle, kernel), "set_kernel")
+
+    def kernel(self) -> int:
+        """The kernel family calls run (KERNEL_MMA or KERNEL_TC)."""
+        v = load_library().mla_verify_plan_get_kernel(self.handle)
+        if v < 0:
+            raise MlaVerifyError(v, "get_kernel")
+        return v
 
     def set_profile_events(self, after_pack=None, after_partial=None):
         """Record torch.cuda.Events (timing enabled) after the pack kernel and

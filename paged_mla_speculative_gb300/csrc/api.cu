@@ -240,6 +240,11 @@ int mla_verify_plan_set_kernel(mla_verify_plan* pl, int kernel) {
   return MLA_VERIFY_OK;
 }
 
+int mla_verify_plan_get_kernel(const mla_verify_plan* pl) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  return pl->kernel;
+}
+
 int mla_verify_plan_set_profile_events(mla_verify_plan* pl, void* after_pack, void* after_partial) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   pl->ev_after_pack = static_cast<cudaEvent_t>(after_pack);
@@ -297,7 +302,7 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   // the kernels run back to back so that each event brackets one kernel.
   const bool overlap = !pl->ev_after_pack && !pl->ev_after_partial;
   cudaError_t le = cudaSuccess;
-  if (pl->kernel != MLA_VERIFY_KERNEL_MMA)
+  if (pl->kernel == MLA_VERIFY_KERNEL_TC)
     le = mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)

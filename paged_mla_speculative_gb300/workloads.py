@@ -95,6 +95,15 @@ WORKLOADS = {
                             num_heads=64, prefix=("uniform", 512, 131072),
                             tree="random", num_slots=4194304, page_size=64,
                             seed=4),
+    # The small-R regime, where one key row serves few query rows and HBM is
+    # the roof: a tensor-parallel slice of the heads (16 of them) verifying 4
+    # drafts, and plain one-token decode over all 128 heads.
+    "decode_tp8": Workload(name="decode_tp8", batch=16, num_drafts=4,
+                           num_heads=16, prefix=(4096,) * 16, tree="chain",
+                           num_slots=131072, spike_frac=0.01, seed=5),
+    "decode_t1": Workload(name="decode_t1", batch=32, num_drafts=1,
+                          num_heads=128, prefix=(2048,) * 32, tree="chain",
+                          num_slots=131072, spike_frac=0.01, seed=6),
 }
 
 

@@ -165,7 +165,7 @@ def test_page_size_64_matches_page_size_1_bits():
 
 # ------------------------------------------------------------ full size
 FULL = ["decode_batch", "tree", "sweep_p1024", "sweep_p4096", "sweep_p16384", "sweep_p65536",
-        "sweep_p93184", "ragged_ps1", "ragged_ps64"]
+        "sweep_p93184", "ragged_ps1", "ragged_ps64", "decode_tp8", "decode_t1"]
 
 
 @pytest.mark.parametrize("name", FULL)
