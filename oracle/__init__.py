@@ -32,7 +32,8 @@ tree mask.
 
 ``index_builder_ref.build_indices`` restates the per-step index builder (the
 request-to-token table turned into the slot or page table the attention
-reads); its pins are in tests/test_index_builder_pins.py.
+reads); its pins are in tests/test_index_builder_pins.py.  ``compact_ref.compact_kv``
+restates KV compaction into 64-row pages (pins: tests/test_compact_pins.py).
 
 Pins (tests/test_oracle_pins.py): pure-Python brute force on tiny inputs, a
 hand-derived closed-form fixture (tests/golden/), one-visible-key, identical
