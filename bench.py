@@ -85,6 +85,44 @@ def profiled_traffic(workload):
     return None
 
 
+def compaction_timing(mb, plan, inp, w, flush, stream, steps):
+    """µs and GB/s of compacting the step's requests into fresh 64-row pages
+    (L2 flushed before each call); bytes = rows read + rows written."""
+    import torch
+    if inp.page_size != 1:
+        return None
+    pages_needed = sum((int(n) + 63) // 64 for n in inp.kv_lens.tolist())
+    dst = torch.empty((pages_needed * 64, 576), dtype=torch.bfloat16, device="cuda")
+    free = torch.arange(pages_needed, dtype=torch.int32, device="cuda")
+    table = torch.empty(pages_needed, dtype=torch.int32, device="cuda")
+    pin = torch.empty(w.batch + 1, dtype=torch.int32, device="cuda")
+
+    def call():
+        mb.compact_kv(plan, inp.kv_cache, inp.kv_indices, inp.kv_indptr, inp.kv_lens, free, dst,
+                      table, pin, stream=stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    assert plan.get_error() == 0 and torch.equal(table, free)
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ea[i].record(stream)
+        call()
+        eb[i].record(stream)
+    torch.cuda.synchronize()
+    us = statistics.fmean(a.elapsed_time(b) for a, b in zip(ea, eb)) * 1e3
+    rows = int(inp.kv_lens.sum())
+    nbytes = rows * 1152 * 2 + rows * 4 + pages_needed * 8 + (w.batch + 1) * 8
+    peaks, _ = load_peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": us, "pages": pages_needed, "algorithmic_bytes": nbytes, "gbs": gbs,
+            "frac_of_hbm": gbs / hbm, "bound": "hbm", "launches": 2}
+
+
 def small_r_timing(mb, W, name, flush, stream, steps):
     """µs per call, KV GB/s and the fraction of the HBM roof for one of the
     small-R workloads (L2 flushed before every call, events on the stream)."""
@@ -481,6 +519,9 @@ def run_gb300(args):
     # holds each request's slots (pool rows permuted); time the build alone.
     ib = index_builder_timing(mb, plan, inp, w, flush, stream, min(K, 300))
 
+    # KV compaction of this step's requests into fresh 64-row pages.
+    compaction = compaction_timing(mb, plan, inp, w, flush, stream, min(K, 200))
+
     # The small-R regime (a tensor-parallel head slice, one-token decode):
     # HBM is the roof there; same call protocol, fewer calls.
     small_r = {name: small_r_timing(mb, W, name, flush, stream, min(K, 200))
@@ -562,6 +603,7 @@ def run_gb300(args):
                      "peak_source": f"{peak_src} bf16 burst (fp16 has the same tensor rate)"},
         "index_builder": ib,
         "small_r": small_r,
+        "compaction": compaction,
         "clocks": clocks, "gpu_launches": launches,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -239,6 +239,47 @@ int mla_verify_build_indices(mla_verify_plan* plan, int batch, const int32_t* re
                              int32_t* kv_indptr, int32_t* kv_lens, void* stream);
 
 /*
+ * KV compaction: copies each request's page_size 1 rows, in logical order,
+ * into fresh 64-row pages of `kv_dst` taken in order from `free_pages`, and
+ * writes the page_size 64 table of the same requests -- the defragmentation
+ * the pages name as a step after the custom verify kernel ("The Moment of
+ * Truth: Benchmarking a Custom sm_120 Verify Kernel Against Triton", section
+ * "The Broader Context: From Kernel to System"), so that later verify steps
+ * of those requests can run with page_size 64 over contiguous pages.
+ *
+ *   kv_src        bf16 [src_slots][576], the page_size 1 cache.
+ *   kv_indices, kv_indptr [batch + 1], kv_lens [batch]: the requests' page_size
+ *                 1 slot table (as for mla_verify_attn).
+ *   free_pages    int32 [num_free_pages]: destination page ids, used in order.
+ *   kv_dst        bf16 [dst_slots][576], dst_slots a multiple of 64.  It may be
+ *                 kv_src itself when no destination page holds a row that a
+ *                 request of this call reads.
+ *   page_table    int32 [num_free_pages] out: the consumed prefix of free_pages.
+ *   page_indptr   int32 [batch + 1] out: request b's pages are
+ *                 page_table[page_indptr[b] .. page_indptr[b+1]).
+ *
+ * Row j of request b goes to slot page_table[page_indptr[b] + j / 64] * 64 +
+ * j % 64; the rest of a request's last page is left unchanged; kv_lens stays
+ * valid for the new table.  Device-side problems set sticky bits and never
+ * fault: a length outside [0, max_kv_len] or an indptr range that does not
+ * hold kv_lens[b] slots inside [0, kv_indptr[batch]) gives the request no
+ * pages (MLA_VERIFY_DEV_BAD_LEN / BAD_INDPTR); when the free pages run out
+ * the longest leading run of requests that fits keeps its pages, every later
+ * request gets none (MLA_VERIFY_DEV_CAPACITY); a source slot outside kv_src
+ * is copied as a zero row and a page outside kv_dst is not written
+ * (MLA_VERIFY_DEV_BAD_SLOT).  Host-side errors as for mla_verify_attn (null or
+ * misaligned pointers, batch outside [1, max_batch]; src_slots or
+ * num_free_pages outside [0, 2^31), dst_slots not a positive multiple of 64
+ * below 2^31 give MLA_VERIFY_ERR_ARG).  Allocates nothing, does not
+ * synchronise.
+ */
+int mla_verify_compact_kv(mla_verify_plan* plan, int batch, const void* kv_src, int64_t src_slots,
+                          const int32_t* kv_indices, const int32_t* kv_indptr,
+                          const int32_t* kv_lens, const int32_t* free_pages,
+                          int64_t num_free_pages, void* kv_dst, int64_t dst_slots,
+                          int32_t* page_table, int32_t* page_indptr, void* stream);
+
+/*
  * Allocation-free verify attention, for callers that cannot allocate device
  * memory: code running inside a memory pool that owns the whole device, a
  * serving loop that must not allocate after start-up, or a layer that is only

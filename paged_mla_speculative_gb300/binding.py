@@ -57,6 +57,8 @@ SIGNATURES = {
                                     ctypes.c_float, _P, _P, _P, _P]),
     "mla_verify_build_indices": (_I, [_P, _I, _P, ctypes.c_int64, _I, _P, _P, _P, ctypes.c_int64,
                                       _P, _P, _P]),
+    "mla_verify_compact_kv": (_I, [_P, _I, _P, ctypes.c_int64, _P, _P, _P, _P, ctypes.c_int64, _P,
+                                   ctypes.c_int64, _P, _P, _P]),
     "mla_verify_strerror": (ctypes.c_char_p, [_I]),
     "mla_verify_version": (_I, []),
 }
@@ -276,6 +278,39 @@ def build_indices(plan: Plan, req_to_token, req_pool_indices, prefix_lens, kv_in
         _ptr(kv_indptr), _ptr(kv_lens), _stream_ptr(stream))
     _check(st, "mla_verify_build_indices")
     return kv_indices, kv_indptr, kv_lens
+
+
+def compact_kv(plan: Plan, kv_src, kv_indices, kv_indptr, kv_lens, free_pages, kv_dst,
+               page_table=None, page_indptr=None, stream=None):
+    """KV compaction into 64-row pages on the plan's device; returns
+    (page_table, page_indptr), the page_size 64 table of the same requests.
+
+    kv_src [S, 576] / kv_dst [S2, 576] bf16 (S2 a multiple of 64),
+    kv_indices / kv_indptr / kv_lens int32 (page_size 1 table), free_pages
+    int32 destination page ids used in order.  Enqueued on ``stream``; no sync.
+    """
+    B = kv_lens.shape[0]
+    dev = torch.device("cuda", plan.device)
+    for t, name in ((kv_src, "kv_src"), (kv_dst, "kv_dst")):
+        _expect(t, name, torch.bfloat16, dev)
+        if t.dim() != 2 or t.shape[1] != 576:
+            raise ValueError(f"{name} must be [slots, 576]")
+    _expect(kv_indices, "kv_indices", torch.int32, dev)
+    _expect(kv_indptr, "kv_indptr", torch.int32, dev, (B + 1,))
+    _expect(kv_lens, "kv_lens", torch.int32, dev, (B,))
+    _expect(free_pages, "free_pages", torch.int32, dev)
+    if page_table is None:
+        page_table = torch.empty(max(free_pages.numel(), 4), dtype=torch.int32, device=dev)
+    if page_indptr is None:
+        page_indptr = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    _expect(page_table, "page_table", torch.int32, dev)
+    _expect(page_indptr, "page_indptr", torch.int32, dev, (B + 1,))
+    st = load_library().mla_verify_compact_kv(
+        plan.handle, B, _ptr(kv_src), int(kv_src.shape[0]), _ptr(kv_indices), _ptr(kv_indptr),
+        _ptr(kv_lens), _ptr(free_pages), int(free_pages.numel()), _ptr(kv_dst),
+        int(kv_dst.shape[0]), _ptr(page_table), _ptr(page_indptr), _stream_ptr(stream))
+    _check(st, "mla_verify_compact_kv")
+    return page_table, page_indptr
 
 
 def mla_verify_attn_host(plan: Plan, q, kv_cache, kv_indices, kv_indptr, kv_lens,

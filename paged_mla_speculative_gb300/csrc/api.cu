@@ -381,6 +381,45 @@ int mla_verify_build_indices(mla_verify_plan* pl, int batch, const int32_t* req_
   return MLA_VERIFY_OK;
 }
 
+int mla_verify_compact_kv(mla_verify_plan* pl, int batch, const void* kv_src, int64_t src_slots,
+                          const int32_t* kv_indices, const int32_t* kv_indptr,
+                          const int32_t* kv_lens, const int32_t* free_pages,
+                          int64_t num_free_pages, void* kv_dst, int64_t dst_slots,
+                          int32_t* page_table, int32_t* page_indptr, void* stream) {
+  if (!pl || !kv_src || !kv_indices || !kv_indptr || !kv_lens || !free_pages || !kv_dst ||
+      !page_table || !page_indptr)
+    return MLA_VERIFY_ERR_NULL;
+  if (!aligned16(kv_src) || !aligned16(kv_indices) || !aligned16(kv_indptr) ||
+      !aligned16(kv_lens) || !aligned16(free_pages) || !aligned16(kv_dst) ||
+      !aligned16(page_table) || !aligned16(page_indptr))
+    return MLA_VERIFY_ERR_ALIGN;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  if (src_slots < 0 || src_slots > INT32_MAX || num_free_pages < 0 ||
+      num_free_pages > INT32_MAX || dst_slots <= 0 || dst_slots > INT32_MAX ||
+      dst_slots % mlav::PAGE)
+    return MLA_VERIFY_ERR_ARG;
+  const int dev_status = check_device(pl);
+  if (dev_status != MLA_VERIFY_OK) return dev_status;
+  mlav::CompactArgs a{};
+  a.kv_src = kv_src;
+  a.src_slots = src_slots;
+  a.kv_indices = kv_indices;
+  a.kv_indptr = kv_indptr;
+  a.kv_lens = kv_lens;
+  a.free_pages = free_pages;
+  a.num_free_pages = num_free_pages;
+  a.kv_dst = kv_dst;
+  a.dst_slots = dst_slots;
+  a.page_table = page_table;
+  a.page_indptr = page_indptr;
+  a.batch = batch;
+  a.max_kv_len = pl->max_kv_len;
+  a.err = pl->err;
+  if (mlav::launch_compact_kv(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_VERIFY_ERR_CUDA;
+  return MLA_VERIFY_OK;
+}
+
 int mla_verify_get_error(mla_verify_plan* pl, int* device_status, int clear) {
   if (!pl || !device_status) return MLA_VERIFY_ERR_NULL;
   const int dev_status = check_device(pl);

@@ -43,4 +43,22 @@ struct IndexArgs {
 };
 cudaError_t launch_build_indices(const IndexArgs& a, int max_kv_len, cudaStream_t stream);
 
+// KV compaction into 64-row pages (compact.cu).
+struct CompactArgs {
+  const void* kv_src;               // bf16 [src_slots][576]
+  long long src_slots;
+  const int32_t* kv_indices;        // page_size 1 slot table of the requests
+  const int32_t* kv_indptr;         // [batch + 1]
+  const int32_t* kv_lens;           // [batch]
+  const int32_t* free_pages;        // [num_free_pages] destination page ids, used in order
+  long long num_free_pages;
+  void* kv_dst;                     // bf16 [dst_slots][576], dst_slots a multiple of 64
+  long long dst_slots;
+  int32_t* page_table;              // [num_free_pages] out
+  int32_t* page_indptr;             // [batch + 1] out
+  int batch, max_kv_len;
+  int* err;
+};
+cudaError_t launch_compact_kv(const CompactArgs& a, cudaStream_t stream);
+
 }  // namespace mlav
