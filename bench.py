@@ -166,10 +166,12 @@ def small_r_timing(mb, W, name, flush, stream, steps):
     return res
 
 
-def kernels_of(kernel, ns):
-    """The library kernels one call launches, for the JSON line."""
+def kernels_of(kernel, ns, pack_stay=0):
+    """The library kernels one call launches, for the JSON line (pack_stay >
+    0: the pack that overlaps the attention kernel)."""
     from paged_mla_speculative_gb300 import binding as mb
-    names = {mb.KERNEL_TC: ["pack_kv_kernel", "partial_tc_kernel"],
+    pack = "pack_kv_overlap_kernel" if pack_stay > 0 else "pack_kv_kernel"
+    names = {mb.KERNEL_TC: [pack, "partial_tc_kernel"],
              mb.KERNEL_MMA: ["partial_mma_kernel"]}[kernel]
     return " + ".join(names + (["combine_kernel"] if ns > 1 else []))
 
@@ -583,14 +585,16 @@ def run_gb300(args):
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     t_roof_us = max(work["bytes"] / (hbm * 1e9), flops / (peak * 1e12)) * 1e6
     clocks = clk.summary()
-    launches = K * (len(kernels_of(plan.kernel(), ns).split(" + ")))
+    pack_wide, pack_stay = plan.pack_schedule(w.batch)
+    launches = K * (len(kernels_of(plan.kernel(), ns, pack_stay).split(" + ")))
 
     line = {
         "metric": "verify_attn_us_per_call", "value": us_per_call, "unit": "us/call",
         "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": mean_call,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded), bf16 inputs resident in HBM",
-        "config": config_of(w, {"nsplit": ns, "kernels": kernels_of(plan.kernel(), ns)}),
+        "config": config_of(w, {"nsplit": ns, "kernels": kernels_of(plan.kernel(), ns, pack_stay),
+                                "pack_schedule": {"wide_positions": pack_wide, "overlap_ctas": pack_stay}}),
         "us_per_call_p10_p50_p90": [q[0] * 1e3, statistics.median(call_ms) * 1e3, q[-1] * 1e3],
         "pack_us": mean_pack * 1e3, "partial_us": mean_part * 1e3, "combine_us": mean_comb * 1e3,
         "serialised_us_per_call": statistics.fmean(prof_call_ms) * 1e3,

@@ -135,6 +135,17 @@ int mla_verify_plan_set_nsplit(mla_verify_plan* plan, int nsplit);
 /* The split count a call with `batch` requests will use (>= 1), or < 0. */
 int mla_verify_plan_get_nsplit(const mla_verify_plan* plan, int batch);
 
+/*
+ * The key-pack schedule of the TC family for a call with `batch` requests
+ * and no profiling events.  *stay > 0: the pack overlaps the attention
+ * kernel -- every SM but *stay packs the first *wide 128-key blocks of every
+ * split, then *stay pack CTAs keep packing the rest on the SMs the attention
+ * grid leaves idle while it runs.  *stay = 0: the whole pack runs before the
+ * attention kernel starts (*wide = all positions).  The MMA family packs
+ * nothing (both 0).  MLA_VERIFY_OK, or < 0 (NULL pointer, bad batch).
+ */
+int mla_verify_plan_get_pack_schedule(const mla_verify_plan* plan, int batch, int* wide, int* stay);
+
 /* Select the partial-kernel family (MLA_VERIFY_KERNEL_*; AUTO = TC). */
 int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
 
@@ -150,14 +161,17 @@ int mla_verify_plan_get_kernel(const mla_verify_plan* plan);
  * partial kernel and the combine separately.  Both must be cudaEvent_t
  * created with timing enabled; the records are ordinary stream operations and
  * are captured into graphs like the kernels.  Pass NULLs to stop.  Without
- * events each kernel of a call may start while the previous one finishes
- * (programmatic dependent launch); with events they run back to back, so the
- * split times each kernel alone and the call as a whole is a little slower.
+ * events each kernel of a call may start while the previous one runs
+ * (programmatic dependent launch; the TC partial kernel streams each packed
+ * block as soon as the pack kernel has published it); with events they run
+ * back to back, so the split times each kernel alone and the call as a whole
+ * is slower.
  */
 int mla_verify_plan_set_profile_events(mla_verify_plan* plan, void* after_pack,
                                        void* after_partial);
 
-/* Bytes of device workspace the plan holds (partials + error word). */
+/* Bytes of device workspace the plan holds (partials, packed key blocks,
+ * pack hand-off flags, error word). */
 size_t mla_verify_plan_workspace_bytes(const mla_verify_plan* plan);
 
 /*

@@ -46,6 +46,8 @@ SIGNATURES = {
     "mla_verify_plan_destroy": (None, [_P]),
     "mla_verify_plan_set_nsplit": (_I, [_P, _I]),
     "mla_verify_plan_get_nsplit": (_I, [_P, _I]),
+    "mla_verify_plan_get_pack_schedule": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int),
+                                              ctypes.POINTER(ctypes.c_int)]),
     "mla_verify_plan_set_kernel": (_I, [_P, _I]),
     "mla_verify_plan_get_kernel": (_I, [_P]),
     "mla_verify_plan_workspace_bytes": (ctypes.c_size_t, [_P]),
@@ -157,6 +159,16 @@ class Plan:
         if v < 0:
             raise MlaVerifyError(v, "get_nsplit")
         return v
+
+    def pack_schedule(self, batch: int):
+        """(wide, stay) of the key pack for `batch` requests: stay > 0 when the
+        pack overlaps the attention kernel (see the C header)."""
+        wide, stay = ctypes.c_int(), ctypes.c_int()
+        rc = load_library().mla_verify_plan_get_pack_schedule(self.handle, batch, ctypes.byref(wide),
+                                                              ctypes.byref(stay))
+        if rc != 0:
+            raise MlaVerifyError(rc, "get_pack_schedule")
+        return wide.value, stay.value
 
     def set_kernel(self, kernel: int):
         _check(load_library().mla_verify_plan_set_kernel(self.handle, kernel), "set_kernel")

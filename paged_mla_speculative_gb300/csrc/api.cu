@@ -47,6 +47,7 @@ struct mla_verify_plan {
   // Packed fp16 key blocks for the TC kernel: max_batch x pack_blocks blocks.
   void* packed;
   int pack_blocks;
+  unsigned* pack_sync;    // epoch, ticket, per-quarter ready flags (see Params)
 };
 
 namespace {
@@ -90,11 +91,43 @@ int effective_nsplit(const mla_verify_plan* pl, int batch) {
       pl->forced_nsplit, ceil_div(pl->max_kv_len, keys_per_block(pl->kernel))));
 }
 
+// Pack schedule (see pack_kv.cu).  When the kernels may overlap and the
+// attention grid leaves at least kMinPackSms SMs idle, the two-phase pack:
+// `stay` = those idle SMs keep packing while the attention kernel runs, the
+// others first pack the `wide` leading block positions of every split.
+// `wide` is the fewest positions that keep the narrow phase ahead of the
+// attention kernel, from rates measured on GB300: ~0.15 blocks/us per
+// packing SM, one 128-key block per ~3.4 us per attention CTA, ~5 us before
+// its first block.  When that needs more than half the positions, or
+// otherwise, the whole pack runs first (stay = 0).
+struct PackSchedule {
+  int wide, stay;
+};
+constexpr int kMinPackSms = 16;
+PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, bool overlap) {
+  const int positions = static_cast<int>(ceil_div(pl->pack_blocks, p.nsplit));
+  const long long attn = 1LL * p.nsplit * ceil_div(p.R, kRowsPerTile) * p.batch;
+  const long long idle = pl->num_sms - attn;
+  const PackSchedule whole{positions, 0};
+  if (!overlap || idle < kMinPackSms) return whole;
+  const double per_block_us = 3.4, lead_us = 5.0, blocks_per_us_per_sm = 0.15;
+  const double narrow_us = static_cast<double>(p.nsplit) * p.batch / (idle * blocks_per_us_per_sm);
+  // Position q >= wide is ready after (q - wide + 1) narrow steps and needed
+  // after lead + q attention steps; with narrow steps the slower, the last
+  // position binds.
+  int wide = 1;
+  if (narrow_us > per_block_us)
+    wide = static_cast<int>(std::ceil(positions - (lead_us + (positions - 1) * per_block_us) / narrow_us));
+  wide = std::max(1, wide);
+  if (2 * wide > positions) return whole;
+  return PackSchedule{wide, static_cast<int>(idle)};
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_all(mla_verify_plan* p) {
   void* bufs[] = {p->ws_o, p->ws_lse, p->err, p->st_q, p->st_idx, p->st_indptr,
-                  p->st_lens, p->st_parent, p->st_out, p->st_lse, p->packed};
+                  p->st_lens, p->st_parent, p->st_out, p->st_lse, p->packed, p->pack_sync};
   for (void* b : bufs)
     if (b) cudaFree(b);
 }
@@ -143,7 +176,8 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
-  if (mlav::partial_mma_prepare() != cudaSuccess || mlav::partial_tc_prepare() != cudaSuccess)
+  if (mlav::partial_mma_prepare() != cudaSuccess || mlav::partial_tc_prepare() != cudaSuccess ||
+      mlav::pack_kv_prepare() != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
 
   mla_verify_plan* pl = new (std::nothrow) mla_verify_plan();
@@ -191,14 +225,18 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   const size_t packed_bytes =
       static_cast<size_t>(max_batch) * pl->pack_blocks * mlav::packed_block_bytes();
   ok = ok && cudaMalloc(&pl->packed, packed_bytes) == cudaSuccess;
+  const size_t sync_bytes =
+      (mlav::PACK_SYNC_HEADER + static_cast<size_t>(max_batch) * pl->pack_blocks * 32) * sizeof(unsigned);
+  ok = ok && cudaMalloc(&pl->pack_sync, sync_bytes) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_all(pl);
     delete pl;
     return MLA_VERIFY_ERR_OOM;
   }
-  pl->ws_bytes = rows * (mlav::D_V + 1) * sizeof(float) + 256 + packed_bytes;
-  if (cudaMemset(pl->err, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+  pl->ws_bytes = rows * (mlav::D_V + 1) * sizeof(float) + 256 + packed_bytes + sync_bytes;
+  if (cudaMemset(pl->err, 0, 256) != cudaSuccess || cudaMemset(pl->pack_sync, 0, sync_bytes) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
     free_all(pl);
     delete pl;
     return MLA_VERIFY_ERR_CUDA;
@@ -229,6 +267,22 @@ int mla_verify_plan_get_nsplit(const mla_verify_plan* pl, int batch) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
   return effective_nsplit(pl, batch);
+}
+
+int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int* wide, int* stay) {
+  if (!pl || !wide || !stay) return MLA_VERIFY_ERR_NULL;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  *wide = 0;
+  *stay = 0;
+  if (pl->kernel != MLA_VERIFY_KERNEL_TC) return MLA_VERIFY_OK;
+  mlav::Params p{};
+  p.batch = batch;
+  p.R = pl->R;
+  p.nsplit = effective_nsplit(pl, batch);
+  const PackSchedule ps = pack_schedule(pl, p, true);
+  *wide = ps.wide;
+  *stay = ps.stay;
+  return MLA_VERIFY_OK;
 }
 
 int mla_verify_plan_set_kernel(mla_verify_plan* pl, int kernel) {
@@ -295,6 +349,7 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   p.err = pl->err;
   p.packed = static_cast<const uint8_t*>(pl->packed);
   p.packed_max_blocks = pl->pack_blocks;
+  p.pack_sync = pl->pack_sync;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Each kernel may start while the one before it finishes (programmatic
@@ -302,8 +357,13 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   // the kernels run back to back so that each event brackets one kernel.
   const bool overlap = !pl->ev_after_pack && !pl->ev_after_partial;
   cudaError_t le = cudaSuccess;
-  if (pl->kernel == MLA_VERIFY_KERNEL_TC)
-    le = mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
+  if (pl->kernel == MLA_VERIFY_KERNEL_TC) {
+    const PackSchedule ps = pack_schedule(pl, p, overlap);
+    p.pack_flags = ps.stay > 0;
+    le = ps.stay > 0 ? mlav::launch_pack_kv_overlap(p, pl->packed, pl->pack_blocks, pl->num_sms, ps.wide,
+                                                    ps.stay, s)
+                     : mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
+  }
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)
     le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)

@@ -48,7 +48,16 @@ struct Params {
   int* err;                     // sticky device error word
   const uint8_t* packed;        // packed fp16 key blocks (TC kernel), see pack_kv.cu
   int packed_max_blocks;        // 128-key blocks reserved per request in `packed`
+  int pack_flags;               // 1: the pack publishes per-unit ready flags
+                                // (overlapping pack); 0: wait for its grid
+  // Hand-off between the pack and the attention kernel of one call:
+  // [0] epoch (calls completed), [1] ticket (attention CTAs done this call),
+  // [4 + 32 * (b * packed_max_blocks + kb) + g] = epoch + 1 once keys
+  // 4g .. 4g+3 of block kb of request b are packed in this call.
+  unsigned* pack_sync;
 };
+
+constexpr int PACK_SYNC_HEADER = 4;   // words before the per-quarter flags
 
 // Per-request facts every CTA of the request derives the same way.
 struct Request {

@@ -22,7 +22,15 @@ cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap
 
 // Per-call gather of the key rows into packed fp16 operand tiles.
 size_t packed_block_bytes();
+// The whole pack ahead of the attention kernel (Params::pack_flags = 0).
 cudaError_t launch_pack_kv(const Params& p, void* packed, int max_blocks, cudaStream_t stream);
+// The two-phase pack that overlaps the attention kernel (pack_flags = 1):
+// num_ctas persistent CTAs (one per SM); CTAs stay .. num_ctas-1 pack the
+// first `wide_positions` blocks of every split and exit, CTAs 0 .. stay-1
+// pack the rest.  pack_kv_prepare sets its shared-memory attributes.
+cudaError_t pack_kv_prepare();
+cudaError_t launch_pack_kv_overlap(const Params& p, void* packed, int max_blocks, int num_ctas,
+                                   int wide_positions, int stay, cudaStream_t stream);
 
 // LSE combine of the split partials into out/lse.
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool overlap);

@@ -142,6 +142,46 @@ __device__ __forceinline__ int block_slot(const Params& p, const Request& rq, in
   return static_cast<int>(s);
 }
 
+// Wait (bounded) until the pack kernel has published all 32 four-key units
+// of block kb of request b for this call: lane l watches unit l's flag with
+// acquire loads.  Whole warp; false on a timeout or an earlier abort.
+__device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsigned tag,
+                                            volatile int* abort, int* err) {
+  const int lane = threadIdx.x & 31;
+  const unsigned* flag = p.pack_sync + PACK_SYNC_HEADER +
+                         32 * (static_cast<size_t>(b) * p.packed_max_blocks + kb) + lane;
+  const long long t0 = clock64();
+  while (true) {   // every exit decision is warp-uniform
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
+    if (__all_sync(0xffffffffu, v == tag)) break;
+    if (__any_sync(0xffffffffu, *abort != 0)) return false;
+    if (__any_sync(0xffffffffu, clock64() - t0 > WAIT_LIMIT)) {
+      if (lane == 0) {
+        *abort = 1;
+        atomicOr(err, ERR_TIMEOUT);
+      }
+      __syncwarp();
+      return false;
+    }
+  }
+  // The packed bytes were written through the generic proxy; the bulk copies
+  // that follow read them through the async proxy.
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+  return true;
+}
+
+// Every CTA takes one ticket when it is done; the last one of the grid
+// advances the epoch, so the next call's pack kernel publishes a new tag.
+__device__ __forceinline__ void finish_call(const Params& p) {
+  __threadfence();
+  const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+  if (atomicAdd(p.pack_sync + 1, 1u) == total - 1) {
+    p.pack_sync[1] = 0;
+    atomicAdd(p.pack_sync, 1u);
+  }
+}
+
 __device__ __forceinline__ uint32_t widen_word(uint32_t w) {
   const float lo = __uint_as_float(w << 16);
   const float hi = __uint_as_float(w & 0xffff0000u);
@@ -208,10 +248,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     if (split == 0 && rt == 0 && tid == 0)
       atomicOr(p.err, (rq.n < p.T || rq.n > p.max_kv_len) ? ERR_LEN : ERR_INDPTR);
     write_nan_rows(p, b, split, row0, tid);
+    if (tid == 0) finish_call(p);
     return;
   }
   if (sbase & 1023) {   // swizzled operand tiles need a 1024-byte aligned base
-    if (tid == 0) atomicOr(p.err, ERR_INTERNAL);
+    if (tid == 0) {
+      atomicOr(p.err, ERR_INTERNAL);
+      finish_call(p);
+    }
     write_nan_rows(p, b, split, row0, tid);
     return;
   }
@@ -243,13 +287,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     // The whole warp runs the loop; one elected lane issues each copy.
     const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PACKED_BLOCK;
     // The packed blocks come from the pack kernel just before this one on
-    // the stream: wait for it (a no-op when launched without overlap).
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // the stream, which may still be running: with per-unit flags each block
+    // is read once its 32 units carry this call's tag, else after the whole
+    // pack grid (a no-op when launched without overlap).
+    const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
+    if (!p.pack_flags) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     int issued = 0;   // copies issued, in (block, g) order
 #pragma unroll 1
     for (int it = 0; it < nb; ++it) {
       const uint8_t* src = blocks + static_cast<size_t>(kb0 + it) * PACKED_BLOCK;
       const uint32_t prev = static_cast<uint32_t>((it - 1) & 1);
+      if (p.pack_flags && !wait_packed(p, b, kb0 + it, tag, s_abort, p.err)) break;
       for (int g = 0; g < 5; ++g) {
         // Pair g of this block overwrites pair g of the previous one (and
         // the rope chunk its P^T): wait until O^T(k-1) has read them.
@@ -547,13 +595,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   tc::fence_before_sync();
   __syncthreads();
   if (warp == MMA_WARP) tc::tmem_dealloc<TMEM_COLS>(tmem);
+  if (tid == 0) finish_call(p);
 }
 
 }  // namespace
 
 cudaError_t partial_tc_prepare() {
-  return cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SMEM_TOTAL);
+  cudaError_t e = cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
 }
 
 cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap) {

@@ -1,0 +1,137 @@
+"""The key pack overlapping the attention kernel, and the whole-pack schedule.
+
+When the attention grid leaves SMs idle, the pack keeps running on them while
+the attention kernel streams each 128-key block as soon as its ready flags
+carry the call's tag; otherwise the whole pack runs first.  Both schedules
+must give the oracle's answer, and the flags must not let a call read a
+block packed by an earlier call (repeated calls and graph replays with new
+data in the same buffers).
+"""
+import numpy as np
+import pytest
+import torch
+
+from paged_mla_speculative_gb300 import binding as mb
+from paged_mla_speculative_gb300 import workloads as W
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_mla_speculative_gb300 import build
+    build.build()
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _attention_ctas(plan, batch, rows):
+    return plan.nsplit(batch) * ((rows + 63) // 64) * batch
+
+
+def test_decode_batch_shape_overlaps():
+    """8 requests x 512 rows x 4104 keys: the attention grid leaves SMs idle,
+    so the pack keeps those and packs only the leading positions first."""
+    plan = mb.Plan(8, 8, 64, 1, 65536, 4104)
+    wide, stay = plan.pack_schedule(8)
+    idle = _sms() - _attention_ctas(plan, 8, 512)
+    positions = -(-33 // plan.nsplit(8))
+    if idle < 16:
+        assert stay == 0 and wide == positions
+    else:
+        assert stay == idle
+        assert 1 <= wide and 2 * wide <= positions
+    plan.set_kernel(mb.KERNEL_MMA)
+    assert plan.pack_schedule(8) == (0, 0)
+    plan.close()
+
+
+def test_overlapping_pack_repeated_calls():
+    w = W.Workload(name="ov", batch=4, num_drafts=8, num_heads=64, prefix=(1500, 900, 2000, 33),
+                   tree="random", num_slots=8192, spike_frac=0.01, seed=610)
+    inp = W.make_inputs(w)
+    g = G.to_cuda(inp)
+    with G.make_plan(g) as plan:
+        wide, stay = plan.pack_schedule(4)
+        assert stay > 0, (wide, stay)
+        first = None
+        for _ in range(4):
+            out, lse = G.run(plan, g)
+            assert plan.get_error() == 0
+            if first is None:
+                first = (out.clone(), lse.clone())
+            else:
+                assert torch.equal(out, first[0]) and torch.equal(lse, first[1])
+    ref_o, ref_l = G.oracle_full(inp)
+    G.assert_parity(first[0].cpu().numpy(), first[1].cpu().numpy(), ref_o, ref_l)
+
+
+def test_overlapping_pack_new_data_each_call():
+    """Same buffers, different keys and lengths every call: a block packed by
+    the previous call must never be read as this call's."""
+    cases = [W.make_inputs(W.Workload(name="ovd", batch=3, num_drafts=4, num_heads=32,
+                                      prefix=pre, tree="random", num_slots=8192,
+                                      spike_frac=0.01, seed=620 + i))
+             for i, pre in enumerate([(1800, 700, 1200), (300, 1900, 64), (1000, 1000, 1000)])]
+    dev = torch.device("cuda")
+    q = torch.empty_like(cases[0].q, device=dev)
+    cache = torch.empty_like(cases[0].kv_cache, device=dev)
+    idx = torch.zeros(max(c.kv_indices.numel() for c in cases), dtype=torch.int32, device=dev)
+    indptr = torch.empty(4, dtype=torch.int32, device=dev)
+    lens = torch.empty(3, dtype=torch.int32, device=dev)
+    par = torch.empty((3, 4), dtype=torch.int32, device=dev)
+    plan = mb.Plan(3, 4, 32, 1, 8192, 1904)
+    plan.set_nsplit(2)   # 8 block positions per split: the overlapping schedule
+    assert plan.pack_schedule(3)[1] > 0
+    for c in cases + cases[::-1]:
+        q.copy_(c.q)
+        cache.copy_(c.kv_cache)
+        idx[:c.kv_indices.numel()].copy_(c.kv_indices)
+        indptr.copy_(c.kv_indptr)
+        lens.copy_(c.kv_lens)
+        par.copy_(c.draft_parent)
+        out, lse = mb.mla_verify_attn(plan, q, cache, idx, indptr, lens, par, c.scale)
+        torch.cuda.synchronize()
+        ref_o, ref_l = G.oracle_full(c)
+        G.assert_parity(out.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+    assert plan.get_error() == 0
+    plan.close()
+
+
+def test_whole_pack_when_no_sm_is_idle():
+    """As many attention CTAs as SMs: the whole pack runs first."""
+    tiles = 8                                   # 512 rows
+    batch = max(1, _sms() // tiles)
+    w = W.Workload(name="whole", batch=batch, num_drafts=8, num_heads=64, prefix=(120,) * batch,
+                   tree="chain", num_slots=8192, spike_frac=0.01, seed=630)
+    inp = W.make_inputs(w)
+    g = G.to_cuda(inp)
+    with G.make_plan(g, nsplit=1) as plan:
+        wide, stay = plan.pack_schedule(batch)
+        if _sms() - batch * tiles < 16:
+            assert stay == 0 and wide == 1
+        out, lse = G.run(plan, g)
+        assert plan.get_error() == 0
+    ref_o, ref_l = G.oracle_full(inp)
+    G.assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+
+
+def test_profiling_events_use_the_whole_pack():
+    """With profiling events between the kernels the same overlapping-shape
+    call runs the kernels back to back; results are bit-identical."""
+    w = W.Workload(name="ev", batch=4, num_drafts=8, num_heads=64, prefix=(1500, 900, 2000, 33),
+                   tree="random", num_slots=8192, spike_frac=0.01, seed=610)
+    g = G.to_cuda(W.make_inputs(w))
+    with G.make_plan(g) as plan:
+        o1, l1 = G.run(plan, g)
+        o1, l1 = o1.clone(), l1.clone()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        plan.set_profile_events(e0, e1)
+        o2, l2 = G.run(plan, g)
+        assert plan.get_error() == 0
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
