@@ -232,6 +232,8 @@ __global__ void __maxnreg__(64) pack_kv_overlap_kernel(const Params p, uint8_t* 
   // The attention kernel may be scheduled as soon as every pack CTA runs:
   // its copy warp waits for each block's flags before reading it.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  const int cta = static_cast<int>(blockIdx.x);
+  if (cta >= stay && cta - stay >= wide_units) return;   // no unit in the wide phase: free the SM
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nq = p.nsplit * p.batch * per_split;   // blocks in the pack order
   const int4* s_tab = nullptr;
@@ -244,7 +246,6 @@ __global__ void __maxnreg__(64) pack_kv_overlap_kernel(const Params p, uint8_t* 
   const int units = UNITS_PER_BLOCK * nq;            // < 2^31 (host check)
   const int wide_end = min(wide_units, units);
   const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
-  const int cta = static_cast<int>(blockIdx.x);
   const int n = gridDim.x - stay;     // CTAs of the wide phase: warp w of CTA c takes units
   const bool wide = cta >= stay;      // w * n + c, w * n + c + 32 n, ..
   const int first = wide ? warp * n + (cta - stay) : wide_end + cta * WPC + warp;

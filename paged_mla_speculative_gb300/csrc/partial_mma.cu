@@ -39,7 +39,8 @@ constexpr int OFF_P = OFF_KV1 + SMEM_KV;
 constexpr int OFF_RED = OFF_P + SMEM_P;          // float [2][64]: block max / row sums
 constexpr int OFF_SLOT = OFF_RED + 2 * 64 * 4;    // int32 [3][64]: slot of each key, -1 if none
 constexpr int OFF_MASK = OFF_SLOT + 3 * 64 * 4;   // uint32 [32]: ancestor masks
-constexpr int SMEM_TOTAL = OFF_MASK + MAX_T * 4;
+constexpr int OFF_PAR = OFF_MASK + MAX_T * 4;     // int32 [32]: draft parents
+constexpr int SMEM_TOTAL = OFF_PAR + MAX_T * 4;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 
 // Byte offset of 16-byte chunk `c` of row `r` in a tile of 72-chunk rows.
@@ -172,7 +173,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
   const int kb0 = static_cast<int>((static_cast<long long>(split) * nblk) / p.nsplit);
   const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * nblk) / p.nsplit);
 
-  if (tid < p.T) s_mask[tid] = ancestor_mask(p.draft_parent + b * p.T, tid, p.err);
+  // Parents in one parallel load; the chains are walked in shared memory
+  // after the barrier (a walk through global memory costs one round trip a
+  // step), and the main loop's barriers order the masks before their use.
+  int* s_par = reinterpret_cast<int*>(smem + OFF_PAR);
+  if (tid < p.T) s_par[tid] = p.draft_parent[b * p.T + tid];
   // Slots of the first two blocks; later blocks' slots are fetched one
   // iteration ahead so the gather never waits on an index load.
   if (tid < BN && kb1 > kb0) {
@@ -197,6 +202,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
     load_kv_block(p, s_slot, smem + OFF_KV0, tid);
     cp_async_commit();
   }
+  if (tid < p.T) s_mask[tid] = ancestor_mask(s_par, tid, p.err);
 
   float o[32][4];
 #pragma unroll

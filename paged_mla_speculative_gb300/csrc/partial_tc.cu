@@ -68,7 +68,8 @@ constexpr int OFF_MASK = OFF_L + 64 * 4;        // uint32 [32] ancestor masks
 constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -1 past R
 constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [16] mbarriers
 constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, abort flag
-constexpr int SMEM_TOTAL = OFF_MISC + 16;
+constexpr int OFF_PAR = OFF_MISC + 16;          // int [32] draft parents
+constexpr int SMEM_TOTAL = OFF_PAR + MAX_T * 4;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
@@ -237,6 +238,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   float* s_l = reinterpret_cast<float*>(smem + OFF_L);
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
   int* s_tofr = reinterpret_cast<int*>(smem + OFF_TOFR);
+  int* s_par = reinterpret_cast<int*>(smem + OFF_PAR);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
   const uint32_t sbase = smem_u32(smem);
@@ -265,7 +267,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * nblk) / p.nsplit);
   const int nb = kb1 - kb0;
 
-  if (tid < p.T) s_mask[tid] = ancestor_mask(p.draft_parent + b * p.T, tid, p.err);
+  // Parents in one parallel load; the softmax warps walk the chains in
+  // shared memory (a walk through global memory costs one round trip a step).
+  if (tid < p.T) s_par[tid] = p.draft_parent[b * p.T + tid];
   if (tid < BM) s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
   if (tid == 0) {
     for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 1);
@@ -354,7 +358,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   } else {
     // ============================= softmax =================================
     // Q tile: 64 rows x 9 swizzled chunks (rows beyond R zero), then fp16.
+    // The ancestor masks are ready after the barrier that follows the load.
     if (nb > 0) {
+      if (tid < p.T) s_mask[tid] = ancestor_mask(s_par, tid, p.err);
       const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
 #pragma unroll 1
       for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
