@@ -6,7 +6,7 @@
 // log-sum-exp lse_s:
 //     lse = log sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * o_s.
 // A split with no visible key has lse_s = -inf and weight 0 (its o_s is not
-// read).  A NaN lse_s (request rejected by the partial kernel) makes the row
+// used).  A NaN lse_s (request rejected by the partial kernel) makes the row
 // NaN.  One warp per row; each lane owns 16 of the 512 value dims.
 #include "common.cuh"
 #include "kernels.h"
@@ -17,6 +17,7 @@ namespace mlav {
 namespace {
 
 constexpr int WARPS = 8;
+constexpr int EARLY = 4;   // splits whose rows are loaded before the weights are known
 
 __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
   // The split partials come from the kernel just before this one on the
@@ -30,6 +31,16 @@ __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
   const int ns = p.nsplit;
 
   const float L = lane < ns ? p.ws_lse[(static_cast<size_t>(b) * ns + lane) * p.R + r] : -INFINITY;
+  float4 early[EARLY][4];
+#pragma unroll
+  for (int s = 0; s < EARLY; ++s) {
+    if (s < ns) {
+      const float4* src = reinterpret_cast<const float4*>(
+          p.ws_o + ((static_cast<size_t>(b) * ns + s) * p.R + r) * D_V);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) early[s][k] = __ldcs(src + lane + 32 * k);
+    }
+  }
   const bool any_nan = __any_sync(0xffffffffu, L != L);
   float mx = L;
 #pragma unroll
@@ -44,7 +55,23 @@ __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < ns; ++s) {
+  // The first EARLY splits' rows were loaded together with the LSEs (one
+  // round trip instead of two); a split of weight 0 adds nothing (its row
+  // may be unwritten: it is never used).
+#pragma unroll
+  for (int s = 0; s < EARLY; ++s) {
+    if (s >= ns) break;
+    const float ws = __shfl_sync(0xffffffffu, w, s);
+    if (ws == 0.f) continue;  // uniform across the warp
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc[k].x += ws * early[s][k].x;
+      acc[k].y += ws * early[s][k].y;
+      acc[k].z += ws * early[s][k].z;
+      acc[k].w += ws * early[s][k].w;
+    }
+  }
+  for (int s = EARLY; s < ns; ++s) {
     const float ws = __shfl_sync(0xffffffffu, w, s);
     if (ws == 0.f) continue;  // uniform across the warp
     const float4* src = reinterpret_cast<const float4*>(
