@@ -48,6 +48,22 @@ constexpr int NTHREADS = 256;           // pack_kv_kernel
 constexpr int OV_THREADS = 1024;        // pack_kv_overlap_kernel
 constexpr int BLOCK_BYTES = 9 * BN * 128;
 
+// The key rows are read exactly once per call: load them past L1 and mark
+// them first to leave L2, so the packed blocks the attention kernel reads
+// next stay there.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 load_row_granule(const uint4* src, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(src), "l"(pol));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t widen(uint32_t w) {
   const float lo = __uint_as_float(w << 16);
   const float hi = __uint_as_float(w & 0xffff0000u);
@@ -85,6 +101,7 @@ __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8
   uint8_t* dst = packed + (static_cast<size_t>(b) * max_blocks + kb) * BLOCK_BYTES;
   constexpr int PER_THREAD = QUARTER * ROW_CHUNKS / NTHREADS;   // 9
   static_assert(QUARTER * ROW_CHUNKS == PER_THREAD * NTHREADS, "even split");
+  const uint64_t pol = evict_first_policy();
   uint4 v[PER_THREAD];
   int off[PER_THREAD];
 #pragma unroll
@@ -94,7 +111,7 @@ __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8
     const int j = key0 + jl;                // key within the block
     const int slot = s_slot[jl];
     off[u] = (q >> 3) * (BN * 128) + j * 128 + (((q & 7) ^ (j & 7)) << 4);
-    v[u] = slot >= 0 ? __ldg(reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(slot) * D_QK) + q)
+    v[u] = slot >= 0 ? load_row_granule(reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(slot) * D_QK) + q, pol)
                      : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
@@ -166,12 +183,10 @@ __device__ __forceinline__ void load_unit(const Params& p, const Unit& t, int la
   const uint4* src = reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(sk) * D_QK) + (lane & 7);
 #pragma unroll
   for (int i = 0; i < PER_LANE; ++i) v[i] = make_uint4(0, 0, 0, 0);
-  if (sk >= 0) {   // streamed once: keep L1 out of it
+  if (sk >= 0) {   // streamed once
+    const uint64_t pol = evict_first_policy();
 #pragma unroll
-    for (int i = 0; i < PER_LANE; ++i)
-      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                   : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w)
-                   : "l"(src + 8 * i));
+    for (int i = 0; i < PER_LANE; ++i) v[i] = load_row_granule(src + 8 * i, pol);
   }
 }
 
