@@ -135,3 +135,24 @@ def test_profiling_events_use_the_whole_pack():
         o2, l2 = G.run(plan, g)
         assert plan.get_error() == 0
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("page_size,out_dtype", [(64, torch.float32), (1, torch.bfloat16),
+                                                 (64, torch.bfloat16)])
+def test_overlapping_pack_pages_and_bf16(page_size, out_dtype):
+    """The overlapping schedule with a 64-row page table and with bf16 output
+    (bf16 must equal the fp32 result rounded)."""
+    w = W.Workload(name="ovp", batch=4, num_drafts=8, num_heads=64, prefix=(1500, 900, 2000, 33),
+                   tree="random", num_slots=16384, page_size=page_size, spike_frac=0.01, seed=640)
+    inp = W.make_inputs(w)
+    g = G.to_cuda(inp)
+    with G.make_plan(g, out_dtype=out_dtype) as plan:
+        assert plan.pack_schedule(4)[1] > 0
+        out, lse = G.run(plan, g)
+        assert plan.get_error() == 0
+    with G.make_plan(g) as plan32:
+        o32, l32 = G.run(plan32, g)
+    if out_dtype == torch.bfloat16:
+        assert torch.equal(out, o32.to(torch.bfloat16)) and torch.equal(lse, l32)
+    ref_o, ref_l = G.oracle_full(inp)
+    G.assert_parity(o32.cpu().numpy(), l32.cpu().numpy(), ref_o, ref_l)
