@@ -245,12 +245,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   const uint32_t mbar0 = sbase + OFF_MBAR;
   auto mbar = [&](int i) { return mbar0 + 8u * static_cast<uint32_t>(i); };
 
+  // Q tile: 64 rows x 9 swizzled chunks (rows beyond R zero), loaded by the
+  // softmax warps first -- its address needs nothing from the request, so
+  // the load overlaps the request lookup.  Every exit drains it.
+  if (warp < SOFTMAX_WARPS) {
+    const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
+#pragma unroll 1
+    for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
+      const int r = e / ROW_CHUNKS, q = e - r * ROW_CHUNKS;
+      const int gr = row0 + r;
+      const bool in = gr < p.R;
+      cp_async16(sbase + OFF_Q + (q >> 3) * Q_CHUNK + r * 128 + (((q & 7) ^ (r & 7)) << 4),
+                 in ? qb + static_cast<size_t>(gr) * D_QK + q * 8 : p.q, in ? 16 : 0);
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  }
+
   const Request rq = load_request(p, b);
   if (!rq.ok) {
     if (split == 0 && rt == 0 && tid == 0)
       atomicOr(p.err, (rq.n < p.T || rq.n > p.max_kv_len) ? ERR_LEN : ERR_INDPTR);
     write_nan_rows(p, b, split, row0, tid);
     if (tid == 0) finish_call(p);
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     return;
   }
   if (sbase & 1023) {   // swizzled operand tiles need a 1024-byte aligned base
@@ -259,6 +276,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       finish_call(p);
     }
     write_nan_rows(p, b, split, row0, tid);
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
     return;
   }
 
@@ -357,20 +375,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     }
   } else {
     // ============================= softmax =================================
-    // Q tile: 64 rows x 9 swizzled chunks (rows beyond R zero), then fp16.
-    // The ancestor masks are ready after the barrier that follows the load.
+    // The Q tile (issued at entry) to fp16.  The ancestor masks are ready
+    // after the barrier that follows the load.
     if (nb > 0) {
       if (tid < p.T) s_mask[tid] = ancestor_mask(s_par, tid, p.err);
-      const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
-#pragma unroll 1
-      for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
-        const int r = e / ROW_CHUNKS, q = e - r * ROW_CHUNKS;
-        const int gr = row0 + r;
-        const bool in = gr < p.R;
-        cp_async16(sbase + OFF_Q + (q >> 3) * Q_CHUNK + r * 128 + (((q & 7) ^ (r & 7)) << 4),
-                   in ? qb + static_cast<size_t>(gr) * D_QK + q * 8 : p.q, in ? 16 : 0);
-      }
-      asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
       named_sync(1, SOFTMAX_WARPS * 32);
 #pragma unroll 1
       for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
@@ -381,6 +390,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       tc::fence_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(mbar(MB_Q));
+    } else {
+      asm volatile("cp.async.wait_all;\n" ::: "memory");   // no key block: Q unused
     }
     const int j = quad * 32 + lane;     // key of this thread = TMEM lane
     const int hc = warp >> 2;           // query-row columns hc*32 .. +32
