@@ -156,3 +156,39 @@ def test_overlapping_pack_pages_and_bf16(page_size, out_dtype):
         assert torch.equal(out, o32.to(torch.bfloat16)) and torch.equal(lse, l32)
     ref_o, ref_l = G.oracle_full(inp)
     G.assert_parity(o32.cpu().numpy(), l32.cpu().numpy(), ref_o, ref_l)
+
+
+def test_schedules_alternate_on_one_plan():
+    """Calls on one plan switch between the whole pack (a full attention grid)
+    and the overlapping pack (few requests); every call must still read only
+    blocks packed in that call."""
+    tiles = 8                                   # 512 rows
+    big = max(1, _sms() // tiles)
+    wbig = W.Workload(name="alt_big", batch=big, num_drafts=8, num_heads=64,
+                      prefix=tuple(100 + 37 * i for i in range(big)), tree="random",
+                      num_slots=16384, spike_frac=0.01, seed=650)
+    wsmall = W.Workload(name="alt_small", batch=3, num_drafts=8, num_heads=64,
+                        prefix=(1400, 700, 1800), tree="random", num_slots=16384,
+                        spike_frac=0.01, seed=651)
+    ibig, ismall = W.make_inputs(wbig), W.make_inputs(wsmall)
+    gbig, gsmall = G.to_cuda(ibig), G.to_cuda(ismall)
+    plan = mb.Plan(big, 8, 64, 1, 16384, 1808)
+    plan.set_nsplit(1)
+    sched = {big: plan.pack_schedule(big), 3: plan.pack_schedule(3)}
+    if _sms() - big * tiles < 16:
+        assert sched[big][1] == 0
+    refs = {}
+    for i in range(6):
+        g, inp = (gbig, ibig) if i % 2 == 0 else (gsmall, ismall)
+        out, lse = mb.mla_verify_attn(plan, g.q, g.kv_cache, g.kv_indices, g.kv_indptr, g.kv_lens,
+                                      g.draft_parent, g.scale)
+        torch.cuda.synchronize()
+        key = inp.workload.name
+        if key not in refs:
+            refs[key] = G.oracle_full(inp)
+            G.assert_parity(out.cpu().numpy(), lse.cpu().numpy(), *refs[key])
+            refs[key + "_out"] = (out.clone(), lse.clone())
+        else:
+            assert torch.equal(out, refs[key + "_out"][0]) and torch.equal(lse, refs[key + "_out"][1])
+    assert plan.get_error() == 0
+    plan.close()
