@@ -47,7 +47,11 @@ struct mla_verify_plan {
   // Packed fp16 key blocks for the TC kernel: max_batch x pack_blocks blocks.
   void* packed;
   int pack_blocks;
-  unsigned* pack_sync;    // epoch, ticket, per-quarter ready flags (see Params)
+  unsigned* pack_sync;    // epoch, ticket, per-unit ready flags (see Params)
+  size_t pack_sync_bytes;
+  // A call failed after its pack kernel was launched: its flags may carry
+  // the tag the next call will use, so the next call clears them first.
+  bool pack_flags_dirty;
 };
 
 namespace {
@@ -228,6 +232,7 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   const size_t sync_bytes =
       (mlav::PACK_SYNC_HEADER + static_cast<size_t>(max_batch) * pl->pack_blocks * 32) * sizeof(unsigned);
   ok = ok && cudaMalloc(&pl->pack_sync, sync_bytes) == cudaSuccess;
+  pl->pack_sync_bytes = sync_bytes;
   if (!ok) {
     cudaGetLastError();
     free_all(pl);
@@ -357,17 +362,26 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   // the kernels run back to back so that each event brackets one kernel.
   const bool overlap = !pl->ev_after_pack && !pl->ev_after_partial;
   cudaError_t le = cudaSuccess;
-  if (pl->kernel == MLA_VERIFY_KERNEL_TC) {
+  if (pl->kernel == MLA_VERIFY_KERNEL_TC && pl->pack_flags_dirty) {
+    // Zero the flags, keep the epoch and the (reset) ticket: no tag is 0.
+    const size_t head = mlav::PACK_SYNC_HEADER * sizeof(unsigned);
+    le = cudaMemsetAsync(reinterpret_cast<uint8_t*>(pl->pack_sync) + head, 0, pl->pack_sync_bytes - head, s);
+    if (le == cudaSuccess) le = cudaMemsetAsync(pl->pack_sync + 1, 0, sizeof(unsigned), s);
+    if (le == cudaSuccess) pl->pack_flags_dirty = false;
+  }
+  if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC) {
     const PackSchedule ps = pack_schedule(pl, p, overlap);
     p.pack_flags = ps.stay > 0;
     le = ps.stay > 0 ? mlav::launch_pack_kv_overlap(p, pl->packed, pl->pack_blocks, pl->num_sms, ps.wide,
                                                     ps.stay, s)
                      : mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
   }
+  const bool packed = le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC;
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)
     le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
                                              : mlav::launch_partial_tc(p, s, overlap);
+  if (packed && le != cudaSuccess) pl->pack_flags_dirty = true;   // the epoch did not advance
   if (le == cudaSuccess && pl->ev_after_partial) le = cudaEventRecord(pl->ev_after_partial, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   if (ns > 1 && mlav::launch_combine(p, s, overlap) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;

@@ -174,12 +174,15 @@ __device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsi
 
 // Every CTA takes one ticket when it is done; the last one of the grid
 // advances the epoch, so the next call's pack kernel publishes a new tag.
+// The epoch stays below 2^32 - 1, so the tag (epoch + 1) is never 0 -- the
+// value of a flag no call has written -- and consecutive tags differ.
 __device__ __forceinline__ void finish_call(const Params& p) {
   __threadfence();
   const unsigned total = gridDim.x * gridDim.y * gridDim.z;
   if (atomicAdd(p.pack_sync + 1, 1u) == total - 1) {
     p.pack_sync[1] = 0;
-    atomicAdd(p.pack_sync, 1u);
+    const unsigned e = *reinterpret_cast<volatile unsigned*>(p.pack_sync);
+    *reinterpret_cast<volatile unsigned*>(p.pack_sync) = e + 1u == 0xffffffffu ? 0u : e + 1u;
   }
 }
 
