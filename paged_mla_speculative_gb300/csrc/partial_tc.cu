@@ -12,8 +12,8 @@
 //     O^T[dim, row] += V_block^T[512 x 128] . P^T[128 x 64]              (fp16)
 // O^T lives in tensor memory for the whole split (4 tiles of 128 dims x 64
 // rows = columns 0..255) and S^T in columns 256..319.  With one thread per
-// key the softmax reduces each query row across the 128 TMEM lanes
-// (redux.sync per warp, shared memory across four warps).  The running row
+// key the softmax reduces each query row across the 128 TMEM lanes (a
+// shuffle transpose-reduce per warp, shared memory across four warps).  The running row
 // max is exact, so P <= 1 and the key holding the max has P = 1 exactly (a
 // lazily moved max would round the dominant key's weight too, which doubles
 // the worst-case output error on spiky keys); O^T columns are rescaled in
@@ -23,12 +23,15 @@
 //
 // The key blocks come from the per-call pack (pack_kv.cu): 147456 contiguous
 // bytes per 128-key block, already fp16 and already in the 128-byte-swizzled
-// operand layout, so each chunk pair arrives with one 32 KB bulk copy.
+// operand layout, so each chunk pair arrives with one 32 KB bulk copy.  The
+// pack may still be running: the copy warp then waits for each block's
+// ready flags (tagged with the call's epoch) instead of the whole pack grid,
+// and the last CTA to finish advances the epoch.
 //
 // Roles (10 warps):
 //   warps 0-7  softmax: one thread per (key of the block, half of the 64 query
 //              rows); warps w and w+4 share TMEM lane quadrant w.  First they
-//              load the Q tile and widen it to fp16;
+//              load the Q tile (issued at entry) and widen it to fp16;
 //   warp 8     issues the MMAs (one elected lane of the converged warp); it
 //              owns the TMEM allocation;
 //   warp 9     streams the packed blocks with cp.async.bulk (elected lane).
