@@ -134,16 +134,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity, giving up after `limit` cycles.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity, long long limit) {
-  if (mbar_test(mbar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_test(mbar, parity)) {
-    if (clock64() - t0 > limit) return false;
-  }
-  return true;
-}
-
 __device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -158,23 +148,5 @@ __device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
 }
-// Arrive once every cp.async this thread issued so far has landed; the
-// barrier's expected count already includes this arrival.
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t mbar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
-}
-
-// Arrive once and add `bytes` to the barrier's expected transaction count.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(v));
-  return r;
-}
-
 }  // namespace tc
 }  // namespace mlav
