@@ -170,6 +170,19 @@ int mla_verify_plan_get_kernel(const mla_verify_plan* plan);
 int mla_verify_plan_set_profile_events(mla_verify_plan* plan, void* after_pack,
                                        void* after_partial);
 
+/*
+ * Testing hook: a fault injected on the host into the plan's next call (then
+ * cleared).  MLA_VERIFY_FAULT_SKIP_PACK (TC family): the call launches the
+ * attention kernel waiting for per-block ready flags but not the pack kernel
+ * that sets them, so every block wait runs out after its cycle limit (about
+ * a second): the rows come out NaN, the device status word gets
+ * MLA_VERIFY_DEV_TIMEOUT and the context stays usable.  MLA_VERIFY_OK, or
+ * MLA_VERIFY_ERR_ARG for an unknown fault.
+ */
+#define MLA_VERIFY_FAULT_NONE         0
+#define MLA_VERIFY_FAULT_SKIP_PACK    1
+int mla_verify_plan_inject_fault(mla_verify_plan* plan, int fault);
+
 /* Bytes of device workspace the plan holds (partials, packed key blocks,
  * pack hand-off flags, error word). */
 size_t mla_verify_plan_workspace_bytes(const mla_verify_plan* plan);

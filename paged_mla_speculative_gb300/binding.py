@@ -22,6 +22,8 @@ OUT_BF16 = 1
 KERNEL_AUTO = 0
 KERNEL_MMA = 1
 KERNEL_TC = 2
+FAULT_NONE = 0
+FAULT_SKIP_PACK = 1
 MAX_NSPLIT = 32
 
 DEV_BAD_SLOT = 1
@@ -46,6 +48,7 @@ SIGNATURES = {
     "mla_verify_plan_destroy": (None, [_P]),
     "mla_verify_plan_set_nsplit": (_I, [_P, _I]),
     "mla_verify_plan_get_nsplit": (_I, [_P, _I]),
+    "mla_verify_plan_inject_fault": (_I, [_P, _I]),
     "mla_verify_plan_get_pack_schedule": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(ctypes.c_int)]),
     "mla_verify_plan_set_kernel": (_I, [_P, _I]),
@@ -169,6 +172,11 @@ class Plan:
         if rc != 0:
             raise MlaVerifyError(rc, "get_pack_schedule")
         return wide.value, stay.value
+
+    def inject_fault(self, fault: int):
+        """Testing hook: inject a host-side fault into the next call (see the
+        C header, FAULT_SKIP_PACK)."""
+        _check(load_library().mla_verify_plan_inject_fault(self.handle, fault), "inject_fault")
 
     def set_kernel(self, kernel: int):
         _check(load_library().mla_verify_plan_set_kernel(self.handle, kernel), "set_kernel")

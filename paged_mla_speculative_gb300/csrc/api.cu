@@ -52,6 +52,7 @@ struct mla_verify_plan {
   // A call failed after its pack kernel was launched: its flags may carry
   // the tag the next call will use, so the next call clears them first.
   bool pack_flags_dirty;
+  int fault;              // MLA_VERIFY_FAULT_* injected into the next call
 };
 
 namespace {
@@ -290,6 +291,13 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int*
   return MLA_VERIFY_OK;
 }
 
+int mla_verify_plan_inject_fault(mla_verify_plan* pl, int fault) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  if (fault != MLA_VERIFY_FAULT_NONE && fault != MLA_VERIFY_FAULT_SKIP_PACK) return MLA_VERIFY_ERR_ARG;
+  pl->fault = fault;
+  return MLA_VERIFY_OK;
+}
+
 int mla_verify_plan_set_kernel(mla_verify_plan* pl, int kernel) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (kernel != MLA_VERIFY_KERNEL_AUTO && kernel != MLA_VERIFY_KERNEL_MMA &&
@@ -369,14 +377,18 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
     if (le == cudaSuccess) le = cudaMemsetAsync(pl->pack_sync + 1, 0, sizeof(unsigned), s);
     if (le == cudaSuccess) pl->pack_flags_dirty = false;
   }
-  if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC) {
+  const bool skip_pack = pl->fault == MLA_VERIFY_FAULT_SKIP_PACK;
+  pl->fault = MLA_VERIFY_FAULT_NONE;
+  if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && skip_pack) {
+    p.pack_flags = 1;   // injected: nothing sets the flags the attention kernel waits for
+  } else if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC) {
     const PackSchedule ps = pack_schedule(pl, p, overlap);
     p.pack_flags = ps.stay > 0;
     le = ps.stay > 0 ? mlav::launch_pack_kv_overlap(p, pl->packed, pl->pack_blocks, pl->num_sms, ps.wide,
                                                     ps.stay, s)
                      : mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
   }
-  const bool packed = le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC;
+  const bool packed = le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack;
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)
     le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)

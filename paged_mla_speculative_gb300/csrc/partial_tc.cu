@@ -82,6 +82,7 @@ constexpr int MB_S = 5;       // S^T done (tcgen05.commit)
 constexpr int MB_P = 6;       // P^T written, O^T rescaled (one arrival per softmax warp)
 constexpr int MB_Q = 7;       // Q tile in fp16 (one arrival per softmax warp)
 constexpr int MB_OT = 8;      // [4] O^T tile d done (tcgen05.commit)
+constexpr int MB_DONE = 12;   // after an abort: every MMA the CTA issued is done
 
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t TM_S = 256;                  // S^T columns; O^T tile d at d * 64
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     tc::mbar_init(mbar(MB_S), 1);
     tc::mbar_init(mbar(MB_P), SOFTMAX_WARPS);
     tc::mbar_init(mbar(MB_Q), SOFTMAX_WARPS);
+    tc::mbar_init(mbar(MB_DONE), 1);
     for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_OT + i), 1);
     tc::mbar_fence_init();
     *s_abort = 0;
@@ -377,6 +379,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
           }
           tc::commit(mbar(MB_OT + d));
         }
+      }
+      // After an abort the waits above returned early and the softmax warps'
+      // wait for the last O^T tile may not have covered every MMA: let them
+      // all finish before TMEM is freed.
+      if (__any_sync(0xffffffffu, *s_abort != 0)) {
+        tc::commit(mbar(MB_DONE));
+        wait_drain(mbar(MB_DONE), 0, p.err);
       }
     }
   } else {

@@ -141,3 +141,28 @@ def test_host_entry_point_matches_device_entry_point():
                                 inp.kv_indices.cpu().pin_memory(), inp.kv_indptr.cpu(),
                                 inp.kv_lens.cpu(), inp.draft_parent.cpu(), inp.scale, out, lse)
     assert torch.equal(out, o_dev.cpu()) and torch.equal(lse, l_dev.cpu())
+
+
+@pytest.mark.parametrize("nsplit", [1, 2])
+def test_bounded_wait_runs_out_and_reports_timeout(nsplit):
+    """Fault injected on the host: the attention kernel waits for ready flags
+    that nothing sets.  Every wait gives up after its cycle limit (about a
+    second): the rows are NaN, the status word reports the timeout, and the
+    context stays usable -- the next call is correct."""
+    inp = _case(seed=7, prefix=(300, 77))
+    with G.make_plan(inp, nsplit=nsplit) as plan:
+        plan.inject_fault(mb.FAULT_SKIP_PACK)
+        out, lse = G.run(plan, inp)
+        assert plan.get_error() & mb.DEV_TIMEOUT
+        assert torch.isnan(out).all() and torch.isnan(lse).all()
+        o2, l2 = G.run(plan, inp)
+        assert plan.get_error() == 0
+    ref_o, ref_l = G.oracle_full(W.make_inputs(inp.workload))
+    G.assert_parity(o2.cpu().numpy(), l2.cpu().numpy(), ref_o, ref_l)
+
+
+def test_unknown_fault_is_rejected():
+    inp = _case(seed=8)
+    with G.make_plan(inp) as plan:
+        with pytest.raises(mb.MlaVerifyError):
+            plan.inject_fault(99)
