@@ -15,9 +15,10 @@ cudaError_t launch_partial_mma(const Params& p, cudaStream_t stream);
 // Split-KV partial kernel on tcgen05 tensor cores with TMEM accumulators.
 cudaError_t partial_tc_prepare();
 // `overlap`: launch with programmatic stream serialisation, so the kernel's
-// CTAs may start while the previous kernel on the stream (the pack, the
-// partial kernel) finishes; the kernel waits for that kernel's results with
-// griddepcontrol.wait before reading them.
+// CTAs may start while the previous kernel on the stream (the pack) runs;
+// the kernel then reads each packed block after its ready flags carry the
+// call's tag (Params::pack_flags = 1), or after griddepcontrol.wait, which
+// waits for the whole pack grid (pack_flags = 0).
 cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap);
 
 // Per-call gather of the key rows into packed fp16 operand tiles.
@@ -32,7 +33,8 @@ cudaError_t pack_kv_prepare();
 cudaError_t launch_pack_kv_overlap(const Params& p, void* packed, int max_blocks, int num_ctas,
                                    int wide_positions, int stay, cudaStream_t stream);
 
-// LSE combine of the split partials into out/lse.
+// LSE combine of the split partials into out/lse (`overlap`: may be
+// scheduled early; it waits for the partial kernel with griddepcontrol.wait).
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool overlap);
 
 // Per-step index builder (index_builder.cu).
