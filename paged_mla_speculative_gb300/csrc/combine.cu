@@ -17,7 +17,7 @@ namespace mlav {
 namespace {
 
 constexpr int WARPS = 8;
-constexpr int EARLY = 4;   // splits whose rows are loaded before the weights are known
+constexpr int EARLY = 2;   // splits whose rows are loaded before the weights are known
 
 __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
   // The split partials come from the kernel just before this one on the
