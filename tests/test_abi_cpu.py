@@ -68,6 +68,9 @@ def test_null_plan_is_rejected():
     assert lib.mla_verify_attn(None, 1, None, None, None, None, None, None,
                                ctypes.c_float(0.1), None, None, None) == -1
     assert lib.mla_verify_plan_get_nsplit(None, 1) == -1
+    w, st = ctypes.c_int(), ctypes.c_int()
+    assert lib.mla_verify_plan_get_pack_schedule(None, 1, ctypes.byref(w), ctypes.byref(st)) == -1
+    assert lib.mla_verify_plan_inject_fault(None, 1) == -1
     lib.mla_verify_plan_destroy(None)
 
 
