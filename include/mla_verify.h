@@ -141,8 +141,10 @@ int mla_verify_plan_get_nsplit(const mla_verify_plan* plan, int batch);
  * kernel -- every SM but *stay packs the first *wide 128-key blocks of every
  * split, then *stay pack CTAs keep packing the rest on the SMs the attention
  * grid leaves idle while it runs.  *stay = 0: the whole pack runs before the
- * attention kernel starts (*wide = all positions).  The MMA family packs
- * nothing (both 0).  MLA_VERIFY_OK, or < 0 (NULL pointer, bad batch).
+ * attention kernel starts (*wide = all positions).  Both 0: no pack -- the
+ * MMA family, or T*H <= 64 (one row tile per request), where each attention
+ * CTA gathers its own key blocks from the cache.  MLA_VERIFY_OK, or < 0
+ * (NULL pointer, bad batch).
  */
 int mla_verify_plan_get_pack_schedule(const mla_verify_plan* plan, int batch, int* wide, int* stay);
 

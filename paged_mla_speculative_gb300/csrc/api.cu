@@ -109,6 +109,7 @@ struct PackSchedule {
   int wide, stay;
 };
 constexpr int kMinPackSms = 16;
+constexpr long long kDirectMaxTiles = 1;   // 2 tiles measured slower (each block gathered twice)
 PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, bool overlap) {
   const int positions = static_cast<int>(ceil_div(pl->pack_blocks, p.nsplit));
   const long long attn = 1LL * p.nsplit * ceil_div(p.R, kRowsPerTile) * p.batch;
@@ -280,7 +281,8 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int*
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
   *wide = 0;
   *stay = 0;
-  if (pl->kernel != MLA_VERIFY_KERNEL_TC) return MLA_VERIFY_OK;
+  if (pl->kernel != MLA_VERIFY_KERNEL_TC || ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles)
+    return MLA_VERIFY_OK;
   mlav::Params p{};
   p.batch = batch;
   p.R = pl->R;
@@ -379,8 +381,17 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   }
   const bool skip_pack = pl->fault == MLA_VERIFY_FAULT_SKIP_PACK;
   pl->fault = MLA_VERIFY_FAULT_NONE;
+  // One row tile per request: each key block is read by one attention CTA,
+  // which gathers it itself instead of going through the pack (which writes
+  // every block and reads it back).
+  const bool direct = pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack &&
+                      ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles;
+  bool attn_overlap = overlap;
   if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && skip_pack) {
     p.pack_flags = 1;   // injected: nothing sets the flags the attention kernel waits for
+  } else if (le == cudaSuccess && direct) {
+    p.direct_all = 1;
+    attn_overlap = false;   // the first kernel of the call: no programmatic overlap with the last call
   } else if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC) {
     const PackSchedule ps = pack_schedule(pl, p, overlap);
     p.pack_flags = ps.stay > 0;
@@ -388,11 +399,11 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
                                                     ps.stay, s)
                      : mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
   }
-  const bool packed = le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack;
+  const bool packed = le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack && !direct;
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)
     le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
-                                             : mlav::launch_partial_tc(p, s, overlap);
+                                             : mlav::launch_partial_tc(p, s, attn_overlap);
   if (packed && le != cudaSuccess) pl->pack_flags_dirty = true;   // the epoch did not advance
   if (le == cudaSuccess && pl->ev_after_partial) le = cudaEventRecord(pl->ev_after_partial, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;

@@ -50,6 +50,8 @@ struct Params {
   int packed_max_blocks;        // 128-key blocks reserved per request in `packed`
   int pack_flags;               // 1: the pack publishes per-unit ready flags
                                 // (overlapping pack); 0: wait for its grid
+  int direct_all;               // 1: no pack; every attention CTA gathers its
+                                // own key blocks from the cache
   // Hand-off between the pack and the attention kernel of one call:
   // [0] epoch (calls completed), [1] ticket (attention CTAs done this call),
   // [4 + 32 * (b * packed_max_blocks + kb) + g] = epoch + 1 once keys

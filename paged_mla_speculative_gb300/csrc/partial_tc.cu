@@ -72,7 +72,8 @@ constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -
 constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [16] mbarriers
 constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, abort flag
 constexpr int OFF_PAR = OFF_MISC + 16;          // int [32] draft parents
-constexpr int SMEM_TOTAL = OFF_PAR + MAX_T * 4;
+constexpr int OFF_SLOTK = OFF_PAR + MAX_T * 4;  // int [128] slots of the block being gathered (direct mode)
+constexpr int SMEM_TOTAL = OFF_SLOTK + BN * 4;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
   int* s_tofr = reinterpret_cast<int*>(smem + OFF_TOFR);
   int* s_par = reinterpret_cast<int*>(smem + OFF_PAR);
+  int* s_slotk = reinterpret_cast<int*>(smem + OFF_SLOTK);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
   const uint32_t sbase = smem_u32(smem);
@@ -312,7 +314,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == COPY_WARP) {
+  if (warp == COPY_WARP && p.direct_all) {
+    // direct mode: the softmax warps gather the key blocks themselves
+  } else if (warp == COPY_WARP) {
     // ======================= packed-block producer ==========================
     // The whole warp runs the loop; one elected lane issues each copy.
     const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PACKED_BLOCK;
@@ -419,13 +423,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     float lpart[HALF];                  // this key's share of its rows' sums
 #pragma unroll
     for (int c = 0; c < HALF; ++c) lpart[c] = 0.f;
-    bool next_ok = nb > 0 && block_slot(p, rq, kb0, j, false) >= 0;
+    // Direct mode: out-of-cache slots are reported here (else by the pack).
+    const bool direct = p.direct_all != 0;
+    int slot_next = nb > 0 ? block_slot(p, rq, kb0, j, direct) : -1;
+    bool next_ok = slot_next >= 0;
 #pragma unroll 1
     for (int it = 0; it < nb; ++it) {
       const int kb = kb0 + it;
       const uint32_t par = static_cast<uint32_t>(it & 1);
       const bool key_ok = next_ok;
-      if (it + 1 < nb) next_ok = block_slot(p, rq, kb + 1, j, false) >= 0;
+      if (direct) {
+        // Gather block kb: 128 scattered rows straight from the cache into
+        // the swizzled chunk tiles (absent or invalid keys zero-filled),
+        // once O^T(kb-1) has read the previous block and its P^T; widen to
+        // fp16 in place; release the chunk barriers to the MMA warp as if
+        // the copies had landed.
+        if (it > 0) {
+          wait_warp(mbar(MB_OT + 3), static_cast<uint32_t>((it - 1) & 1), s_abort, p.err);
+          tc::fence_after_sync();
+        }
+        if (hc == 0) s_slotk[j] = slot_next;
+        named_sync(1, SOFTMAX_WARPS * 32);
+#pragma unroll 1
+        for (int e = tid; e < BN * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
+          const int k = e / ROW_CHUNKS, q = e - k * ROW_CHUNKS;
+          const int sl = s_slotk[k];
+          cp_async16(sbase + OFF_KV + (q >> 3) * KV_CHUNK + k * 128 + (((q & 7) ^ (k & 7)) << 4),
+                     sl >= 0 ? p.kv + static_cast<size_t>(sl) * D_QK + q * 8 : p.kv, sl >= 0 ? 16 : 0);
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        if (it + 1 < nb) {   // the next block's slot, while the rows are in flight
+          slot_next = block_slot(p, rq, kb + 1, j, true);
+          next_ok = slot_next >= 0;
+        }
+        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+        named_sync(1, SOFTMAX_WARPS * 32);
+#pragma unroll 1
+        for (int e = tid; e < BN * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
+          uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_KV + e * 16);
+          uint4 v = *ptr;
+          *ptr = make_uint4(widen_word(v.x), widen_word(v.y), widen_word(v.z), widen_word(v.w));
+        }
+        tc::fence_async_smem();
+        named_sync(1, SOFTMAX_WARPS * 32);
+        if (tid == 0)
+          for (int g = 0; g < 5; ++g) tc::mbar_arrive(mbar(MB_CHUNK + g));
+      } else if (it + 1 < nb) {
+        next_ok = block_slot(p, rq, kb + 1, j, false) >= 0;
+      }
       const int jg = kb * BN + j;
       wait_warp(mbar(MB_S), par, s_abort, p.err);
       tc::fence_after_sync();

@@ -192,3 +192,23 @@ def test_schedules_alternate_on_one_plan():
             assert torch.equal(out, refs[key + "_out"][0]) and torch.equal(lse, refs[key + "_out"][1])
     assert plan.get_error() == 0
     plan.close()
+
+
+@pytest.mark.parametrize("nsplit", [1, 3])
+def test_one_row_tile_gathers_directly(nsplit):
+    """T*H <= 64: no pack; every attention CTA gathers its own key blocks.
+    Ragged lengths (a request shorter than one block, one ending mid-block),
+    repeated calls bit-identical, parity with the oracle."""
+    w = W.Workload(name="direct", batch=3, num_drafts=4, num_heads=16, prefix=(900, 129, 0),
+                   tree="random", num_slots=4096, spike_frac=0.01, seed=700)
+    inp = W.make_inputs(w)
+    g = G.to_cuda(inp)
+    with G.make_plan(g, nsplit=nsplit) as plan:
+        assert plan.pack_schedule(3) == (0, 0)
+        o1, l1 = G.run(plan, g)
+        o1, l1 = o1.clone(), l1.clone()
+        o2, l2 = G.run(plan, g)
+        assert plan.get_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ref_o, ref_l = G.oracle_full(inp)
+    G.assert_parity(o1.cpu().numpy(), l1.cpu().numpy(), ref_o, ref_l)
