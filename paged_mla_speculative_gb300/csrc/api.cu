@@ -64,37 +64,7 @@ int keys_per_block(int kernel) { return kernel == MLA_VERIFY_KERNEL_MMA ? 64 : 1
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-// Split count for `batch` requests: minimise (waves of CTAs) x (key blocks
-// per CTA) plus the cost of moving the split partials through the combine,
-// in units of one CTA key-block step.
-int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel) {
-  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, kRowsPerTile);
-  const long long max_blocks = ceil_div(pl->max_kv_len, keys_per_block(kernel));
-  const int cap = static_cast<int>(std::min<long long>(mlav::MAX_NSPLIT, max_blocks));
-  // Bytes one CTA block-step is worth (about 2 us of HBM time at 6 TB/s).
-  const double bytes_per_step = 12e6;
-  int best = 1;
-  double best_cost = 1e300;
-  for (int ns = 1; ns <= cap; ++ns) {
-    const long long ctas = units * ns;
-    const double waves = static_cast<double>(ceil_div(ctas, pl->num_sms));
-    const double steps = static_cast<double>(ceil_div(max_blocks, ns));
-    double cost = waves * steps;
-    if (ns > 1) cost += 1.0 + static_cast<double>(units) * kRowsPerTile * ns * 4096.0 / bytes_per_step;
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = ns;
-    }
-  }
-  return best;
-}
-
-// Forced counts are clamped to the number of key blocks of max_kv_len.
-int effective_nsplit(const mla_verify_plan* pl, int batch) {
-  if (!pl->forced_nsplit) return auto_nsplit(pl, batch, pl->kernel);
-  return static_cast<int>(std::min<long long>(
-      pl->forced_nsplit, ceil_div(pl->max_kv_len, keys_per_block(pl->kernel))));
-}
+constexpr long long kDirectMaxTiles = 1;   // 2 tiles measured slower (each block gathered twice)
 
 // Pack schedule (see pack_kv.cu).  When the kernels may overlap and the
 // attention grid leaves at least kMinPackSms SMs idle, the two-phase pack:
@@ -109,15 +79,14 @@ struct PackSchedule {
   int wide, stay;
 };
 constexpr int kMinPackSms = 16;
-constexpr long long kDirectMaxTiles = 1;   // 2 tiles measured slower (each block gathered twice)
-PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, bool overlap) {
-  const int positions = static_cast<int>(ceil_div(pl->pack_blocks, p.nsplit));
-  const long long attn = 1LL * p.nsplit * ceil_div(p.R, kRowsPerTile) * p.batch;
+PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool overlap) {
+  const int positions = static_cast<int>(ceil_div(pl->pack_blocks, nsplit));
+  const long long attn = 1LL * nsplit * ceil_div(pl->R, kRowsPerTile) * batch;
   const long long idle = pl->num_sms - attn;
   const PackSchedule whole{positions, 0};
   if (!overlap || idle < kMinPackSms) return whole;
   const double per_block_us = 3.4, lead_us = 5.0, blocks_per_us_per_sm = 0.15;
-  const double narrow_us = static_cast<double>(p.nsplit) * p.batch / (idle * blocks_per_us_per_sm);
+  const double narrow_us = static_cast<double>(nsplit) * batch / (idle * blocks_per_us_per_sm);
   // Position q >= wide is ready after (q - wide + 1) narrow steps and needed
   // after lead + q attention steps; with narrow steps the slower, the last
   // position binds.
@@ -127,6 +96,64 @@ PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, boo
   wide = std::max(1, wide);
   if (2 * wide > positions) return whole;
   return PackSchedule{wide, static_cast<int>(idle)};
+}
+
+PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, bool overlap) {
+  return pack_plan(pl, p.batch, p.nsplit, overlap);
+}
+
+// What the pack leaves on a call's critical path, in attention block steps
+// (~3.4 us): the wide phase (~9 us) when it overlaps, else the whole gather
+// of up to batch x max_kv_len rows (1152 B read + 1152 B written each at
+// ~4.5 TB/s, plus ~3 us); nothing when the attention CTAs gather directly.
+double pack_steps(const mla_verify_plan* pl, int batch, int nsplit) {
+  if (ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles) return 0.0;
+  const PackSchedule ps = pack_plan(pl, batch, nsplit, true);
+  if (ps.stay > 0) return 9.0 / 3.4;
+  return (2304.0 * batch * pl->max_kv_len / 4.5e12 * 1e6 + 3.0) / 3.4;
+}
+
+// Split count for `batch` requests: minimise (waves of CTAs) x (key blocks
+// per CTA) plus the cost of moving the split partials through the combine,
+// in units of one CTA key-block step.
+int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel) {
+  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, kRowsPerTile);
+  const long long max_blocks = ceil_div(pl->max_kv_len, keys_per_block(kernel));
+  const int cap = static_cast<int>(std::min<long long>(mlav::MAX_NSPLIT, max_blocks));
+  // Bytes one CTA block-step is worth (about 2 us of HBM time at 6 TB/s).
+  const double bytes_per_step = 12e6;
+  auto best_split = [&](bool with_pack) {
+    int best = 1;
+    double best_cost = 1e300;
+    for (int ns = 1; ns <= cap; ++ns) {
+      const long long ctas = units * ns;
+      const double waves = static_cast<double>(ceil_div(ctas, pl->num_sms));
+      const double steps = static_cast<double>(ceil_div(max_blocks, ns));
+      double cost = waves * steps;
+      if (ns > 1) cost += 1.0 + static_cast<double>(units) * kRowsPerTile * ns * 4096.0 / bytes_per_step;
+      if (with_pack) cost += pack_steps(pl, batch, ns);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = ns;
+      }
+    }
+    return best;
+  };
+  const int best = best_split(false);
+  // A choice that needs several waves of attention CTAs also runs the whole
+  // pack first; weigh the pack in then (one wave with the pack overlapping
+  // can win: tree, 4 x 16 row tiles x 16k keys, 278 -> 256 us).  Single-wave
+  // choices are kept: beside a running pack the attention blocks take longer
+  // than the planner's step, and weighing the pack picked worse splits there.
+  if (kernel == MLA_VERIFY_KERNEL_TC && units * best > pl->num_sms) return best_split(true);
+  return best;
+}
+
+// Forced counts are clamped to the number of key blocks of max_kv_len.
+int effective_nsplit(const mla_verify_plan* pl, int batch) {
+  if (!pl->forced_nsplit) return auto_nsplit(pl, batch, pl->kernel);
+  return static_cast<int>(std::min<long long>(
+      pl->forced_nsplit, ceil_div(pl->max_kv_len, keys_per_block(pl->kernel))));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
