@@ -1,19 +1,25 @@
 #!/usr/bin/env python
 """Benchmark of the GB300 verify attention (MLA, paged KV cache, draft tree).
 
-One step = one verify call (split-KV partial kernel + LSE combine) over the
-decode-batch workload (B=8 requests, 4096-token prefix each, T=8 chain
-drafts, H=64 heads, page_size=1 scattered slots in a 65536-slot cache, 1% of
-keys x8), inputs resident in HBM.  Prints one JSON line.
+The metric is µs per call and KV-read GB/s against context.  One step is one
+verify call (key pack + split-KV partial kernel + LSE combine), replayed from
+a CUDA graph, over one point of the context sweep: B=1 request, T=8 chain
+drafts, H=64 heads, page_size=1 slots scattered in a 131072-slot cache, 1% of
+the keys x8, prefix P in {1024, 4096, 16384, 65536, 93184}.  The K timed
+steps run at the largest point (P=93184), which is the line's `value`; every
+sweep point and every other workload (decode batch, tree, the two ragged
+batches, tiny, the small-R shapes) is timed the same way, with fewer calls,
+and reported under `workloads`.  Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle as reference arm
 
 Timing: every step writes a 512 MB buffer (larger than the 126 MB L2) before
-the call, then CUDA events on the call's stream bracket the call; an event
-the library records between its two kernels splits partial and combine.
-Under torchrun every rank runs an independent replica (the operation has no
-cross-request exchange), and the slowest rank's time is reported.
+the replay, then CUDA events on the replay stream bracket it.  A second pass
+of eager calls with events the library records between its kernels splits
+pack, partial and combine.  Under torchrun every rank runs an independent
+replica (requests have no cross-request exchange) and the slowest rank's
+time is reported.
 """
 from __future__ import annotations
 
@@ -32,6 +38,11 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
+METRIC = "MLA verify attn \u00b5s/call and KV-read GB/s (% of GB300 HBM roofline) vs context"
+CURVE_NAME = "context_sweep"
+SWEEP = ["sweep_p1024", "sweep_p4096", "sweep_p16384", "sweep_p65536", "sweep_p93184"]
+HEADLINE = "sweep_p93184"      # the largest sweep point: the line's value
+OTHERS = ["tiny", "decode_batch", "tree", "ragged_ps1", "ragged_ps64", "decode_tp8", "decode_t1"]
 
 
 def parse_args(argv=None):
@@ -40,7 +51,10 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", default="decode_batch")
+    ap.add_argument("--workload", default=CURVE_NAME,
+                    help=f"{CURVE_NAME} (default: the sweep plus every other workload) or one workload")
+    ap.add_argument("--other-steps", type=int, default=200,
+                    help="timed calls per workload besides the headline point")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -123,55 +137,15 @@ def compaction_timing(mb, plan, inp, w, flush, stream, steps):
             "frac_of_hbm": gbs / hbm, "bound": "hbm", "launches": 2}
 
 
-def small_r_timing(mb, W, name, flush, stream, steps):
-    """µs per call, KV GB/s and the fraction of the HBM roof for one of the
-    small-R workloads (L2 flushed before every call, events on the stream)."""
-    import torch
-    w = W.WORKLOADS[name]
-    inp = W.make_inputs(w, device="cuda")
-    work = W.algorithmic_work(inp.prefix, w.num_drafts, w.num_heads)
-    plan = mb.Plan(w.batch, w.num_drafts, w.num_heads, w.page_size, w.num_slots,
-                   max(inp.kv_lens.tolist()))
-    out, lse = plan.new_outputs(w.batch)
-
-    def call():
-        mb.mla_verify_attn(plan, inp.q, inp.kv_cache, inp.kv_indices, inp.kv_indptr,
-                           inp.kv_lens, inp.draft_parent, inp.scale, out, lse, stream=stream)
-
-    for _ in range(3):
-        flush.zero_()
-        call()
-    torch.cuda.synchronize()
-    ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for i in range(steps):
-        flush.zero_()
-        ea[i].record(stream)
-        call()
-        eb[i].record(stream)
-    torch.cuda.synchronize()
-    assert plan.get_error() == 0
-    us = statistics.fmean(a.elapsed_time(b) for a, b in zip(ea, eb)) * 1e3
-    peaks, _ = load_peaks()
-    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    kv_gbs = work["kv_bytes"] / (us * 1e-6) / 1e9
-    tc = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    t_hbm, t_tc = work["bytes"] / (hbm * 1e9), work["flops"] / (tc * 1e12)
-    t_roof = max(t_hbm, t_tc) * 1e6
-    res = {"us_per_call": us, "kv_gbs": kv_gbs, "kv_frac_of_hbm": kv_gbs / hbm,
-           "roofline_time_us": t_roof, "frac_of_roofline": t_roof / us,
-           "bound": "hbm" if t_hbm > t_tc else "tensor",
-           "nsplit": plan.nsplit(w.batch), "rows_per_request": w.num_drafts * w.num_heads}
-    plan.close()
-    return res
-
-
-def kernels_of(kernel, ns, pack_stay=0):
+def kernels_of(kernel, ns, pack_stay=0, schedule=None):
     """The library kernels one call launches, for the JSON line (pack_stay >
-    0: the pack that overlaps the attention kernel)."""
+    0: the pack that overlaps the attention kernel; schedule "none": the
+    attention CTAs gather their own keys, no pack)."""
     from paged_mla_speculative_gb300 import binding as mb
-    pack = "pack_kv_overlap_kernel" if pack_stay > 0 else "pack_kv_kernel"
-    names = {mb.KERNEL_TC: [pack, "partial_tc_kernel"],
+    pack = ["pack_kv_overlap_kernel" if pack_stay > 0 else "pack_kv_kernel"]
+    if schedule == "none":
+        pack = []
+    names = {mb.KERNEL_TC: pack + ["partial_tc_kernel"],
              mb.KERNEL_MMA: ["partial_mma_kernel"]}[kernel]
     return " + ".join(names + (["combine_kernel"] if ns > 1 else []))
 
@@ -329,16 +303,27 @@ def max_over_ranks(ws, value):
     return float(t.item())
 
 
-def config_of(w, extra=None):
+def workload_config(w):
     prefix = w.prefix if w.prefix[0] != "uniform" else f"U[{w.prefix[1]},{w.prefix[2]}]"
-    c = {"workload": w.name, "batch": w.batch,
-         "context": prefix[0] if isinstance(prefix, tuple) and len(set(prefix)) == 1 else prefix,
-         "drafts": w.num_drafts, "tree": w.tree, "heads": w.num_heads, "page_size": w.page_size,
-         "cache_slots": w.num_slots, "spiky_keys": f"{w.spike_frac:.0%} x{w.spike_mult:g}",
-         "input_dtype": "bf16", "out_dtype": "fp32", "parallelism": "replicas",
-         "l2": "flushed: 512 MB write before every call"}
-    if extra:
-        c.update(extra)
+    return {"workload": w.name, "batch": w.batch,
+            "context": prefix[0] if isinstance(prefix, tuple) and len(set(prefix)) == 1 else prefix,
+            "drafts": w.num_drafts, "tree": w.tree, "heads": w.num_heads, "page_size": w.page_size,
+            "cache_slots": w.num_slots, "spiky_keys": f"{w.spike_frac:.0%} x{w.spike_mult:g}"}
+
+
+def config_of(name):
+    """The line's `config`: identical in both arms for the same workload."""
+    from paged_mla_speculative_gb300 import workloads as W
+    common = {"input_dtype": "bf16", "out_dtype": "fp32", "parallelism": "replicas",
+              "l2": "flushed: 512 MB write before every call"}
+    if name == CURVE_NAME:
+        w = W.WORKLOADS[HEADLINE]
+        c = workload_config(w)
+        c.update({"workload": CURVE_NAME, "headline_point": HEADLINE,
+                  "context": [W.WORKLOADS[n].prefix[0] for n in SWEEP]})
+    else:
+        c = workload_config(W.WORKLOADS[name])
+    c.update(common)
     return c
 
 
@@ -348,85 +333,173 @@ def _bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
 
 
-def oracle_seconds_per_call(inp, budget_s):
-    """CPU oracle on whole requests, round robin, until the budget is spent."""
-    import numpy as np
+def oracle_call(inp):
+    """The fp64 oracle over one whole call's inputs (all requests)."""
     import oracle
-    qb, cb = _bits(inp.q), _bits(inp.kv_cache)
-    idx = inp.kv_indices.cpu().numpy()
-    ptr = inp.kv_indptr.cpu().numpy()
-    lens = inp.kv_lens.cpu().numpy()
-    par = inp.draft_parent.cpu().numpy()
-    B = len(lens)
+    idx, ptr = inp["idx"], inp["ptr"]
+    return oracle.mla_verify(inp["q"], inp["cache"], idx, ptr, inp["lens"], inp["par"], inp["scale"],
+                             inp["ps"])
+
+
+def oracle_inputs(inp):
+    return {"q": _bits(inp.q), "cache": _bits(inp.kv_cache), "idx": inp.kv_indices.cpu().numpy(),
+            "ptr": inp.kv_indptr.cpu().numpy(), "lens": inp.kv_lens.cpu().numpy(),
+            "par": inp.draft_parent.cpu().numpy(), "scale": inp.scale, "ps": inp.page_size}
+
+
+def oracle_seconds_per_call(inp, budget_s):
+    """CPU oracle on whole calls of the same inputs until the budget is spent
+    (at least one call).  Returns (seconds per call, calls run)."""
+    oi = oracle_inputs(inp)
     done, t0 = 0, time.perf_counter()
     while True:
-        b = done % B
-        sub_ptr = np.array([0, ptr[b + 1] - ptr[b]], dtype=np.int64)
-        oracle.mla_verify(qb[b:b + 1], cb, idx[ptr[b]:ptr[b + 1]], sub_ptr, lens[b:b + 1],
-                          par[b:b + 1], inp.scale, inp.page_size)
+        oracle_call(oi)
         done += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return el / done * B, done
+    return el / done, done
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle on this machine's host cores, timed
+    per whole call on the workload the GPU arm's `value` is quoted on."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    import numpy as np
-    import oracle
     from paged_mla_speculative_gb300 import workloads as W
-    w = W.WORKLOADS[args.workload]
-    inp = W.make_inputs(w, device="cpu")
-    qb, cb = _bits(inp.q), _bits(inp.kv_cache)
-    idx, ptr = inp.kv_indices.numpy(), inp.kv_indptr.numpy()
-    lens, par = inp.kv_lens.numpy(), inp.draft_parent.numpy()
-    B, T, H = w.batch, w.num_drafts, w.num_heads
-    rows_per_call = B * T * H
-
-    def step(i, nrows):
-        b, t = (i // T) % B, i % T
-        rows = [(b, t, h) for h in range(nrows)]
-        oracle.mla_verify_rows(rows, qb, cb, idx, ptr, lens, par, inp.scale, inp.page_size)
-
-    # Size the per-step sample so warm-up + steps end within ~150 s.
-    t0 = time.perf_counter()
-    step(0, 1)
-    t_row = max(time.perf_counter() - t0, 1e-4)
-    budget = 150.0 / max(1, args.steps + args.warmup)
-    nrows = max(1, min(H, int(budget / t_row)))
-    for i in range(args.warmup):
-        step(i, nrows)
-    times, t_start = [], time.perf_counter()
-    steps_run = 0
-    for i in range(args.steps):
-        s0 = time.perf_counter()
-        step(i, nrows)
-        times.append(time.perf_counter() - s0)
-        steps_run += 1
-        if time.perf_counter() - t_start > 180.0:
+    name = HEADLINE if args.workload == CURVE_NAME else args.workload
+    w = W.WORKLOADS[name]
+    oi = oracle_inputs(W.make_inputs(w, device="cpu"))
+    budget = 150.0                       # wall seconds for warm-up + steps
+    t_start = time.perf_counter()
+    for _ in range(args.warmup):
+        oracle_call(oi)
+        if time.perf_counter() - t_start > budget / 3:
             break
-    per_row = sum(times) / (steps_run * nrows)
-    us_per_call = per_row * rows_per_call * 1e6
+    times = []
+    for _ in range(args.steps):
+        s0 = time.perf_counter()
+        oracle_call(oi)
+        times.append(time.perf_counter() - s0)
+        if time.perf_counter() - t_start > budget:
+            break
+    us_per_call = statistics.fmean(times) * 1e6
     cores = len(os.sched_getaffinity(0))
     line = {
-        "impl": "reference", "metric": "verify_attn_us_per_call", "value": us_per_call,
-        "unit": "us/call", "n_gpus": ws, "steps": args.steps, "steps_run": steps_run,
-        "warmup": args.warmup, "ms_per_step": sum(times) / steps_run * 1e3,
+        "impl": "reference", "metric": METRIC, "value": us_per_call,
+        "unit": "us/call", "n_gpus": ws, "steps": args.steps, "steps_run": len(times),
+        "warmup": args.warmup, "ms_per_step": us_per_call / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded), generated on the host",
-        "config": config_of(w),
+        "config": config_of(args.workload),
         "cpu_baseline": {"value": us_per_call, "unit": "us/call", "cores": cores, "kind": "oracle",
-                         "sample": f"{nrows} query rows of one (request, draft) per step, "
-                                   f"gather included, scaled to {rows_per_call} rows per call"},
+                         "sample": f"whole calls of {name} (fp64 NumPy, gather + masked softmax + "
+                                   f"weighted sum), {len(times)} timed"},
         "e2e": {"value": us_per_call, "unit": "us/call", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def measure_workload(mb, W, name, flush, steps, clocks=None):
+    """µs per call of one workload: `steps` CUDA-graph replays (the capture-
+    safe production path), each after an L2 flush, bracketed by events on the
+    replay stream; then eager calls, and eager calls with the library's
+    events between its kernels (pack / partial / combine split)."""
+    import torch
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, device="cuda")
+    work = W.algorithmic_work(inp.prefix, w.num_drafts, w.num_heads)
+    plan = mb.Plan(w.batch, w.num_drafts, w.num_heads, w.page_size, w.num_slots,
+                   max(inp.kv_lens.tolist()))
+    ns = plan.nsplit(w.batch)
+    out, lse = plan.new_outputs(w.batch)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+
+    def call():
+        mb.mla_verify_attn(plan, inp.q, inp.kv_cache, inp.kv_indices, inp.kv_indptr,
+                           inp.kv_lens, inp.draft_parent, inp.scale, out, lse, stream=st)
+
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            flush.zero_()
+            call()
+    st.synchronize()
+    assert plan.get_error() == 0, f"{name}: device error word set during warm-up"
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        call()
+
+    def timed(n, fn, events=False):
+        ea = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        eb = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        pk = [torch.cuda.Event(enable_timing=True) for _ in range(n)] if events else None
+        pm = [torch.cuda.Event(enable_timing=True) for _ in range(n)] if events else None
+        if events:
+            for e in pk + pm:
+                e.record(st)
+            st.synchronize()
+        with torch.cuda.stream(st):
+            for i in range(n):
+                flush.zero_()
+                if events:
+                    plan.set_profile_events(pk[i], pm[i])
+                ea[i].record(st)
+                fn()
+                eb[i].record(st)
+        st.synchronize()
+        if events:
+            plan.set_profile_events(None, None)
+            return ([a.elapsed_time(k) for a, k in zip(ea, pk)],
+                    [k.elapsed_time(m) for k, m in zip(pk, pm)],
+                    [m.elapsed_time(b) for m, b in zip(pm, eb)],
+                    [a.elapsed_time(b) for a, b in zip(ea, eb)])
+        return [a.elapsed_time(b) for a, b in zip(ea, eb)]
+
+    t0 = time.perf_counter()
+    if clocks is not None:
+        with clocks:
+            graph_ms = timed(steps, g.replay)
+    else:
+        graph_ms = timed(steps, g.replay)
+    wall = time.perf_counter() - t0
+    k2 = min(steps, 100)
+    eager_ms = timed(k2, call)
+    pack_ms, part_ms, comb_ms, ser_ms = timed(k2, call, events=True)
+    assert plan.get_error() == 0, f"{name}: device error word set while timing"
+    peaks, peak_src = load_peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tc = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    us = statistics.fmean(graph_ms) * 1e3
+    q = statistics.quantiles(graph_ms, n=10) if len(graph_ms) >= 10 else [min(graph_ms), max(graph_ms)]
+    t_hbm, t_tc = work["bytes"] / (hbm * 1e9), work["flops"] / (tc * 1e12)
+    t_roof = max(t_hbm, t_tc) * 1e6
+    part_us = statistics.fmean(part_ms) * 1e3
+    wide, stay = plan.pack_schedule(w.batch)
+    sched = "none" if (wide, stay) == (0, 0) else ("overlap" if stay > 0 else "whole")
+    kv_gbs = work["kv_bytes"] / (us * 1e-6) / 1e9
+    res = {
+        "us_per_call": us, "us_p10_p50_p90": [q[0] * 1e3, statistics.median(graph_ms) * 1e3, q[-1] * 1e3],
+        "eager_us_per_call": statistics.fmean(eager_ms) * 1e3,
+        "kv_gbs": kv_gbs, "kv_frac_of_hbm": kv_gbs / hbm,
+        "roofline_time_us": t_roof, "frac_of_roofline": t_roof / us,
+        "bound": "hbm" if t_hbm > t_tc else "tensor",
+        "pack_us": statistics.fmean(pack_ms) * 1e3, "partial_us": part_us,
+        "combine_us": statistics.fmean(comb_ms) * 1e3,
+        "serialised_us_per_call": statistics.fmean(ser_ms) * 1e3,
+        "partial_tflops": work["flops"] / (part_us * 1e-6) / 1e12,
+        "partial_frac_of_tensor_peak": work["flops"] / (part_us * 1e-6) / 1e12 / tc,
+        "keys": work["keys"], "kv_bytes": work["kv_bytes"], "flops": work["flops"],
+        "nsplit": ns, "pack_schedule": sched, "kernels": kernels_of(plan.kernel(), ns, stay, sched),
+        "calls_timed": len(graph_ms),
+    }
+    state = {"inp": inp, "plan": plan, "out": out, "lse": lse, "work": work, "wall": wall,
+             "peak_src": peak_src, "tc_peak": tc, "stream": st}
+    return res, state
 
 
 def run_gb300(args):
@@ -442,115 +515,27 @@ def run_gb300(args):
         mbuild.build()
     barrier(ws)
 
-    w = W.WORKLOADS[args.workload]
-    inp = W.make_inputs(w, device="cuda")
-    work = W.algorithmic_work(inp.prefix, w.num_drafts, w.num_heads)
-    max_len = max(inp.kv_lens.tolist())
-    plan = mb.Plan(w.batch, w.num_drafts, w.num_heads, w.page_size, w.num_slots, max_len)
-    ns = plan.nsplit(w.batch)
-    out, lse = plan.new_outputs(w.batch)
-    stream = torch.cuda.current_stream()
+    head = HEADLINE if args.workload == CURVE_NAME else args.workload
+    others = ([n for n in SWEEP + OTHERS if n != head] if args.workload == CURVE_NAME else [])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-
-    def call():
-        mb.mla_verify_attn(plan, inp.q, inp.kv_cache, inp.kv_indices, inp.kv_indptr,
-                           inp.kv_lens, inp.draft_parent, inp.scale, out, lse, stream=stream)
-
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        call()
-    torch.cuda.synchronize()
-    assert plan.get_error() == 0, "device error word set during warm-up"
-
-    K = args.steps
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:
         pass
-
+    K = args.steps
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
     barrier(ws)
     torch.cuda.synchronize()
-    with ClockSampler(uuid) as clk:
-        t0 = time.perf_counter()
-        for i in range(K):
-            flush.zero_()
-            ev_a[i].record(stream)
-            call()
-            ev_b[i].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+    clk = ClockSampler(uuid)
+    res, st = measure_workload(mb, W, head, flush, K, clocks=clk)
     barrier(ws)
-    call_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
-
-    # Per-kernel split: a second, shorter pass with events between the
-    # kernels.  The library then runs the kernels back to back (no launch
-    # overlap), so each difference times one kernel alone; the partial
-    # kernel's time here is the roofline's denominator.
-    kp = min(K, 300)
-    pa = [torch.cuda.Event(enable_timing=True) for _ in range(kp)]
-    pk = [torch.cuda.Event(enable_timing=True) for _ in range(kp)]
-    pm = [torch.cuda.Event(enable_timing=True) for _ in range(kp)]
-    pb = [torch.cuda.Event(enable_timing=True) for _ in range(kp)]
-    for e in pk + pm:
-        e.record(stream)
-    torch.cuda.synchronize()
-    for i in range(kp):
-        flush.zero_()
-        plan.set_profile_events(pk[i], pm[i])
-        pa[i].record(stream)
-        call()
-        pb[i].record(stream)
-    torch.cuda.synchronize()
-    plan.set_profile_events(None, None)
-    pack_ms = [a.elapsed_time(k) for a, k in zip(pa, pk)]
-    part_ms = [k.elapsed_time(m) for k, m in zip(pk, pm)]
-    comb_ms = [m.elapsed_time(b) for m, b in zip(pm, pb)]
-    prof_call_ms = [a.elapsed_time(b) for a, b in zip(pa, pb)]
-
-    mean_call = max_over_ranks(ws, statistics.fmean(call_ms))
-    mean_pack = max_over_ranks(ws, statistics.fmean(pack_ms))
-    mean_part = max_over_ranks(ws, statistics.fmean(part_ms))
-    mean_comb = max_over_ranks(ws, statistics.fmean(comb_ms))
-    us_per_call = mean_call * 1e3 / ws          # whole job: ws replicas in parallel
-    q = statistics.quantiles(call_ms, n=10)
-
-    # Per-step index builder on the same step: the request-to-token table
-    # holds each request's slots (pool rows permuted); time the build alone.
-    ib = index_builder_timing(mb, plan, inp, w, flush, stream, min(K, 300))
-
-    # KV compaction of this step's requests into fresh 64-row pages.
-    compaction = compaction_timing(mb, plan, inp, w, flush, stream, min(K, 200))
-
-    # The small-R regime (a tensor-parallel head slice, one-token decode):
-    # HBM is the roof there; same call protocol, fewer calls.
-    small_r = {name: small_r_timing(mb, W, name, flush, stream, min(K, 200))
-               for name in ("decode_tp8", "decode_t1")}
-
-    # CUDA-graph replay of the same call (capture-safe path), device timed.
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream()
-    s.wait_stream(stream)
-    with torch.cuda.stream(s):
-        call_s = lambda: mb.mla_verify_attn(plan, inp.q, inp.kv_cache, inp.kv_indices,  # noqa: E731
-                                            inp.kv_indptr, inp.kv_lens, inp.draft_parent,
-                                            inp.scale, out, lse, stream=s)
-        call_s()
-    s.synchronize()
-    with torch.cuda.graph(g, stream=s):
-        call_s()
-    gk = min(K, 500)
-    ga = [torch.cuda.Event(enable_timing=True) for _ in range(gk)]
-    gb = [torch.cuda.Event(enable_timing=True) for _ in range(gk)]
-    for i in range(gk):
-        flush.zero_()
-        ga[i].record(stream)
-        g.replay()
-        gb[i].record(stream)
-    torch.cuda.synchronize()
-    graph_us = statistics.fmean(a.elapsed_time(b) for a, b in zip(ga, gb)) * 1e3
+    plan, inp, out, work = st["plan"], st["inp"], st["out"], st["work"]
+    w = W.WORKLOADS[head]
+    mean_call_ms = max_over_ranks(ws, res["us_per_call"] / 1e3)
+    mean_part_ms = max_over_ranks(ws, res["partial_us"] / 1e3)
+    us_per_call = mean_call_ms * 1e3 / ws          # whole job: ws replicas in parallel
 
     # End to end through the host-buffer entry point: H2D of the step's
     # inputs from pinned memory, the call, D2H of out/lse, stream sync.
@@ -560,7 +545,8 @@ def run_gb300(args):
     hlen = inp.kv_lens.cpu().pin_memory()
     hpar = inp.draft_parent.cpu().pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    hlse = torch.empty(st["lse"].shape, dtype=torch.float32).pin_memory()
+    stream = st["stream"]
     for _ in range(3):
         mb.mla_verify_attn_host(plan, hq, inp.kv_cache, hidx, hptr, hlen, hpar, inp.scale,
                                 hout, hlse, stream=stream)
@@ -576,52 +562,71 @@ def run_gb300(args):
     d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
     assert torch.equal(hout, out.cpu()), "host entry point disagrees with device entry point"
     assert plan.get_error() == 0
+    launches = K * len(res["kernels"].split(" + "))
 
-    peaks, peak_src = load_peaks()
-    flops = work["flops"]
-    achieved = flops / (mean_part * 1e-3) / 1e12
-    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    kv_gbs = work["kv_bytes"] / (mean_call * 1e-3) / 1e9
-    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    t_roof_us = max(work["bytes"] / (hbm * 1e9), flops / (peak * 1e12)) * 1e6
-    clocks = clk.summary()
-    pack_wide, pack_stay = plan.pack_schedule(w.batch)
-    launches = K * (len(kernels_of(plan.kernel(), ns, pack_stay).split(" + ")))
+    extra = {}
+    if head == "decode_batch" or args.workload == CURVE_NAME:
+        # NEXT rows measured on the decode-batch step: the per-step index
+        # builder and KV compaction of its requests.
+        db_inp = inp if head == "decode_batch" else W.make_inputs(W.WORKLOADS["decode_batch"], device="cuda")
+        dbw = W.WORKLOADS["decode_batch"]
+        db_plan = plan if head == "decode_batch" else mb.Plan(
+            dbw.batch, dbw.num_drafts, dbw.num_heads, dbw.page_size, dbw.num_slots,
+            max(db_inp.kv_lens.tolist()))
+        extra["index_builder"] = index_builder_timing(mb, db_plan, db_inp, dbw, flush, stream, min(K, 300))
+        extra["compaction"] = compaction_timing(mb, db_plan, db_inp, dbw, flush, stream, min(K, 200))
+        if db_plan is not plan:
+            db_plan.close()
+        del db_inp
 
+    tc_peak = st["tc_peak"]
+    achieved = work["flops"] / (mean_part_ms * 1e-3) / 1e12
     line = {
-        "metric": "verify_attn_us_per_call", "value": us_per_call, "unit": "us/call",
-        "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": mean_call,
+        "metric": METRIC, "value": us_per_call, "unit": "us/call",
+        "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": mean_call_ms,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded), bf16 inputs resident in HBM",
-        "config": config_of(w, {"nsplit": ns, "kernels": kernels_of(plan.kernel(), ns, pack_stay),
-                                "pack_schedule": {"wide_positions": pack_wide, "overlap_ctas": pack_stay}}),
-        "us_per_call_p10_p50_p90": [q[0] * 1e3, statistics.median(call_ms) * 1e3, q[-1] * 1e3],
-        "pack_us": mean_pack * 1e3, "partial_us": mean_part * 1e3, "combine_us": mean_comb * 1e3,
-        "serialised_us_per_call": statistics.fmean(prof_call_ms) * 1e3,
-        "graph_replay_us_per_call": graph_us,
-        "kv_gbs": kv_gbs, "kv_frac_of_hbm": kv_gbs / hbm,
-        "roofline_time_us": t_roof_us, "frac_of_roofline": t_roof_us / (mean_call * 1e3),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
-                     "kernel": "partial_tc_kernel",
-                     "peak_source": f"{peak_src} bf16 burst (fp16 has the same tensor rate)"},
-        "index_builder": ib,
-        "small_r": small_r,
-        "compaction": compaction,
-        "clocks": clocks, "gpu_launches": launches,
+        "config": config_of(args.workload),
+        "headline": {"workload": head, **{k: res[k] for k in (
+            "kv_gbs", "kv_frac_of_hbm", "roofline_time_us", "frac_of_roofline", "bound", "nsplit",
+            "pack_schedule", "kernels", "us_p10_p50_p90", "eager_us_per_call", "pack_us",
+            "partial_us", "combine_us")}},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tc_peak, "traffic": profiled_traffic(head),
+                     "kernel": "partial_tc_kernel", "workload": head,
+                     "peak_source": f"{st['peak_src']} bf16 burst (fp16 has the same tensor rate)"},
+        "clocks": clk.summary(), "gpu_launches": launches,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "timed_wall_s": wall,
+        "timed_wall_s": st["wall"],
     }
-    if ws == 1 and rank == 0 and not args.no_cpu_baseline:
-        sec, nreq = oracle_seconds_per_call(inp, args.cpu_seconds)
+    line.update(extra)
+    cpu_inp = inp if (ws == 1 and rank == 0 and not args.no_cpu_baseline) else None
+    plan.close()
+    del st, out
+    torch.cuda.empty_cache()
+
+    # The rest of the curve and every other workload, same protocol.
+    if others:
+        curve = {head: {**res}}
+        for n in others:
+            r, s2 = measure_workload(mb, W, n, flush, min(args.other_steps, K))
+            s2["plan"].close()
+            del s2
+            torch.cuda.empty_cache()
+            curve[n] = r
+        line["workloads"] = {n: curve[n] for n in SWEEP + OTHERS if n in curve}
+        line["curve"] = [{"context": W.WORKLOADS[n].prefix[0], "us_per_call": curve[n]["us_per_call"],
+                          "kv_gbs": curve[n]["kv_gbs"], "frac_of_roofline": curve[n]["frac_of_roofline"],
+                          "partial_frac_of_tensor_peak": curve[n]["partial_frac_of_tensor_peak"]}
+                         for n in SWEEP]
+    if cpu_inp is not None:
+        sec, ncalls = oracle_seconds_per_call(cpu_inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": sec * 1e6, "unit": "us/call",
                                 "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-                                "sample": f"{nreq} whole requests of the same inputs (fp64 NumPy), "
-                                          f"scaled to {w.batch} requests per call"}
+                                "sample": f"{ncalls} whole calls of {head} (fp64 NumPy, same inputs)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    plan.close()
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

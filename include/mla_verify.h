@@ -38,10 +38,11 @@
  * Every device pointer must be 16-byte aligned.
  *
  * Numerics: both products run on the tensor cores in fp16 with fp32
- * accumulation; the bf16 inputs are widened to fp16 in shared memory, which
- * is exact for |x| in [2^-14, 65504] (smaller magnitudes keep an absolute
- * error below 2^-25; values beyond the fp16 range are not supported).  The
- * softmax runs in fp32.
+ * accumulation; the bf16 inputs are widened to fp16, which is exact for |x|
+ * in [2^-14, 65504] (smaller magnitudes keep an absolute error below 2^-25).
+ * A gathered key or query value of magnitude 65536 or more (or NaN) has no
+ * fp16 counterpart: the kernel that widens it sets MLA_VERIFY_DEV_RANGE and
+ * the rows that read it come out inf or NaN.  The softmax runs in fp32.
  *
  * Ownership: the caller owns every tensor.  The plan owns its workspace
  * (split partials), a device error word and, for mla_verify_attn_host, its
@@ -90,6 +91,9 @@ extern "C" {
 #define MLA_VERIFY_DEV_INTERNAL      32   /* an internal layout invariant failed   */
 #define MLA_VERIFY_DEV_BAD_POOL      64   /* index builder: pool row / prefix / length out of range */
 #define MLA_VERIFY_DEV_CAPACITY     128   /* index builder: kv_indices capacity exceeded */
+#define MLA_VERIFY_DEV_RANGE        256   /* a q or key value is outside the fp16 range
+                                             (|x| >= 65536, or NaN): rows that used it
+                                             are not reliable */
 
 /* Output element type. */
 #define MLA_VERIFY_OUT_F32            0
@@ -220,9 +224,55 @@ int mla_verify_attn_host(mla_verify_plan* plan, int batch, const void* q_host,
                          void* out_host, float* lse_host, void* stream);
 
 /*
+ * Context-parallel split of one call over several GPUs (or several calls):
+ * the KV split with a reduce step of "The Decisive A/B: When Benchmarking
+ * Honesty Reveals the Real Bottleneck" (section "The Context"), taken one
+ * level up -- each rank computes the partial of its shard of every request's
+ * keys, the ranks exchange the partials (an all-gather), and each rank
+ * merges them with mla_verify_combine_parts.
+ *
+ * Shards: request b's ceil(n_b / 128) blocks of 128 consecutive logical keys
+ * are dealt out evenly -- shard s of S takes blocks floor(s * nb / S) ..
+ * floor((s+1) * nb / S) - 1, clipped to n_b -- so the shards are disjoint
+ * and cover every key.  A shard may be empty for short requests.
+ *
+ * mla_verify_attn_partial: the verify attention restricted to shard `shard`
+ * of `num_shards` (0 <= shard < num_shards <= MLA_VERIFY_MAX_NSPLIT), with
+ * the inputs of mla_verify_attn.  A key counts iff it is in the shard and
+ * visible as usual.  Writes part_out fp32 [B, T, H, 512], normalised over the
+ * counted keys, and part_lse fp32 [B, T, H], their log-sum-exp (natural log);
+ * a row with no counted key gets part_lse = -inf and part_out = 0 (weight 0
+ * in the merge).  Same rules as mla_verify_attn otherwise (capturable, no
+ * allocation or synchronisation; device-side errors set the sticky bits).
+ * MLA_VERIFY_ERR_ARG for a bad shard / num_shards.
+ *
+ * mla_verify_combine_parts: merges num_parts (1..MLA_VERIFY_MAX_NSPLIT)
+ * partials of the same batch, laid out shard-major as an all-gather leaves
+ * them: parts_out fp32 [num_parts, B, T, H, 512], parts_lse fp32
+ * [num_parts, B, T, H].  lse = log sum_s exp(lse_s), out = sum_s
+ * exp(lse_s - lse) * out_s, written in the plan's out_dtype; partials with
+ * lse_s = -inf have weight 0, a NaN lse_s makes the row NaN.  With the parts
+ * of shards 0 .. S-1 of one set of inputs this equals mla_verify_attn on
+ * those inputs (up to rounding).  Capturable; allocates nothing.
+ */
+int mla_verify_attn_partial(mla_verify_plan* plan, int batch, const void* q,
+                            const void* kv_cache, const int32_t* kv_indices,
+                            const int32_t* kv_indptr, const int32_t* kv_lens,
+                            const int32_t* draft_parent, float scale, int shard,
+                            int num_shards, float* part_out, float* part_lse, void* stream);
+int mla_verify_combine_parts(mla_verify_plan* plan, int batch, int num_parts,
+                             const float* parts_out, const float* parts_lse, void* out,
+                             float* lse, void* stream);
+
+/*
  * Read the sticky device error word (MLA_VERIFY_DEV_* bits) into
- * *device_status; clear it when `clear` is nonzero.  Synchronises the
- * plan's device: call outside graph capture.
+ * *device_status; clear it when `clear` is nonzero.  Waits for the plan's
+ * last eagerly launched call (an event the plan records at the end of every
+ * mla_verify_attn, mla_verify_build_indices and mla_verify_compact_kv call
+ * made outside stream capture), then reads and clears the word on a private
+ * stream of the plan: other streams and devices are not synchronised.  Work
+ * replayed from a CUDA graph is not tracked: synchronise the replay stream
+ * first.  Call outside graph capture.
  */
 int mla_verify_get_error(mla_verify_plan* plan, int* device_status, int clear);
 
@@ -329,6 +379,10 @@ int mla_verify_compact_kv(mla_verify_plan* plan, int batch, const void* kv_src, 
  *
  * The first call on each device looks up the array's device address and sets
  * a kernel attribute for that device: make it before any stream capture.
+ * When a CUDA call of this entry fails (for example after cudaDeviceReset,
+ * which discards the device context the cached address belongs to), the call
+ * returns MLA_VERIFY_ERR_CUDA and the next call on that device repeats the
+ * set-up.
  * Every call on a device shares the one array, so calls that overlap on the
  * GPU (different streams, or different host threads without ordering) race
  * on it and corrupt each other's results; serialise them.

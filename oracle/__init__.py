@@ -32,7 +32,10 @@ tree mask.
 
 ``index_builder_ref.build_indices`` restates the per-step index builder (the
 request-to-token table turned into the slot or page table the attention
-reads); its pins are in tests/test_index_builder_pins.py.  ``compact_ref.compact_kv``
+reads); its pins are in tests/test_index_builder_pins.py.
+``shard_key_range``, ``mla_verify_key_range`` and ``lse_merge`` restate the
+context-parallel split: one shard's partial over its keys and the reduce of
+the shards' partials (pins: tests/test_context_parallel_pins.py).  ``compact_ref.compact_kv``
 restates KV compaction into 64-row pages (pins: tests/test_compact_pins.py).
 
 Pins (tests/test_oracle_pins.py): pure-Python brute force on tiny inputs, a
@@ -48,4 +51,7 @@ from .mla_verify_ref import (  # noqa: F401
     mla_verify,
     mla_verify_rows,
     mla_verify_split_combine,
+    shard_key_range,
+    mla_verify_key_range,
+    lse_merge,
 )

@@ -29,10 +29,12 @@ def _on_root_path(parent, t: int, i: int) -> bool:
 
 
 def brute_verify(q_bits, cache_bits, kv_indices, kv_indptr, kv_lens, parent,
-                 scale, page_size):
+                 scale, page_size, key_ranges=None):
     """q_bits: nested lists [B][T][H][576] of bf16 bit patterns (ints);
     cache_bits: list of rows of bf16 bit patterns.  Returns nested lists
-    out[B][T][H][512], lse[B][T][H]."""
+    out[B][T][H][512], lse[B][T][H].  key_ranges: optional [(lo, hi)] per
+    request; only keys lo <= j < hi count, and a row with no counted key
+    gets lse -inf and a zero out."""
     B = len(q_bits)
     T = len(q_bits[0])
     H = len(q_bits[0][0])
@@ -54,12 +56,18 @@ def brute_verify(q_bits, cache_bits, kv_indices, kv_indptr, kv_lens, parent,
                 qv = [_bf16(x) for x in q_bits[b][t][h]]
                 weights, vis_rows = [], []
                 for j in range(n):
+                    if key_ranges is not None and not key_ranges[b][0] <= j < key_ranges[b][1]:
+                        continue
                     if j >= P and not _on_root_path(parent[b], t, j - P):
                         continue
                     s = scale * math.fsum(qv[d] * rows[j][d] for d in range(576))
                     weights.append(math.exp(s))
                     vis_rows.append(rows[j])
                 z = math.fsum(weights)
+                if not weights:
+                    ot.append([0.0] * 512)
+                    lt.append(-math.inf)
+                    continue
                 ot.append([math.fsum(w * r[d] for w, r in zip(weights, vis_rows)) / z
                            for d in range(512)])
                 lt.append(math.log(z))

@@ -184,3 +184,66 @@ def mla_verify_split_combine(q, kv_cache, kv_indices, kv_indptr, kv_lens,
             out[b, t] = sum(w[r][:, None] * parts[r][0] for r in range(nsplit))
             lse[b, t] = tot
     return out, lse
+
+
+def shard_key_range(n: int, shard: int, num_shards: int, block: int = 128) -> Tuple[int, int]:
+    """Logical keys [lo, hi) that shard `shard` of `num_shards` covers in a
+    request of n keys (the context-parallel split of the partial + reduce
+    design, "The Decisive A/B ...", section "The Context").
+
+    The request's ceil(n / 128) blocks of 128 consecutive keys are dealt out
+    evenly: shard s takes blocks floor(s * nb / S) .. floor((s+1) * nb / S) - 1,
+    so a shard boundary never cuts a block; the range is clipped to n.
+    """
+    nb = -(-int(n) // block)
+    b0 = (shard * nb) // num_shards
+    b1 = ((shard + 1) * nb) // num_shards
+    return min(int(n), b0 * block), min(int(n), b1 * block)
+
+
+def mla_verify_key_range(q, kv_cache, kv_indices, kv_indptr, kv_lens,
+                         draft_parent, scale: float, page_size: int,
+                         lo: Sequence[int], hi: Sequence[int]):
+    """The definition restricted to the logical keys [lo[b], hi[b]) of each
+    request: a key counts iff it is in range and visible as usual.
+
+    Returns out [B,T,H,512] (normalised over the counted keys) and lse
+    [B,T,H] (their log-sum-exp).  A row with no counted key has lse = -inf
+    and out = 0, the weight-0 partial of the reduce step.
+    """
+    qf = bf16_bits_to_f64(q)
+    B, T, H, _ = qf.shape
+    out = np.zeros((B, T, H, D_V))
+    lse = np.full((B, T, H), -np.inf)
+    for b in range(B):
+        n = int(kv_lens[b])
+        P = n - T
+        keys = gather_request_keys(kv_cache, kv_indices, kv_indptr, b, n, page_size)
+        anc = ancestor_sets(np.asarray(draft_parent)[b])
+        inr = np.zeros(n, dtype=bool)
+        inr[int(lo[b]):int(hi[b])] = True
+        for t in range(T):
+            vis = _visible(P, n, anc[t]) & inr
+            if vis.any():
+                out[b, t], lse[b, t] = _attend(qf[b, t], keys, vis, scale)
+    return out, lse
+
+
+def lse_merge(parts_out, parts_lse):
+    """The reduce step over S partials, in fp64: parts_out [S, ..., 512],
+    parts_lse [S, ...] ->
+        lse = log sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * out_s.
+    Partials with lse_s = -inf have weight 0; when every partial of a row has
+    -inf the row is lse = -inf, out = 0.
+    """
+    po = np.asarray(parts_out, dtype=np.float64)
+    pl = np.asarray(parts_lse, dtype=np.float64)
+    mx = pl.max(axis=0)
+    base = np.where(np.isfinite(mx), mx, 0.0)
+    w = np.exp(pl - base)                            # exp(-inf) = 0
+    tot = w.sum(axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(tot > 0, base + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+        wn = np.where(tot > 0, w / np.where(tot > 0, tot, 1.0), 0.0)
+    out = (wn[..., None] * po).sum(axis=0)
+    return out, lse

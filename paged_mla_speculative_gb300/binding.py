@@ -34,6 +34,7 @@ DEV_TIMEOUT = 16
 DEV_INTERNAL = 32
 DEV_BAD_POOL = 64
 DEV_CAPACITY = 128
+DEV_RANGE = 256
 
 STATUS = {0: "OK", -1: "ERR_NULL", -2: "ERR_ALIGN", -3: "ERR_SHAPE", -4: "ERR_BATCH",
           -5: "ERR_SCALE", -6: "ERR_CUDA", -7: "ERR_DEVICE", -8: "ERR_OOM", -9: "ERR_ARG",
@@ -57,6 +58,9 @@ SIGNATURES = {
     "mla_verify_plan_set_profile_events": (_I, [_P, _P, _P]),
     "mla_verify_attn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
     "mla_verify_attn_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
+    "mla_verify_attn_partial": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _P, _P,
+                                     _P]),
+    "mla_verify_combine_parts": (_I, [_P, _I, _I, _P, _P, _P, _P, _P]),
     "mla_verify_get_error": (_I, [_P, ctypes.POINTER(_I), _I]),
     "mla_verify_attn_static": (_I, [_I, _I, _I, _I, ctypes.c_int64, _I, _I, _P, _P, _P, _P, _P, _P,
                                     ctypes.c_float, _P, _P, _P, _P]),
@@ -262,6 +266,53 @@ def mla_verify_attn(plan: Plan, q, kv_cache, kv_indices, kv_indptr, kv_lens, dra
         _ptr(kv_lens), _ptr(draft_parent), float(scale), _ptr(out), _ptr(lse),
         _stream_ptr(stream))
     _check(st, "mla_verify_attn")
+    return out, lse
+
+
+def mla_verify_attn_partial(plan: Plan, q, kv_cache, kv_indices, kv_indptr, kv_lens,
+                            draft_parent, scale: float, shard: int, num_shards: int,
+                            part_out=None, part_lse=None, stream=None):
+    """One context-parallel shard of the verify attention; returns (part_out
+    fp32 [B,T,H,512], part_lse fp32 [B,T,H]) over the keys of shard `shard`
+    of `num_shards` (see the C header).  Enqueued on ``stream``; no sync."""
+    B = q.shape[0]
+    dev = torch.device("cuda", plan.device)
+    _expect(q, "q", torch.bfloat16, dev, (B, plan.T, plan.H, 576))
+    _expect(kv_cache, "kv_cache", torch.bfloat16, dev)
+    _expect(kv_indices, "kv_indices", torch.int32, dev)
+    _expect(kv_indptr, "kv_indptr", torch.int32, dev, (B + 1,))
+    _expect(kv_lens, "kv_lens", torch.int32, dev, (B,))
+    _expect(draft_parent, "draft_parent", torch.int32, dev, (B, plan.T))
+    if part_out is None:
+        part_out = torch.empty((B, plan.T, plan.H, 512), dtype=torch.float32, device=dev)
+    if part_lse is None:
+        part_lse = torch.empty((B, plan.T, plan.H), dtype=torch.float32, device=dev)
+    _expect(part_out, "part_out", torch.float32, dev, (B, plan.T, plan.H, 512))
+    _expect(part_lse, "part_lse", torch.float32, dev, (B, plan.T, plan.H))
+    st = load_library().mla_verify_attn_partial(
+        plan.handle, B, _ptr(q), _ptr(kv_cache), _ptr(kv_indices), _ptr(kv_indptr),
+        _ptr(kv_lens), _ptr(draft_parent), float(scale), int(shard), int(num_shards),
+        _ptr(part_out), _ptr(part_lse), _stream_ptr(stream))
+    _check(st, "mla_verify_attn_partial")
+    return part_out, part_lse
+
+
+def mla_verify_combine_parts(plan: Plan, parts_out, parts_lse, out=None, lse=None, stream=None):
+    """Merge shard partials laid out shard-major (parts_out fp32 [S,B,T,H,512],
+    parts_lse fp32 [S,B,T,H]) into (out, lse) in the plan's output dtype."""
+    S, B = parts_out.shape[0], parts_out.shape[1]
+    dev = torch.device("cuda", plan.device)
+    _expect(parts_out, "parts_out", torch.float32, dev, (S, B, plan.T, plan.H, 512))
+    _expect(parts_lse, "parts_lse", torch.float32, dev, (S, B, plan.T, plan.H))
+    if out is None or lse is None:
+        o2, l2 = plan.new_outputs(B)
+        out = o2 if out is None else out
+        lse = l2 if lse is None else lse
+    _expect(out, "out", plan.out_dtype, dev, (B, plan.T, plan.H, 512))
+    _expect(lse, "lse", torch.float32, dev, (B, plan.T, plan.H))
+    st = load_library().mla_verify_combine_parts(plan.handle, B, S, _ptr(parts_out), _ptr(parts_lse),
+                                                 _ptr(out), _ptr(lse), _stream_ptr(stream))
+    _check(st, "mla_verify_combine_parts")
     return out, lse
 
 

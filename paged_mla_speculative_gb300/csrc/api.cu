@@ -53,6 +53,11 @@ struct mla_verify_plan {
   // the tag the next call will use, so the next call clears them first.
   bool pack_flags_dirty;
   int fault;              // MLA_VERIFY_FAULT_* injected into the next call
+  // mla_verify_get_error: an event recorded at the end of the last call made
+  // outside capture, and a private stream to read the error word on.
+  cudaEvent_t done_ev;
+  bool done_recorded;
+  cudaStream_t aux;
 };
 
 namespace {
@@ -79,8 +84,8 @@ struct PackSchedule {
   int wide, stay;
 };
 constexpr int kMinPackSms = 16;
-PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool overlap) {
-  const int positions = static_cast<int>(ceil_div(pl->pack_blocks, nsplit));
+PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool overlap, int shards = 1) {
+  const int positions = static_cast<int>(ceil_div(ceil_div(pl->pack_blocks, shards), nsplit));
   const long long attn = 1LL * nsplit * ceil_div(pl->R, kRowsPerTile) * batch;
   const long long idle = pl->num_sms - attn;
   const PackSchedule whole{positions, 0};
@@ -99,26 +104,32 @@ PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool ov
 }
 
 PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, bool overlap) {
-  return pack_plan(pl, p.batch, p.nsplit, overlap);
+  return pack_plan(pl, p.batch, p.nsplit, overlap, p.num_shards);
 }
 
 // What the pack leaves on a call's critical path, in attention block steps
 // (~3.4 us): the wide phase (~9 us) when it overlaps, else the whole gather
 // of up to batch x max_kv_len rows (1152 B read + 1152 B written each at
 // ~4.5 TB/s, plus ~3 us); nothing when the attention CTAs gather directly.
-double pack_steps(const mla_verify_plan* pl, int batch, int nsplit) {
+double pack_steps(const mla_verify_plan* pl, int batch, int nsplit, int shards) {
   if (ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles) return 0.0;
-  const PackSchedule ps = pack_plan(pl, batch, nsplit, true);
+  const PackSchedule ps = pack_plan(pl, batch, nsplit, true, shards);
   if (ps.stay > 0) return 9.0 / 3.4;
-  return (2304.0 * batch * pl->max_kv_len / 4.5e12 * 1e6 + 3.0) / 3.4;
+  return (2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0) / 3.4;
+}
+
+// Keys a request can hold in a call covering one of `shards` shards: a
+// shard takes at most ceil(nb / shards) of the request's nb 128-key blocks.
+long long call_keys(const mla_verify_plan* pl, int shards) {
+  return std::min<long long>(pl->max_kv_len, ceil_div(ceil_div(pl->max_kv_len, 128), shards) * 128);
 }
 
 // Split count for `batch` requests: minimise (waves of CTAs) x (key blocks
 // per CTA) plus the cost of moving the split partials through the combine,
 // in units of one CTA key-block step.
-int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel) {
+int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel, int shards = 1) {
   const long long units = static_cast<long long>(batch) * ceil_div(pl->R, kRowsPerTile);
-  const long long max_blocks = ceil_div(pl->max_kv_len, keys_per_block(kernel));
+  const long long max_blocks = ceil_div(call_keys(pl, shards), keys_per_block(kernel));
   const int cap = static_cast<int>(std::min<long long>(mlav::MAX_NSPLIT, max_blocks));
   // Bytes one CTA block-step is worth (about 2 us of HBM time at 6 TB/s).
   const double bytes_per_step = 12e6;
@@ -131,7 +142,7 @@ int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel) {
       const double steps = static_cast<double>(ceil_div(max_blocks, ns));
       double cost = waves * steps;
       if (ns > 1) cost += 1.0 + static_cast<double>(units) * kRowsPerTile * ns * 4096.0 / bytes_per_step;
-      if (with_pack) cost += pack_steps(pl, batch, ns);
+      if (with_pack) cost += pack_steps(pl, batch, ns, shards);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best = ns;
@@ -149,11 +160,11 @@ int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel) {
   return best;
 }
 
-// Forced counts are clamped to the number of key blocks of max_kv_len.
-int effective_nsplit(const mla_verify_plan* pl, int batch) {
-  if (!pl->forced_nsplit) return auto_nsplit(pl, batch, pl->kernel);
+// Forced counts are clamped to the number of key blocks a request can have.
+int effective_nsplit(const mla_verify_plan* pl, int batch, int shards = 1) {
+  if (!pl->forced_nsplit) return auto_nsplit(pl, batch, pl->kernel, shards);
   return static_cast<int>(std::min<long long>(
-      pl->forced_nsplit, ceil_div(pl->max_kv_len, keys_per_block(pl->kernel))));
+      pl->forced_nsplit, ceil_div(call_keys(pl, shards), keys_per_block(pl->kernel))));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -163,6 +174,18 @@ void free_all(mla_verify_plan* p) {
                   p->st_lens, p->st_parent, p->st_out, p->st_lse, p->packed, p->pack_sync};
   for (void* b : bufs)
     if (b) cudaFree(b);
+}
+
+// Mark the end of an eagerly launched call for mla_verify_get_error.  A call
+// recorded into a graph is not tracked (the event would not fire on replay).
+cudaError_t note_done(mla_verify_plan* pl, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs != cudaStreamCaptureStatusNone) return cudaSuccess;
+  e = cudaEventRecord(pl->done_ev, s);
+  if (e == cudaSuccess) pl->done_recorded = true;
+  return e;
 }
 
 int check_device(const mla_verify_plan* pl) {
@@ -270,7 +293,11 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   }
   pl->ws_bytes = rows * (mlav::D_V + 1) * sizeof(float) + 256 + packed_bytes + sync_bytes;
   if (cudaMemset(pl->err, 0, 256) != cudaSuccess || cudaMemset(pl->pack_sync, 0, sync_bytes) != cudaSuccess ||
+      cudaEventCreateWithFlags(&pl->done_ev, cudaEventDisableTiming) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&pl->aux, cudaStreamNonBlocking) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
+    if (pl->done_ev) cudaEventDestroy(pl->done_ev);
+    if (pl->aux) cudaStreamDestroy(pl->aux);
     free_all(pl);
     delete pl;
     return MLA_VERIFY_ERR_CUDA;
@@ -285,6 +312,8 @@ void mla_verify_plan_destroy(mla_verify_plan* pl) {
   cudaGetDevice(&prev);
   cudaSetDevice(pl->device);
   cudaDeviceSynchronize();
+  if (pl->done_ev) cudaEventDestroy(pl->done_ev);
+  if (pl->aux) cudaStreamDestroy(pl->aux);
   free_all(pl);
   if (prev >= 0) cudaSetDevice(prev);
   delete pl;
@@ -314,6 +343,7 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int*
   p.batch = batch;
   p.R = pl->R;
   p.nsplit = effective_nsplit(pl, batch);
+  p.num_shards = 1;
   const PackSchedule ps = pack_schedule(pl, p, true);
   *wide = ps.wide;
   *stay = ps.stay;
@@ -350,10 +380,16 @@ int mla_verify_plan_set_profile_events(mla_verify_plan* pl, void* after_pack, vo
 
 size_t mla_verify_plan_workspace_bytes(const mla_verify_plan* pl) { return pl ? pl->ws_bytes : 0; }
 
-int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* kv_cache,
-                    const int32_t* kv_indices, const int32_t* kv_indptr, const int32_t* kv_lens,
-                    const int32_t* draft_parent, float scale, void* out, float* lse,
-                    void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One verify call (or one shard of it) on `s`: argument checks, the split
+// count, then pack / partial / combine.  `out_bf16` is the output type.
+int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_cache,
+                const int32_t* kv_indices, const int32_t* kv_indptr, const int32_t* kv_lens,
+                const int32_t* draft_parent, float scale, int shard, int num_shards, void* out,
+                float* lse, bool out_bf16, cudaStream_t s) {
   if (!pl || !q || !kv_cache || !kv_indices || !kv_indptr || !kv_lens || !draft_parent || !out ||
       !lse)
     return MLA_VERIFY_ERR_NULL;
@@ -362,9 +398,11 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
     return MLA_VERIFY_ERR_ALIGN;
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
   if (!std::isfinite(scale)) return MLA_VERIFY_ERR_SCALE;
+  if (num_shards < 1 || num_shards > mlav::MAX_NSPLIT || shard < 0 || shard >= num_shards)
+    return MLA_VERIFY_ERR_ARG;
   const int dev_status = check_device(pl);
   if (dev_status != MLA_VERIFY_OK) return dev_status;
-  const int ns = effective_nsplit(pl, batch);
+  const int ns = effective_nsplit(pl, batch, num_shards);
   if (1LL * batch * ns > pl->ws_capacity) return MLA_VERIFY_ERR_SHAPE;
 
   Params p{};
@@ -383,17 +421,19 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   p.num_slots = pl->num_slots;
   p.max_kv_len = pl->max_kv_len;
   p.nsplit = ns;
+  p.shard = shard;
+  p.num_shards = num_shards;
   p.ws_o = pl->ws_o;
   p.ws_lse = pl->ws_lse;
+  p.ws_stride_b = 1LL * ns * pl->R;
+  p.ws_stride_s = pl->R;
   p.out = out;
   p.lse = lse;
-  p.out_bf16 = pl->out_dtype == MLA_VERIFY_OUT_BF16;
+  p.out_bf16 = out_bf16 ? 1 : 0;
   p.err = pl->err;
   p.packed = static_cast<const uint8_t*>(pl->packed);
   p.packed_max_blocks = pl->pack_blocks;
   p.pack_sync = pl->pack_sync;
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Each kernel may start while the one before it finishes (programmatic
   // dependent launch), except when profiling events sit between them: then
   // the kernels run back to back so that each event brackets one kernel.
@@ -435,6 +475,61 @@ int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* k
   if (le == cudaSuccess && pl->ev_after_partial) le = cudaEventRecord(pl->ev_after_partial, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   if (ns > 1 && mlav::launch_combine(p, s, overlap) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (note_done(pl, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  return MLA_VERIFY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_verify_attn(mla_verify_plan* pl, int batch, const void* q, const void* kv_cache,
+                    const int32_t* kv_indices, const int32_t* kv_indptr, const int32_t* kv_lens,
+                    const int32_t* draft_parent, float scale, void* out, float* lse,
+                    void* stream) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  return launch_call(pl, batch, q, kv_cache, kv_indices, kv_indptr, kv_lens, draft_parent, scale, 0, 1,
+                     out, lse, pl->out_dtype == MLA_VERIFY_OUT_BF16, static_cast<cudaStream_t>(stream));
+}
+
+int mla_verify_attn_partial(mla_verify_plan* pl, int batch, const void* q, const void* kv_cache,
+                            const int32_t* kv_indices, const int32_t* kv_indptr,
+                            const int32_t* kv_lens, const int32_t* draft_parent, float scale,
+                            int shard, int num_shards, float* part_out, float* part_lse,
+                            void* stream) {
+  return launch_call(pl, batch, q, kv_cache, kv_indices, kv_indptr, kv_lens, draft_parent, scale, shard,
+                     num_shards, part_out, part_lse, false, static_cast<cudaStream_t>(stream));
+}
+
+int mla_verify_combine_parts(mla_verify_plan* pl, int batch, int num_parts, const float* parts_out,
+                             const float* parts_lse, void* out, float* lse, void* stream) {
+  if (!pl || !parts_out || !parts_lse || !out || !lse) return MLA_VERIFY_ERR_NULL;
+  if (!aligned16(parts_out) || !aligned16(parts_lse) || !aligned16(out) || !aligned16(lse))
+    return MLA_VERIFY_ERR_ALIGN;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  if (num_parts < 1 || num_parts > mlav::MAX_NSPLIT) return MLA_VERIFY_ERR_ARG;
+  const int dev_status = check_device(pl);
+  if (dev_status != MLA_VERIFY_OK) return dev_status;
+  Params p{};
+  p.batch = batch;
+  p.T = pl->T;
+  p.H = pl->H;
+  p.R = pl->R;
+  p.nsplit = num_parts;
+  p.shard = 0;
+  p.num_shards = 1;
+  // Part s of request b, row r: parts_out[((s * batch + b) * R + r) * 512].
+  p.ws_o = const_cast<float*>(parts_out);
+  p.ws_lse = const_cast<float*>(parts_lse);
+  p.ws_stride_b = pl->R;
+  p.ws_stride_s = 1LL * batch * pl->R;
+  p.out = out;
+  p.lse = lse;
+  p.out_bf16 = pl->out_dtype == MLA_VERIFY_OUT_BF16;
+  p.err = pl->err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mlav::launch_combine(p, s, false) != cudaSuccess || note_done(pl, s) != cudaSuccess)
+    return MLA_VERIFY_ERR_CUDA;
   return MLA_VERIFY_OK;
 }
 
@@ -500,7 +595,8 @@ int mla_verify_build_indices(mla_verify_plan* pl, int batch, const int32_t* req_
   a.kv_indptr = kv_indptr;
   a.kv_lens = kv_lens;
   a.err = pl->err;
-  if (mlav::launch_build_indices(a, pl->max_kv_len, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (mlav::launch_build_indices(a, pl->max_kv_len, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      note_done(pl, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
   return MLA_VERIFY_OK;
 }
@@ -539,7 +635,8 @@ int mla_verify_compact_kv(mla_verify_plan* pl, int batch, const void* kv_src, in
   a.batch = batch;
   a.max_kv_len = pl->max_kv_len;
   a.err = pl->err;
-  if (mlav::launch_compact_kv(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (mlav::launch_compact_kv(a, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      note_done(pl, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
   return MLA_VERIFY_OK;
 }
@@ -549,11 +646,13 @@ int mla_verify_get_error(mla_verify_plan* pl, int* device_status, int clear) {
   const int dev_status = check_device(pl);
   if (dev_status != MLA_VERIFY_OK) return dev_status;
   int v = 0;
-  if (cudaDeviceSynchronize() != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
-  if (cudaMemcpy(&v, pl->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  // The last eager call's kernels are done once its event is; the word is
+  // then read (and cleared) on the plan's own stream only.
+  if (pl->done_recorded && cudaEventSynchronize(pl->done_ev) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, pl->err, sizeof(int), cudaMemcpyDeviceToHost, pl->aux) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
-  if (clear && cudaMemset(pl->err, 0, sizeof(int)) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
-  if (clear && cudaDeviceSynchronize() != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (clear && cudaMemsetAsync(pl->err, 0, sizeof(int), pl->aux) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (cudaStreamSynchronize(pl->aux) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
   *device_status = v;
   return MLA_VERIFY_OK;
 }

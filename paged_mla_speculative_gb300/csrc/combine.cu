@@ -30,13 +30,12 @@ __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
   const int r = static_cast<int>(row - static_cast<long long>(b) * p.R);
   const int ns = p.nsplit;
 
-  const float L = lane < ns ? p.ws_lse[(static_cast<size_t>(b) * ns + lane) * p.R + r] : -INFINITY;
+  const float L = lane < ns ? p.ws_lse[ws_base(p, b, lane) + r] : -INFINITY;
   float4 early[EARLY][4];
 #pragma unroll
   for (int s = 0; s < EARLY; ++s) {
     if (s < ns) {
-      const float4* src = reinterpret_cast<const float4*>(
-          p.ws_o + ((static_cast<size_t>(b) * ns + s) * p.R + r) * D_V);
+      const float4* src = reinterpret_cast<const float4*>(p.ws_o + (ws_base(p, b, s) + r) * D_V);
 #pragma unroll
       for (int k = 0; k < 4; ++k) early[s][k] = __ldcs(src + lane + 32 * k);
     }
@@ -74,8 +73,7 @@ __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
   for (int s = EARLY; s < ns; ++s) {
     const float ws = __shfl_sync(0xffffffffu, w, s);
     if (ws == 0.f) continue;  // uniform across the warp
-    const float4* src = reinterpret_cast<const float4*>(
-        p.ws_o + ((static_cast<size_t>(b) * ns + s) * p.R + r) * D_V);
+    const float4* src = reinterpret_cast<const float4*>(p.ws_o + (ws_base(p, b, s) + r) * D_V);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float4 v = __ldcs(src + lane + 32 * k);

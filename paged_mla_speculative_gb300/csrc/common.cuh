@@ -1,6 +1,7 @@
 // Shared device-side definitions of the verify-attention kernels.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,6 +25,7 @@ enum : int {
   ERR_INTERNAL = 32,
   ERR_POOL = 64,       // index builder: pool row, prefix or length out of range
   ERR_CAPACITY = 128,  // index builder: kv_indices capacity exceeded
+  ERR_RANGE = 256,     // an input value widened to fp16 is outside its range
 };
 
 // Arguments of one verify call, shared by every kernel of the call.
@@ -52,6 +54,13 @@ struct Params {
                                 // (overlapping pack); 0: wait for its grid
   int direct_all;               // 1: no pack; every attention CTA gathers its
                                 // own key blocks from the cache
+  // Context-parallel shard of this call: every request's 128-key blocks are
+  // dealt out evenly over num_shards and the call covers shard `shard` only
+  // (0 and 1 for a whole call).
+  int shard, num_shards;
+  // Workspace row of split s of request b, query row r:
+  // b * ws_stride_b + s * ws_stride_s + r (rows of 512 floats / one lse).
+  long long ws_stride_b, ws_stride_s;
   // Hand-off between the pack and the attention kernel of one call:
   // [0] epoch (calls completed), [1] ticket (attention CTAs done this call),
   // [4 + 32 * (b * packed_max_blocks + kb) + g] = epoch + 1 once keys
@@ -66,8 +75,11 @@ struct Request {
   int n;        // kv_len: prefix + drafts
   int P;        // prefix length
   int ip0;      // first index position
+  int lo, hi;   // logical keys [lo, hi) this call covers (its shard)
   bool ok;      // length and indptr consistent
 };
+
+constexpr int SHARD_KEYS = 128;   // shard boundaries fall on multiples of this
 
 __device__ __forceinline__ Request load_request(const Params& p, int b) {
   Request r;
@@ -80,7 +92,29 @@ __device__ __forceinline__ Request load_request(const Params& p, int b) {
   const bool len_ok = r.n >= p.T && r.n <= p.max_kv_len;
   const bool ptr_ok = r.ip0 >= 0 && ip1 >= r.ip0 && ip1 <= ipn && (long long)(ip1 - r.ip0) == need;
   r.ok = len_ok && ptr_ok;
+  // Shard s of S takes the request's 128-key blocks floor(s*nb/S) ..
+  // floor((s+1)*nb/S) - 1, clipped to n.
+  const long long nb = (static_cast<long long>(r.n) + SHARD_KEYS - 1) / SHARD_KEYS;
+  const long long b0 = nb * p.shard / p.num_shards, b1 = nb * (p.shard + 1) / p.num_shards;
+  r.lo = static_cast<int>(min(static_cast<long long>(r.n), b0 * SHARD_KEYS));
+  r.hi = static_cast<int>(min(static_cast<long long>(r.n), b1 * SHARD_KEYS));
+  if (!r.ok) r.lo = r.hi = 0;
   return r;
+}
+
+// Blocks [kb0, kb1) of `bn` keys that split `split` of `nsplit` takes of the
+// request's range [lo, hi): the range's blocks divided evenly.
+__device__ __forceinline__ void split_blocks(const Request& rq, int bn, int split, int nsplit, int& kb0,
+                                             int& kb1) {
+  const int a = rq.lo / bn, z = (rq.hi + bn - 1) / bn;
+  const long long nb = z > a ? z - a : 0;
+  kb0 = a + static_cast<int>(nb * split / nsplit);
+  kb1 = a + static_cast<int>(nb * (split + 1) / nsplit);
+}
+
+// First workspace row of split s of request b.
+__device__ __forceinline__ size_t ws_base(const Params& p, int b, int s) {
+  return static_cast<size_t>(b * p.ws_stride_b + s * p.ws_stride_s);
 }
 
 // Bit i of the result is set iff draft i is t itself or an ancestor of t.
@@ -112,6 +146,26 @@ __device__ __forceinline__ long long key_slot(const Params& p, int ip0, int j) {
   }
   const long long pg = p.kv_indices[ip0 + j / PAGE];
   return (pg >= 0 && pg < p.num_slots / PAGE) ? pg * PAGE + (j % PAGE) : -1;
+}
+
+// bf16 pair -> fp16 pair (round to nearest).  Exact for |x| in [2^-14,
+// 65504]; a magnitude of 65536 or more becomes inf, which `bad` records (it
+// is also set by a NaN input) so the caller can report ERR_RANGE.
+__device__ __forceinline__ uint32_t widen_bf16x2(uint32_t w, bool& bad) {
+  const float lo = __uint_as_float(w << 16);
+  const float hi = __uint_as_float(w & 0xffff0000u);
+  __half2 h = __floats2half2_rn(lo, hi);
+  const uint32_t r = *reinterpret_cast<uint32_t*>(&h);
+  bad |= ((r & 0x7c00u) == 0x7c00u) | ((r & 0x7c000000u) == 0x7c000000u);
+  return r;
+}
+__device__ __forceinline__ uint4 widen_bf16x8(uint4 v, bool& bad) {
+  return make_uint4(widen_bf16x2(v.x, bad), widen_bf16x2(v.y, bad), widen_bf16x2(v.z, bad),
+                    widen_bf16x2(v.w, bad));
+}
+// One atomic per warp for a per-thread range flag (all lanes must call).
+__device__ __forceinline__ void report_range(bool bad, int* err) {
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(err, ERR_RANGE);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {

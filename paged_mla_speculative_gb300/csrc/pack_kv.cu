@@ -64,13 +64,6 @@ __device__ __forceinline__ uint4 load_row_granule(const uint4* src, uint64_t pol
   return v;
 }
 
-__device__ __forceinline__ uint32_t widen(uint32_t w) {
-  const float lo = __uint_as_float(w << 16);
-  const float hi = __uint_as_float(w & 0xffff0000u);
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
 constexpr int QUARTER = BN / 4;   // keys per CTA of pack_kv_kernel
 
 // One CTA packs a quarter block (32 keys x 72 granules): every thread has
@@ -85,13 +78,12 @@ __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8
   const int kb = blockIdx.x >> 2, quarter = blockIdx.x & 3, b = blockIdx.y, tid = threadIdx.x;
   const Request rq = load_request(p, b);
   if (!rq.ok) return;                      // the attention kernel reports the request
-  const int nblk = (rq.n + BN - 1) / BN;
-  if (kb >= nblk) return;
+  if (kb < rq.lo / BN || kb >= (rq.hi + BN - 1) / BN) return;   // outside the call's keys
   const int key0 = quarter * QUARTER;      // first key of this quarter within the block
   if (tid < QUARTER) {
     const int j = kb * BN + key0 + tid;
     long long s = -1;
-    if (j < rq.n) {
+    if (j >= rq.lo && j < rq.hi) {
       s = key_slot(p, rq.ip0, j);
       if (s < 0) atomicOr(p.err, ERR_SLOT);
     }
@@ -114,10 +106,10 @@ __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8
     v[u] = slot >= 0 ? load_row_granule(reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(slot) * D_QK) + q, pol)
                      : make_uint4(0, 0, 0, 0);
   }
+  bool bad = false;
 #pragma unroll
-  for (int u = 0; u < PER_THREAD; ++u)
-    *reinterpret_cast<uint4*>(dst + off[u]) =
-        make_uint4(widen(v[u].x), widen(v[u].y), widen(v[u].z), widen(v[u].w));
+  for (int u = 0; u < PER_THREAD; ++u) *reinterpret_cast<uint4*>(dst + off[u]) = widen_bf16x8(v[u], bad);
+  report_range(bad, p.err);
 }
 
 constexpr int UNIT_KEYS = 4;                        // keys per warp unit
@@ -126,12 +118,6 @@ constexpr int PER_LANE = ROW_CHUNKS / 8;               // 9 granules per lane (8
 static_assert(UNIT_KEYS * 8 == 32 && PER_LANE * 8 == ROW_CHUNKS, "8 lanes per key");
 static_assert(UNITS_PER_BLOCK == 32, "one flag per lane of the reader's warp");
 
-// Block range [kb0, kb1) of split `split` of a request with nblk blocks: the
-// same even division the attention kernel uses.
-__device__ __forceinline__ int split_begin(int split, int nblk, int nsplit) {
-  return static_cast<int>((static_cast<long long>(split) * nblk) / nsplit);
-}
-
 // Packed blocks whose descriptions every pack CTA tabulates in shared memory
 // (16 bytes each); larger calls describe each block as they reach it.
 constexpr int TABLE_BLOCKS = 12288;
@@ -139,18 +125,21 @@ constexpr int TABLE_BLOCKS = 12288;
 // Block q of the pack order: split q % nsplit, request (q / nsplit) %
 // batch, position q / nsplit / batch within the split.  Returns (packed
 // block b * max_blocks + kb, first index position of the request, first key
-// kb * 128, kv_len), or x = -1 when there is nothing to pack (past the
-// split, or the request is invalid -- the attention kernel reports it).
+// kb * 128, end of the call's keys), or x = -1 when there is nothing to pack
+// (past the split, or the request is invalid -- the attention kernel reports
+// it).  A shard's keys start on a block boundary, so every key of a block
+// from its first key up to the end is in the call's range.
 __device__ __noinline__ int4 block_info(const Params& p, int q, int max_blocks) {
   const int split = q % p.nsplit;
   const int r = q / p.nsplit;
   const int b = r % p.batch, pos = r / p.batch;
   const Request rq = load_request(p, b);
   if (!rq.ok) return make_int4(-1, 0, 0, 0);
-  const int nblk = (rq.n + BN - 1) / BN;
-  const int kb = split_begin(split, nblk, p.nsplit) + pos;
-  if (kb >= split_begin(split + 1, nblk, p.nsplit)) return make_int4(-1, 0, 0, 0);
-  return make_int4(b * max_blocks + kb, rq.ip0, kb * BN, rq.n);
+  int kb0, kb1;   // the attention kernel's division of the call's keys
+  split_blocks(rq, BN, split, p.nsplit, kb0, kb1);
+  const int kb = kb0 + pos;
+  if (kb >= kb1) return make_int4(-1, 0, 0, 0);
+  return make_int4(b * max_blocks + kb, rq.ip0, kb * BN, rq.hi);
 }
 
 // Unit u: 4-key group u % 32 of block u / 32 of the pack order.  blk: the
@@ -191,14 +180,12 @@ __device__ __forceinline__ void load_unit(const Params& p, const Unit& t, int la
 }
 
 __device__ __forceinline__ void store_unit(uint8_t* packed, const Unit& t, int grp, int lane,
-                                           const uint4 (&v)[PER_LANE]) {
+                                           const uint4 (&v)[PER_LANE], bool& bad) {
   const int j = grp * UNIT_KEYS + (lane >> 3);   // key within the block
   uint8_t* dst = packed + static_cast<size_t>(t.blk) * BLOCK_BYTES + j * 128 +
                  (((lane & 7) ^ (j & 7)) << 4);
 #pragma unroll
-  for (int i = 0; i < PER_LANE; ++i)
-    *reinterpret_cast<uint4*>(dst + i * (BN * 128)) =
-        make_uint4(widen(v[i].x), widen(v[i].y), widen(v[i].z), widen(v[i].w));
+  for (int i = 0; i < PER_LANE; ++i) *reinterpret_cast<uint4*>(dst + i * (BN * 128)) = widen_bf16x8(v[i], bad);
 }
 
 // Pack units first, first + stride, .. below `end`.  Per round a warp
@@ -209,6 +196,7 @@ __device__ __forceinline__ void pack_units(const Params& p, const int4* s_tab, u
                                            int max_blocks, int u, int end, int stride, int lane,
                                            unsigned tag) {
   if (u >= end) return;
+  bool bad = false;
   Unit cur = locate(p, s_tab, max_blocks, u, lane);
   uint4 v[PER_LANE];
   if (cur.blk >= 0) load_unit(p, cur, lane, v);
@@ -217,7 +205,7 @@ __device__ __forceinline__ void pack_units(const Params& p, const int4* s_tab, u
     const bool more = u + stride < end;
     const Unit nxt = locate(p, s_tab, max_blocks, more ? u + stride : u, lane);
     if (cur.blk >= 0) {
-      store_unit(packed, cur, u & (UNITS_PER_BLOCK - 1), lane, v);
+      store_unit(packed, cur, u & (UNITS_PER_BLOCK - 1), lane, v, bad);
       // The stores must reach the reader's bulk copies (async proxy).
       asm volatile("fence.proxy.async.global;\n" ::: "memory");
     }
@@ -234,6 +222,7 @@ __device__ __forceinline__ void pack_units(const Params& p, const int4* s_tab, u
     }
     cur = nxt;
   }
+  report_range(bad, p.err);
 }
 
 // Two phases in one launch.  CTAs from `stay` on pack the units of the

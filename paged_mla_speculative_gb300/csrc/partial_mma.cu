@@ -83,21 +83,13 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// bf16 -> fp16 for a tile of `rows` 1152-byte rows, in place.
-__device__ __forceinline__ void widen_tile(uint8_t* tile, int rows, int tid) {
+// bf16 -> fp16 for a tile of `rows` 1152-byte rows, in place; `bad` records
+// a value outside the fp16 range.
+__device__ __forceinline__ void widen_tile(uint8_t* tile, int rows, int tid, bool& bad) {
   const int chunks = rows * ROW_CHUNKS;
   for (int c = tid; c < chunks; c += NTHREADS) {
     uint4* ptr = reinterpret_cast<uint4*>(tile + c * 16);
-    uint4 v = *ptr;
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = __uint_as_float(w[i] << 16);
-      const float hi = __uint_as_float(w[i] & 0xffff0000u);
-      __half2 h = __floats2half2_rn(lo, hi);
-      w[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+    *ptr = widen_bf16x8(*ptr, bad);
   }
 }
 
@@ -105,7 +97,7 @@ __device__ __forceinline__ void widen_tile(uint8_t* tile, int rows, int tid) {
 // table points outside the cache (reported).
 __device__ __forceinline__ int block_slot(const Params& p, const Request& rq, int kb, int r) {
   const int j = kb * BN + r;
-  if (j >= rq.n) return -1;
+  if (j < rq.lo || j >= rq.hi) return -1;
   const long long s = key_slot(p, rq.ip0, j);
   if (s < 0) atomicOr(p.err, ERR_SLOT);
   return static_cast<int>(s);
@@ -139,7 +131,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
   uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
 
   const Request rq = load_request(p, b);
-  const size_t ws_row = (static_cast<size_t>(b) * p.nsplit + split) * p.R;
+  const size_t ws_row = ws_base(p, b, split);
 
   // Rows of this thread's accumulator fragments (local to the 64-row tile).
   const int lrA = rg * 16 + (lane >> 2);
@@ -169,9 +161,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
     return;
   }
 
-  const int nblk = (rq.n + BN - 1) / BN;
-  const int kb0 = static_cast<int>((static_cast<long long>(split) * nblk) / p.nsplit);
-  const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * nblk) / p.nsplit);
+  int kb0, kb1;
+  split_blocks(rq, BN, split, p.nsplit, kb0, kb1);
 
   // Parents in one parallel load; the chains are walked in shared memory
   // after the barrier (a walk through global memory costs one round trip a
@@ -232,8 +223,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_mma_kernel(const Params p
       cp_async_wait<0>();
     }
     __syncthreads();
-    widen_tile(stage, BN, tid);
-    if (kb == kb0) widen_tile(smem, BM, tid);
+    {
+      bool bad = false;
+      widen_tile(stage, BN, tid, bad);
+      if (kb == kb0) widen_tile(smem, BM, tid, bad);
+      report_range(bad, p.err);
+    }
     __syncthreads();
 
     const uint32_t skv = smem_u32(stage);

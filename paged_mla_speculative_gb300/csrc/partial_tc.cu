@@ -142,7 +142,7 @@ __device__ __forceinline__ void wait_drain(uint32_t mbar, uint32_t parity, int* 
 __device__ __forceinline__ int block_slot(const Params& p, const Request& rq, int kb, int r,
                                           bool report) {
   const int j = kb * BN + r;
-  if (j >= rq.n) return -1;
+  if (j < rq.lo || j >= rq.hi) return -1;
   const long long s = key_slot(p, rq.ip0, j);
   if (s < 0 && report) atomicOr(p.err, ERR_SLOT);
   return static_cast<int>(s);
@@ -191,13 +191,6 @@ __device__ __forceinline__ void finish_call(const Params& p) {
   }
 }
 
-__device__ __forceinline__ uint32_t widen_word(uint32_t w) {
-  const float lo = __uint_as_float(w << 16);
-  const float hi = __uint_as_float(w & 0xffff0000u);
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
 // Column maxima of a warp's 32 x 32 tile (lane = key, v[c] = column c) in 31
 // shuffles: each step halves the columns a lane holds and swaps the other
 // half with the partner lane, so lane l ends with the maximum of column l
@@ -217,7 +210,7 @@ __device__ __forceinline__ void transpose_max32(float (&v)[32], int lane) {
 
 __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split, int row0, int tid) {
   const float nan = __int_as_float(0x7fc00000);
-  const size_t ws_row = (static_cast<size_t>(b) * p.nsplit + split) * p.R;
+  const size_t ws_row = ws_base(p, b, split);
   for (int i = tid; i < BM * D_V; i += NTHREADS) {
     const int lr = i / D_V, d = i - lr * D_V;
     const int gr = row0 + lr;
@@ -289,9 +282,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     return;
   }
 
-  const int nblk = (rq.n + BN - 1) / BN;
-  const int kb0 = static_cast<int>((static_cast<long long>(split) * nblk) / p.nsplit);
-  const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * nblk) / p.nsplit);
+  int kb0, kb1;
+  split_blocks(rq, BN, split, p.nsplit, kb0, kb1);
   const int nb = kb1 - kb0;
 
   // Parents in one parallel load; the softmax warps walk the chains in
@@ -400,12 +392,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       if (tid < p.T) s_mask[tid] = ancestor_mask(s_par, tid, p.err);
       asm volatile("cp.async.wait_group 0;\n" ::: "memory");
       named_sync(1, SOFTMAX_WARPS * 32);
+      bool bad = false;
 #pragma unroll 1
       for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
         uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_Q + e * 16);
-        uint4 v = *ptr;
-        *ptr = make_uint4(widen_word(v.x), widen_word(v.y), widen_word(v.z), widen_word(v.w));
+        *ptr = widen_bf16x8(*ptr, bad);
       }
+      report_range(bad, p.err);
       tc::fence_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(mbar(MB_Q));
@@ -458,12 +451,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         }
         asm volatile("cp.async.wait_group 0;\n" ::: "memory");
         named_sync(1, SOFTMAX_WARPS * 32);
+        bool bad = false;
 #pragma unroll 1
         for (int e = tid; e < BN * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
           uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_KV + e * 16);
-          uint4 v = *ptr;
-          *ptr = make_uint4(widen_word(v.x), widen_word(v.y), widen_word(v.z), widen_word(v.w));
+          *ptr = widen_bf16x8(*ptr, bad);
         }
+        report_range(bad, p.err);
         tc::fence_async_smem();
         named_sync(1, SOFTMAX_WARPS * 32);
         if (tid == 0)
@@ -599,7 +593,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       if (gr < p.R) {
         const float lse = l > 0.f ? (s_mref[tid] + log2f(l)) * kLn2 : -INFINITY;
         if (p.nsplit == 1) p.lse[static_cast<size_t>(b) * p.R + gr] = lse;
-        else p.ws_lse[(static_cast<size_t>(b) * p.nsplit + split) * p.R + gr] = lse;
+        else p.ws_lse[ws_base(p, b, split) + gr] = lse;
       }
     }
   }
@@ -660,8 +654,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         const size_t grow = static_cast<size_t>(b) * p.R + row0 + r;
         void* dst = p.nsplit == 1
                         ? static_cast<void*>(static_cast<uint8_t*>(p.out) + grow * row_bytes)
-                        : static_cast<void*>(p.ws_o + ((static_cast<size_t>(b) * p.nsplit + split) * p.R +
-                                                       row0 + r) * D_V);
+                        : static_cast<void*>(p.ws_o + (ws_base(p, b, split) + row0 + r) * D_V);
         asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
                      "r"(sbase + OFF_KV + r * row_bytes), "r"(row_bytes)
                      : "memory");

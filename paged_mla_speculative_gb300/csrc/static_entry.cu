@@ -51,6 +51,16 @@ int setup_device(int dev, void** scratch) {
   return MLA_VERIFY_OK;
 }
 
+// A CUDA call of this entry failed: the cached address may belong to a
+// context that no longer exists (cudaDeviceReset), so the next call on the
+// device repeats the set-up.
+int forget_device(int dev) {
+  cudaGetLastError();
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  g_ready[dev] = false;
+  return MLA_VERIFY_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -95,7 +105,7 @@ extern "C" int mla_verify_attn_static(int batch, int num_drafts, int num_heads, 
     // The fallback word is shared by every call and keeps the last call's
     // bits: clear it first.
     err = reinterpret_cast<int*>(base + MLA_VERIFY_STATIC_SCRATCH_BYTES - 256);
-    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return forget_device(dev);
   }
 
   mlav::Params p{};
@@ -114,6 +124,10 @@ extern "C" int mla_verify_attn_static(int batch, int num_drafts, int num_heads, 
   p.num_slots = num_slots;
   p.max_kv_len = max_kv_len;
   p.nsplit = nsplit;
+  p.shard = 0;
+  p.num_shards = 1;
+  p.ws_stride_b = 1LL * nsplit * R;
+  p.ws_stride_s = R;
   // Every (request, split, row) partial is written before the combine reads
   // it, so the array needs no clearing between calls.
   p.ws_o = reinterpret_cast<float*>(base);
@@ -122,7 +136,7 @@ extern "C" int mla_verify_attn_static(int batch, int num_drafts, int num_heads, 
   p.lse = lse;
   p.out_bf16 = 0;
   p.err = err;
-  if (mlav::launch_partial_mma(p, s) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
-  if (nsplit > 1 && mlav::launch_combine(p, s, false) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
+  if (mlav::launch_partial_mma(p, s) != cudaSuccess) return forget_device(dev);
+  if (nsplit > 1 && mlav::launch_combine(p, s, false) != cudaSuccess) return forget_device(dev);
   return MLA_VERIFY_OK;
 }

@@ -76,3 +76,16 @@ def sample_rows(inp, per_request=3, seed=0):
         for t in ts[:per_request]:
             rows.append((b, int(t), int(g.integers(0, w.num_heads))))
     return rows
+
+
+def assert_bf16_parity(out_bf16, lse, ref_out, ref_lse, what=""):
+    """bf16 output: each element within the fp32 tolerance plus one bf16 ulp
+    of the reference (the rounding of the output itself); lse as for fp32."""
+    o = out_bf16.float().numpy().astype(np.float64)
+    l = np.asarray(lse, dtype=np.float64)
+    assert np.isfinite(o).all() and np.isfinite(l).all(), f"{what}: non-finite output"
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref_out), 2.0 ** -126))) - 7)
+    bad = np.abs(o - ref_out) > OUT_MAX_ABS + ulp
+    assert not bad.any(), f"{what}: {int(bad.sum())} bf16 elements beyond tolerance + 1 ulp"
+    el = np.abs(l - ref_lse)
+    assert el.max() <= LSE_MAX_ABS, f"{what}: lse max abs err {el.max():.3g}"

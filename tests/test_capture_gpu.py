@@ -1,11 +1,15 @@
 """The whole call records into a CUDA graph and replays with new data.
 
-The metadata (kv_lens, indices, parents) and q change between replays, so a
-replay that baked any device value into the graph would give the wrong
-answer; every replay must equal an eager call on the same buffers bit for
-bit, and match the oracle.
+Static buffers are captured once; between replays the metadata (kv_lens,
+indices, parents), q and the cache change, so a replay that baked any device
+value into the graph would give the wrong answer.  Every replay must equal
+an eager call on the same buffers bit for bit, and match the oracle.  Each
+key-pack schedule the library picks (pack overlapping the attention kernel,
+whole pack first, attention CTAs gathering directly), page size 64, bf16
+output, the mma.sync family and full-size workloads are captured.
 """
-import numpy as np
+import dataclasses
+
 import pytest
 import torch
 
@@ -24,25 +28,49 @@ def _cuda():
     build.build()
 
 
-def _inputs(seed, prefix, tree):
-    w = W.Workload(name="cap", batch=3, num_drafts=8, num_heads=16, prefix=prefix, tree=tree,
-                   num_slots=8192, spike_frac=0.01, seed=seed)
+def _inputs(seed, prefix, tree, T, H, ps):
+    w = W.Workload(name="cap", batch=3, num_drafts=T, num_heads=H, prefix=prefix, tree=tree,
+                   num_slots=8192, page_size=ps, spike_frac=0.01, seed=seed)
     return W.make_inputs(w)
 
 
-@pytest.mark.parametrize("nsplit", [1, 4])
-def test_graph_replay_with_changing_metadata(nsplit):
-    cases = [_inputs(1, (1000, 300, 20), "chain"), _inputs(2, (64, 1500, 999), "random"),
-             _inputs(3, (0, 7, 1800), "star")]
+# name: (T, H, page_size, out dtype, kernel, nsplit, expected schedule)
+CASES = {
+    "overlap": (8, 16, 1, torch.float32, mb.KERNEL_TC, 4, "overlap"),
+    "overlap_ps64_bf16": (8, 16, 64, torch.bfloat16, mb.KERNEL_TC, 4, "overlap"),
+    "overlap_one_split": (8, 16, 1, torch.float32, mb.KERNEL_TC, 1, "overlap"),
+    "whole": (8, 64, 1, torch.float32, mb.KERNEL_TC, 6, "whole"),
+    "whole_ps64_bf16": (8, 64, 64, torch.bfloat16, mb.KERNEL_TC, 6, "whole"),
+    "direct": (4, 16, 1, torch.float32, mb.KERNEL_TC, 4, "direct"),
+    "direct_ps64_bf16": (4, 16, 64, torch.bfloat16, mb.KERNEL_TC, 3, "direct"),
+    "direct_one_split": (4, 16, 1, torch.float32, mb.KERNEL_TC, 1, "direct"),
+    "mma": (8, 16, 1, torch.float32, mb.KERNEL_MMA, 3, "none"),
+}
+
+
+def _schedule(plan, batch):
+    wide, stay = plan.pack_schedule(batch)
+    if plan.kernel() == mb.KERNEL_MMA:
+        return "none"
+    if wide == 0 and stay == 0:
+        return "direct"
+    return "overlap" if stay > 0 else "whole"
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_graph_replay_with_changing_metadata(case):
+    T, H, ps, odt, kernel, nsplit, expect = CASES[case]
+    cases = [_inputs(1, (1000, 300, 20), "chain", T, H, ps),
+             _inputs(2, (64, 1500, 999), "random", T, H, ps),
+             _inputs(3, (0, 7, 1800), "star", T, H, ps)]
     max_idx = max(c.kv_indices.numel() for c in cases)
     dev = torch.device("cuda")
-    # Static buffers, sized for the largest case.
     q = torch.empty_like(cases[0].q, device=dev)
     cache = torch.empty_like(cases[0].kv_cache, device=dev)
     idx = torch.zeros(max_idx, dtype=torch.int32, device=dev)
     indptr = torch.empty(4, dtype=torch.int32, device=dev)
     lens = torch.empty(3, dtype=torch.int32, device=dev)
-    par = torch.empty((3, 8), dtype=torch.int32, device=dev)
+    par = torch.empty((3, T), dtype=torch.int32, device=dev)
 
     def load(c):
         q.copy_(c.q)
@@ -52,8 +80,13 @@ def test_graph_replay_with_changing_metadata(nsplit):
         lens.copy_(c.kv_lens)
         par.copy_(c.draft_parent)
 
-    plan = mb.Plan(3, 8, 16, 1, 8192, 2000)
+    plan = mb.Plan(3, T, H, ps, 8192, 2000, odt)
+    plan.set_kernel(kernel)
     plan.set_nsplit(nsplit)
+    sched = _schedule(plan, 3)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if expect != "whole" or sms - 3 * (T * H // 64) * nsplit < 16:
+        assert sched == expect, (case, sched)
     out, lse = plan.new_outputs(3)
     s = torch.cuda.Stream()
     load(cases[0])
@@ -74,6 +107,45 @@ def test_graph_replay_with_changing_metadata(nsplit):
         torch.cuda.synchronize()
         assert torch.equal(go, eo) and torch.equal(gl, el)
         ref_o, ref_l = G.oracle_full(c)
-        G.assert_parity(go.cpu().numpy(), gl.cpu().numpy(), ref_o, ref_l)
+        if odt == torch.float32:
+            G.assert_parity(go.cpu().numpy(), gl.cpu().numpy(), ref_o, ref_l, case)
+        else:
+            G.assert_bf16_parity(go.cpu(), gl.cpu().numpy(), ref_o, ref_l, case)
     assert plan.get_error() == 0
     plan.close()
+
+
+@pytest.mark.parametrize("name", ["decode_batch", "sweep_p65536", "decode_tp8", "decode_t1"])
+def test_full_size_graph_replay(name):
+    """A full-size workload captured in its benchmark configuration: two
+    replays with different q, each bit-identical to an eager call."""
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, device="cuda")
+    with G.make_plan(inp) as plan:
+        out, lse = plan.new_outputs(w.batch)
+        q = inp.q.clone()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+
+        def call(st):
+            mb.mla_verify_attn(plan, q, inp.kv_cache, inp.kv_indices, inp.kv_indptr, inp.kv_lens,
+                               inp.draft_parent, inp.scale, out, lse, stream=st)
+
+        with torch.cuda.stream(s):
+            call(s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            call(s)
+        gen = torch.Generator(device="cuda").manual_seed(5)
+        for i in range(2):
+            if i:
+                q.copy_(torch.randn(q.shape, generator=gen, device="cuda").to(torch.bfloat16))
+            g.replay()
+            torch.cuda.synchronize()
+            go, gl = out.clone(), lse.clone()
+            call(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            assert torch.equal(go, out) and torch.equal(gl, lse), name
+        assert plan.get_error() == 0
+        assert torch.isfinite(out).all()

@@ -4,6 +4,7 @@ visible in device data set the sticky device word and never fault.
 Every bad index here is caught by the kernels' own range checks before any
 memory access (the key is masked or the request is written as NaN)."""
 import ctypes
+import dataclasses
 
 import numpy as np
 import pytest
@@ -166,3 +167,51 @@ def test_unknown_fault_is_rejected():
     with G.make_plan(inp) as plan:
         with pytest.raises(mb.MlaVerifyError):
             plan.inject_fault(99)
+
+
+@pytest.mark.parametrize("where", ["key", "query"])
+@pytest.mark.parametrize("mode", ["packed", "direct", "mma"])
+def test_value_outside_fp16_range_sets_the_range_bit(where, mode):
+    """A bf16 value of 1e5 has no fp16 counterpart: the kernel that widens it
+    reports MLA_VERIFY_DEV_RANGE; an unaffected call leaves the bit clear."""
+    H = 16 if mode == "direct" else 32          # one 64-row tile -> direct gather
+    inp = _case(seed=40, num_heads=H, tree="chain")
+    kernel = mb.KERNEL_MMA if mode == "mma" else mb.KERNEL_TC
+    with G.make_plan(inp, kernel=kernel) as plan:
+        G.run(plan, inp)
+        assert plan.get_error() == 0
+        if where == "key":
+            slot = int(inp.kv_indices[5])
+            cache = inp.kv_cache.clone()
+            cache[slot, 17] = 1.0e5
+            bad = dataclasses.replace(inp, kv_cache=cache)
+        else:
+            q = inp.q.clone()
+            q[1, 2, 3, 100] = -1.0e5
+            bad = dataclasses.replace(inp, q=q)
+        G.run(plan, bad)
+        assert plan.get_error() & mb.DEV_RANGE
+        G.run(plan, inp)
+        assert plan.get_error() == 0
+
+
+def test_get_error_waits_for_the_call_without_a_device_sync():
+    """get_error returns the bits of the last call once it is done, while work
+    on another stream is left running (no device-wide synchronisation)."""
+    inp = _case(seed=41)
+    bad_idx = inp.kv_indices.clone()
+    bad_idx[3] = 10 ** 6
+    bad = dataclasses.replace(inp, kv_indices=bad_idx)
+    other = torch.cuda.Stream()
+    with G.make_plan(inp) as plan:
+        torch.cuda.synchronize()
+        # a one-CTA kernel that spins for a bounded ~0.5 s on another stream
+        with torch.cuda.stream(other):
+            torch.cuda._sleep(1_000_000_000)
+        ev = torch.cuda.Event()
+        ev.record(other)
+        mb.mla_verify_attn(plan, bad.q, bad.kv_cache, bad.kv_indices, bad.kv_indptr, bad.kv_lens,
+                           bad.draft_parent, bad.scale)
+        assert plan.get_error() & mb.DEV_BAD_SLOT
+        assert not ev.query(), "get_error waited for another stream's work"
+        other.synchronize()

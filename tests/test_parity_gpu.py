@@ -1,10 +1,13 @@
 """GPU parity of the verify attention against the fp64 oracle, through the C ABI.
 
-Small cases (several 64-row tiles, several 64-key blocks, ragged tails) are
-compared element by element; the full-size workloads, in the launch
-configuration the benchmark times, are compared on sampled query rows.
+Small cases (several 64-row tiles, several key blocks, ragged tails) and every
+full-size workload, in the launch configuration the benchmark times, are
+compared element by element.
 Tolerances: out max abs 1e-2 and mean abs 1e-3, lse max abs 1e-3.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -168,8 +171,19 @@ FULL = ["decode_batch", "tree", "sweep_p1024", "sweep_p4096", "sweep_p16384", "s
         "sweep_p93184", "ragged_ps1", "ragged_ps64", "decode_tp8", "decode_t1"]
 
 
+def _log_errors(name, errs):
+    """Append a workload's errors to $MLA_VERIFY_PARITY_LOG (JSON lines), if set."""
+    path = os.environ.get("MLA_VERIFY_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"workload": name, "out_max_abs": errs[0], "out_mean_abs": errs[1],
+                                "lse_max_abs": errs[2]}) + "\n")
+
+
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_rows(name):
+def test_full_size_every_element(name):
+    """Every output element of a full-size workload, in the launch
+    configuration the benchmark times, against the fp64 oracle."""
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w, device="cuda")
     with G.make_plan(inp) as plan:   # the automatic configuration the benchmark times
@@ -177,11 +191,7 @@ def test_full_size_sampled_rows(name):
         assert plan.get_error() == 0
     o = out.float().cpu().numpy()
     l = lse.cpu().numpy()
-    assert np.isfinite(o).all() and np.isfinite(l).all()
-    rows = G.sample_rows(inp, per_request=3 if w.batch > 8 else 6, seed=1)
-    if w.batch > 8:
-        rows = [r for r in rows if r[0] % 8 == 0]   # a quarter of the requests
-    ref_o, ref_l = G.oracle_rows(inp, rows)
-    got_o = np.stack([o[b, t, h] for b, t, h in rows])
-    got_l = np.array([l[b, t, h] for b, t, h in rows])
-    G.assert_parity(got_o, got_l, ref_o, ref_l, name)
+    del out, lse
+    ref_o, ref_l = G.oracle_full(inp)
+    errs = G.assert_parity(o, l, ref_o, ref_l, name)
+    _log_errors(name, errs)

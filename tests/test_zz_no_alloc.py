@@ -6,8 +6,8 @@ allocate after start-up, a layer that is only handed pointers).  It keeps its
 split partials in a fixed device array instead of a plan's workspace.  This
 test calls it twice in a row through the C ABI and compares each result with
 mla_verify_attn on the same inputs, same kernel family and same split count,
-within the parity tolerances used everywhere else (out max abs 1e-2, mean abs
-1e-3; lse max abs 1e-3).  It lives in a file collected last so that a run
+and with the fp64 oracle, within the parity tolerances used everywhere else
+(out max abs 1e-2, mean abs 1e-3; lse max abs 1e-3), for page sizes 1 and 64.  It lives in a file collected last so that a run
 stopping at the first failure has already run every other test.
 """
 import ctypes
@@ -43,18 +43,20 @@ def _static_call(inp, nsplit, out, lse, status):
         torch.cuda.current_stream().cuda_stream)
 
 
+@pytest.mark.parametrize("ps", [1, 64])
 @pytest.mark.parametrize("nsplit", [3, 1])
-def test_static_entry_matches_plan_entry_twice(nsplit):
-    inputs = [
-        G.to_cuda(W.make_inputs(W.Workload(name="na", batch=3, num_drafts=8, num_heads=16,
-                                           prefix=(900, 65, 300), tree="random", num_slots=4096,
-                                           spike_frac=0.01, seed=901))),
-        G.to_cuda(W.make_inputs(W.Workload(name="nb", batch=3, num_drafts=8, num_heads=16,
-                                           prefix=(10, 1200, 0), tree="chain", num_slots=4096,
-                                           spike_frac=0.01, seed=902))),
+def test_static_entry_matches_plan_entry_twice(nsplit, ps):
+    raw = [
+        W.make_inputs(W.Workload(name="na", batch=3, num_drafts=8, num_heads=16,
+                                 prefix=(900, 65, 300), tree="random", num_slots=4096,
+                                 page_size=ps, spike_frac=0.01, seed=901)),
+        W.make_inputs(W.Workload(name="nb", batch=3, num_drafts=8, num_heads=16,
+                                 prefix=(10, 1200, 0), tree="chain", num_slots=4096,
+                                 page_size=ps, spike_frac=0.01, seed=902)),
     ]
+    inputs = [G.to_cuda(r) for r in raw]
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
-    for inp in inputs:          # two calls in a row, different data
+    for inp, cpu in zip(inputs, raw):          # two calls in a row, different data
         out = torch.full((3, 8, 16, 512), float("nan"), device="cuda")
         lse = torch.full((3, 8, 16), float("nan"), device="cuda")
         st = _static_call(inp, nsplit, out, lse, status)
@@ -66,6 +68,8 @@ def test_static_entry_matches_plan_entry_twice(nsplit):
         assert int(status[0]) == 0
         G.assert_parity(out.cpu().numpy(), lse.cpu().numpy(), ref_o.cpu().numpy().astype(np.float64),
                         ref_l.cpu().numpy().astype(np.float64), "static vs plan entry")
+        or_o, or_l = G.oracle_full(cpu)
+        G.assert_parity(out.cpu().numpy(), lse.cpu().numpy(), or_o, or_l, "static vs oracle")
 
 
 def test_static_entry_rejects_oversized_calls_and_reports_device_errors():
