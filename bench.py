@@ -76,14 +76,14 @@ def load_peaks():
 def kernel_source_hash():
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "paged_mla_speculative_gb300", "csrc")
-    for name in ("common.cuh", "tc_ptx.cuh", "partial_tc.cu"):
+    for name in ("common.cuh", "tc_ptx.cuh", "partial_tv.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
 def profiled_traffic(workload):
-    """DRAM bytes per launch of the partial kernel from a committed ncu
+    """DRAM bytes per launch of the attention kernel from a committed ncu
     summary, if it was taken on the current kernel source and workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -91,7 +91,7 @@ def profiled_traffic(workload):
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d.get("partial_tc_kernel", {})
+        e = d.get("partial_tv_kernel", {})
         if e.get("source_sha1") == kernel_source_hash() and e.get("workload") == workload:
             return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -137,16 +137,18 @@ def compaction_timing(mb, plan, inp, w, flush, stream, steps):
             "frac_of_hbm": gbs / hbm, "bound": "hbm", "launches": 2}
 
 
-def kernels_of(kernel, ns, pack_stay=0, schedule=None):
-    """The library kernels one call launches, for the JSON line (pack_stay >
-    0: the pack that overlaps the attention kernel; schedule "none": the
-    attention CTAs gather their own keys, no pack)."""
+PACK_NAMES = {1: "whole", 2: "idle_sms", 3: "resident", 4: "none"}
+PACK_KERNELS = {"whole": "pack_kv_kernel", "idle_sms": "pack_kv_overlap_kernel",
+                "resident": "pack_kv_resident_kernel"}
+
+
+def kernels_of(kernel, ns, schedule="whole"):
+    """The library kernels one call launches, for the JSON line (schedule:
+    the key-pack schedule, "none" when the attention CTAs gather their own
+    keys)."""
     from paged_mla_speculative_gb300 import binding as mb
-    pack = ["pack_kv_overlap_kernel" if pack_stay > 0 else "pack_kv_kernel"]
-    if schedule == "none":
-        pack = []
-    names = {mb.KERNEL_TC: pack + ["partial_tc_kernel"],
-             mb.KERNEL_MMA: ["partial_mma_kernel"]}[kernel]
+    tc = ["partial_tc_kernel"] if schedule == "none" else [PACK_KERNELS[schedule], "partial_tv_kernel"]
+    names = {mb.KERNEL_TC: tc, mb.KERNEL_MMA: ["partial_mma_kernel"]}[kernel]
     return " + ".join(names + (["combine_kernel"] if ns > 1 else []))
 
 
@@ -479,8 +481,7 @@ def measure_workload(mb, W, name, flush, steps, clocks=None):
     t_hbm, t_tc = work["bytes"] / (hbm * 1e9), work["flops"] / (tc * 1e12)
     t_roof = max(t_hbm, t_tc) * 1e6
     part_us = statistics.fmean(part_ms) * 1e3
-    wide, stay = plan.pack_schedule(w.batch)
-    sched = "none" if (wide, stay) == (0, 0) else ("overlap" if stay > 0 else "whole")
+    sched = PACK_NAMES[plan.pack_mode(w.batch)]
     kv_gbs = work["kv_bytes"] / (us * 1e-6) / 1e9
     res = {
         "us_per_call": us, "us_p10_p50_p90": [q[0] * 1e3, statistics.median(graph_ms) * 1e3, q[-1] * 1e3],
@@ -494,7 +495,7 @@ def measure_workload(mb, W, name, flush, steps, clocks=None):
         "partial_tflops": work["flops"] / (part_us * 1e-6) / 1e12,
         "partial_frac_of_tensor_peak": work["flops"] / (part_us * 1e-6) / 1e12 / tc,
         "keys": work["keys"], "kv_bytes": work["kv_bytes"], "flops": work["flops"],
-        "nsplit": ns, "pack_schedule": sched, "kernels": kernels_of(plan.kernel(), ns, stay, sched),
+        "nsplit": ns, "pack_schedule": sched, "kernels": kernels_of(plan.kernel(), ns, sched),
         "calls_timed": len(graph_ms),
     }
     state = {"inp": inp, "plan": plan, "out": out, "lse": lse, "work": work, "wall": wall,
@@ -573,8 +574,9 @@ def run_gb300(args):
         db_plan = plan if head == "decode_batch" else mb.Plan(
             dbw.batch, dbw.num_drafts, dbw.num_heads, dbw.page_size, dbw.num_slots,
             max(db_inp.kv_lens.tolist()))
-        extra["index_builder"] = index_builder_timing(mb, db_plan, db_inp, dbw, flush, stream, min(K, 300))
-        extra["compaction"] = compaction_timing(mb, db_plan, db_inp, dbw, flush, stream, min(K, 200))
+        cur = torch.cuda.current_stream()     # the flush and the timed call share a stream
+        extra["index_builder"] = index_builder_timing(mb, db_plan, db_inp, dbw, flush, cur, min(K, 300))
+        extra["compaction"] = compaction_timing(mb, db_plan, db_inp, dbw, flush, cur, min(K, 200))
         if db_plan is not plan:
             db_plan.close()
         del db_inp
@@ -593,7 +595,7 @@ def run_gb300(args):
             "partial_us", "combine_us")}},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak, "traffic": profiled_traffic(head),
-                     "kernel": "partial_tc_kernel", "workload": head,
+                     "kernel": "partial_tv_kernel", "workload": head,
                      "peak_source": f"{st['peak_src']} bf16 burst (fp16 has the same tensor rate)"},
         "clocks": clk.summary(), "gpu_launches": launches,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,

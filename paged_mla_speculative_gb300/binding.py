@@ -22,6 +22,11 @@ OUT_BF16 = 1
 KERNEL_AUTO = 0
 KERNEL_MMA = 1
 KERNEL_TC = 2
+PACK_AUTO = 0
+PACK_WHOLE = 1
+PACK_IDLE_SMS = 2
+PACK_RESIDENT = 3
+PACK_NONE = 4
 FAULT_NONE = 0
 FAULT_SKIP_PACK = 1
 MAX_NSPLIT = 32
@@ -52,6 +57,8 @@ SIGNATURES = {
     "mla_verify_plan_inject_fault": (_I, [_P, _I]),
     "mla_verify_plan_get_pack_schedule": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(ctypes.c_int)]),
+    "mla_verify_plan_set_pack_schedule": (_I, [_P, _I]),
+    "mla_verify_plan_get_pack_mode": (_I, [_P, _I]),
     "mla_verify_plan_set_kernel": (_I, [_P, _I]),
     "mla_verify_plan_get_kernel": (_I, [_P]),
     "mla_verify_plan_workspace_bytes": (ctypes.c_size_t, [_P]),
@@ -176,6 +183,19 @@ class Plan:
         if rc != 0:
             raise MlaVerifyError(rc, "get_pack_schedule")
         return wide.value, stay.value
+
+    def set_pack_schedule(self, schedule: int):
+        """Force a key-pack schedule (PACK_WHOLE / PACK_IDLE_SMS / PACK_RESIDENT)
+        or PACK_AUTO."""
+        _check(load_library().mla_verify_plan_set_pack_schedule(self.handle, schedule),
+               "set_pack_schedule")
+
+    def pack_mode(self, batch: int) -> int:
+        """The pack schedule a call with `batch` requests uses (PACK_NONE: no pack)."""
+        v = load_library().mla_verify_plan_get_pack_mode(self.handle, batch)
+        if v < 0:
+            raise MlaVerifyError(v, "get_pack_mode")
+        return v
 
     def inject_fault(self, fault: int):
         """Testing hook: inject a host-side fault into the next call (see the

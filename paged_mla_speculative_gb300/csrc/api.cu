@@ -53,6 +53,7 @@ struct mla_verify_plan {
   // the tag the next call will use, so the next call clears them first.
   bool pack_flags_dirty;
   int fault;              // MLA_VERIFY_FAULT_* injected into the next call
+  int pack_mode;          // MLA_VERIFY_PACK_* forced, or AUTO
   // mla_verify_get_error: an event recorded at the end of the last call made
   // outside capture, and a private stream to read the error word on.
   cudaEvent_t done_ev;
@@ -81,6 +82,7 @@ constexpr long long kDirectMaxTiles = 1;   // 2 tiles measured slower (each bloc
 // its first block.  When that needs more than half the positions, or
 // otherwise, the whole pack runs first (stay = 0).
 struct PackSchedule {
+  int mode;       // MLA_VERIFY_PACK_WHOLE, _IDLE_SMS or _RESIDENT
   int wide, stay;
 };
 constexpr int kMinPackSms = 16;
@@ -88,8 +90,11 @@ PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool ov
   const int positions = static_cast<int>(ceil_div(ceil_div(pl->pack_blocks, shards), nsplit));
   const long long attn = 1LL * nsplit * ceil_div(pl->R, kRowsPerTile) * batch;
   const long long idle = pl->num_sms - attn;
-  const PackSchedule whole{positions, 0};
-  if (!overlap || idle < kMinPackSms) return whole;
+  const PackSchedule whole{MLA_VERIFY_PACK_WHOLE, positions, 0};
+  if (!overlap || pl->pack_mode == MLA_VERIFY_PACK_WHOLE) return whole;
+  if (pl->pack_mode == MLA_VERIFY_PACK_RESIDENT) return PackSchedule{MLA_VERIFY_PACK_RESIDENT, 0, pl->num_sms};
+  const bool forced_idle = pl->pack_mode == MLA_VERIFY_PACK_IDLE_SMS;
+  if (idle < (forced_idle ? 1 : kMinPackSms)) return whole;
   const double per_block_us = 3.4, lead_us = 5.0, blocks_per_us_per_sm = 0.15;
   const double narrow_us = static_cast<double>(nsplit) * batch / (idle * blocks_per_us_per_sm);
   // Position q >= wide is ready after (q - wide + 1) narrow steps and needed
@@ -99,8 +104,8 @@ PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool ov
   if (narrow_us > per_block_us)
     wide = static_cast<int>(std::ceil(positions - (lead_us + (positions - 1) * per_block_us) / narrow_us));
   wide = std::max(1, wide);
-  if (2 * wide > positions) return whole;
-  return PackSchedule{wide, static_cast<int>(idle)};
+  if (2 * wide > positions && !forced_idle) return whole;
+  return PackSchedule{MLA_VERIFY_PACK_IDLE_SMS, std::min(wide, positions), static_cast<int>(idle)};
 }
 
 PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, bool overlap) {
@@ -114,7 +119,7 @@ PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, boo
 double pack_steps(const mla_verify_plan* pl, int batch, int nsplit, int shards) {
   if (ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles) return 0.0;
   const PackSchedule ps = pack_plan(pl, batch, nsplit, true, shards);
-  if (ps.stay > 0) return 9.0 / 3.4;
+  if (ps.mode != MLA_VERIFY_PACK_WHOLE) return 9.0 / 3.4;
   return (2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0) / 3.4;
 }
 
@@ -233,7 +238,7 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
   if (mlav::partial_mma_prepare() != cudaSuccess || mlav::partial_tc_prepare() != cudaSuccess ||
-      mlav::pack_kv_prepare() != cudaSuccess)
+      mlav::partial_tv_prepare() != cudaSuccess || mlav::pack_kv_prepare() != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
 
   mla_verify_plan* pl = new (std::nothrow) mla_verify_plan();
@@ -350,6 +355,23 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int*
   return MLA_VERIFY_OK;
 }
 
+int mla_verify_plan_set_pack_schedule(mla_verify_plan* pl, int schedule) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  if (schedule != MLA_VERIFY_PACK_AUTO && schedule != MLA_VERIFY_PACK_WHOLE &&
+      schedule != MLA_VERIFY_PACK_IDLE_SMS && schedule != MLA_VERIFY_PACK_RESIDENT)
+    return MLA_VERIFY_ERR_ARG;
+  pl->pack_mode = schedule;
+  return MLA_VERIFY_OK;
+}
+
+int mla_verify_plan_get_pack_mode(const mla_verify_plan* pl, int batch) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  if (pl->kernel != MLA_VERIFY_KERNEL_TC || ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles)
+    return MLA_VERIFY_PACK_NONE;
+  return pack_plan(pl, batch, effective_nsplit(pl, batch), true).mode;
+}
+
 int mla_verify_plan_inject_fault(mla_verify_plan* pl, int fault) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (fault != MLA_VERIFY_FAULT_NONE && fault != MLA_VERIFY_FAULT_SKIP_PACK) return MLA_VERIFY_ERR_ARG;
@@ -461,16 +483,19 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
     attn_overlap = false;   // the first kernel of the call: no programmatic overlap with the last call
   } else if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC) {
     const PackSchedule ps = pack_schedule(pl, p, overlap);
-    p.pack_flags = ps.stay > 0;
-    le = ps.stay > 0 ? mlav::launch_pack_kv_overlap(p, pl->packed, pl->pack_blocks, pl->num_sms, ps.wide,
-                                                    ps.stay, s)
-                     : mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
+    p.pack_flags = ps.mode != MLA_VERIFY_PACK_WHOLE;
+    le = ps.mode == MLA_VERIFY_PACK_RESIDENT
+             ? mlav::launch_pack_kv_resident(p, pl->packed, pl->pack_blocks, pl->num_sms, s)
+         : ps.mode == MLA_VERIFY_PACK_IDLE_SMS
+             ? mlav::launch_pack_kv_overlap(p, pl->packed, pl->pack_blocks, pl->num_sms, ps.wide, ps.stay, s)
+             : mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
   }
   const bool packed = le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack && !direct;
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)
     le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
-                                             : mlav::launch_partial_tc(p, s, attn_overlap);
+         : direct                            ? mlav::launch_partial_tc(p, s, attn_overlap)
+                                             : mlav::launch_partial_tv(p, s, attn_overlap);
   if (packed && le != cudaSuccess) pl->pack_flags_dirty = true;   // the epoch did not advance
   if (le == cudaSuccess && pl->ev_after_partial) le = cudaEventRecord(pl->ev_after_partial, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;

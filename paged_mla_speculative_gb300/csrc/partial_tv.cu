@@ -1,0 +1,723 @@
+// Split-KV partial kernel on the sm_103a tensor cores with the value tiles
+// in tensor memory: the default kernel for packed key blocks.
+//
+// One CTA = one request b, one tile of 64 query rows (r = t*H + h), one key
+// split: the KV-split "partial" half of the partial + reduce design in "The
+// Decisive A/B: When Benchmarking Honesty Reveals the Real Bottleneck"
+// (sections "The Context" and "What This Reveals About the Bottleneck").
+//
+// Products, transposed so that every MMA has M = 128:
+//     S^T[key, row] = K_block[128 x 576] . Q_tile[64 x 576]^T        (fp16)
+//     O^T[dim, row] += V_block^T[512 x 128] . P^T[128 x 64]           (fp16)
+// Tensor memory (512 columns): O^T as 4 tiles of 128 dims x 64 rows
+// (columns 0..255), the value tiles V^T of dims 0..383 as MMA A operands
+// (3 tiles x 64 columns of packed fp16, 256..447) and S^T (448..511).
+//
+// Why the values go to tensor memory.  Shared memory holds the Q tile
+// (72 KB) and one packed key block (144 KB), which leaves no room for a
+// second block; with both products reading the block from shared memory,
+// block k+1 cannot land until PV(k) is done, and PV(k) waits for the softmax
+// of k, so the tensor pipe idles through every softmax.  The packed block is
+// dim-major (pack_kv.cu), which is K-major for V^T, so tcgen05.cp moves the
+// value tiles of dims 0..383 into tensor memory as soon as QK^T has read
+// them; their shared memory then takes the next block, whose QK^T (over the
+// same dims) runs while the softmax of this block does.  Dims 384..511 and
+// the rope dims stay in shared memory (tensor memory is full) and the rope
+// region of each 64-key atom holds P^T once QK^T has read it.
+//
+// The running row max is exact, so P <= 1 and the key holding the max has
+// P = 1 exactly; P and the values are fp16 (P in bf16 costs more than the
+// 1e-2 output tolerance allows).  O^T columns are rescaled in tensor memory
+// only for the 32-row groups whose max moved.
+//
+// Roles (10 warps):
+//   warps 0-7  softmax: one thread per (key of the block, half of the 64
+//              query rows); warps w and w+4 share TMEM lane quadrant w.  They
+//              first load the Q tile (issued at entry) and widen it to fp16;
+//   warp 8     issues the MMAs and copies into tensor memory (one elected
+//              lane of the converged warp); it owns the TMEM allocation;
+//   warp 9     streams the packed blocks with cp.async.bulk, in five groups
+//              per block: dims 0-127, 128-255, 256-383, 384-511 and rope.
+// Tensor-pipe order per block k (mbarriers, every wait bounded):
+//   S^T(k) over dims 0..383 (during the softmax of k-1),
+//   O^T(k-1): tile 3 from shared memory first (its dims of block k may then
+//             load), tiles 0..2 from tensor memory,
+//   V^T(k) tiles 0..2 into tensor memory, each after O^T(k-1) has read the
+//             tile it replaces; each frees its dims' shared memory for k+1,
+//   S^T(k) over dims 384..575 -> the softmax of k may start.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace mlav {
+namespace {
+
+constexpr int BM = 64;          // query rows per CTA: MMA N
+constexpr int BN = 128;         // keys per block: MMA M of S^T
+constexpr int NWARPS = 10;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int SOFTMAX_WARPS = 8, MMA_WARP = 8, COPY_WARP = 9;
+constexpr int HALF = BM / 2;    // query-row columns per softmax thread
+constexpr int Q_CHUNK = BM * 128;   // one 64-dim chunk of the Q tile
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = OFF_Q + 9 * Q_CHUNK;      // packed block: atoms at +0, +PK_ATOM
+constexpr int ROPE_ROW = 512;                    // first rope dim row of an atom (P^T region)
+constexpr int OFF_RED = OFF_KV + PK_BLOCK;       // float [64][4] column max per quad; [4][64] sums
+constexpr int OFF_MREF = OFF_RED + 4 * 64 * 4;   // float [64] final running row max (base 2)
+constexpr int OFF_WARP = OFF_MREF + 64 * 4;      // float [8][2][32] per-warp row max / rescale factor
+constexpr int OFF_L = OFF_WARP + 8 * 64 * 4;     // float [64] reciprocal of the final row sums (0: none)
+constexpr int OFF_MASK = OFF_L + 64 * 4;         // uint32 [32] ancestor masks
+constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;   // int [64] draft of each row, -1 past R
+constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;      // uint64 [24] mbarriers
+constexpr int OFF_MISC = OFF_MBAR + 24 * 8;      // tmem base, abort flag
+constexpr int OFF_PAR = OFF_MISC + 16;           // int [32] draft parents
+constexpr int SMEM_TOTAL = OFF_PAR + MAX_T * 4;
+static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
+static_assert(OFF_KV % 1024 == 0 && PK_ATOM % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+// mbarrier indices
+constexpr int MB_CHUNK = 0;   // [5] copy groups of the block landed (copy bytes)
+constexpr int MB_S = 5;       // S^T done (tcgen05.commit)
+constexpr int MB_P = 6;       // P^T written, O^T rescaled (one arrival per softmax warp)
+constexpr int MB_Q = 7;       // Q tile in fp16 (one arrival per softmax warp)
+constexpr int MB_OT = 8;      // [4] O^T tile d done (tcgen05.commit)
+constexpr int MB_DONE = 12;   // after an abort: every tcgen05 op the CTA issued is done
+constexpr int MB_SFREE = 13;  // every softmax warp holds S^T in registers (8 arrivals)
+constexpr int MB_VCP = 14;    // [3] V^T tile d copied into tensor memory (commit)
+constexpr int NUM_MBAR = 17;
+static_assert(NUM_MBAR <= 24, "mbarrier area");
+
+constexpr int TMEM_COLS = 512;
+constexpr uint32_t TM_V = 256;                  // V^T tile d at TM_V + 64 d (d < 3)
+constexpr uint32_t TM_S = 448;                  // S^T columns; O^T tile d at 64 d
+constexpr long long WAIT_LIMIT = 1LL << 31;     // cycles before a wait gives up
+
+// S^T: A = keys x dims read MN-major from the dim-major block; B = Q K-major.
+constexpr uint32_t IDESC_S = tc::idesc_f16(128, BM, 0, 1, 0);
+// O^T: A = V^T K-major (tensor memory or shared memory); B = P^T MN-major.
+constexpr uint32_t IDESC_O = tc::idesc_f16(128, BM, 0, 0, 1);
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
+// Bounded wait; a timeout (or an earlier one anywhere in the CTA) sets the
+// abort flag so every later wait returns at once.
+__device__ __forceinline__ bool wait_phase(uint32_t mbar, uint32_t parity, volatile int* abort,
+                                           int* err) {
+  if (tc::mbar_test(mbar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (tc::mbar_try(mbar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > WAIT_LIMIT) {
+      *abort = 1;
+      atomicOr(err, ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Warp-wide wait (every lane polls).
+__device__ __forceinline__ void wait_warp(uint32_t mbar, uint32_t parity, volatile int* abort,
+                                          int* err) {
+  wait_phase(mbar, parity, abort, err);
+  __syncwarp();
+}
+
+// Bounded wait that ignores the abort flag: used to let this CTA's own
+// copies and MMAs finish before it exits.
+__device__ __forceinline__ void wait_drain(uint32_t mbar, uint32_t parity, int* err) {
+  const long long t0 = clock64();
+  while (!tc::mbar_try(mbar, parity)) {
+    if (clock64() - t0 > WAIT_LIMIT) {
+      atomicOr(err, ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Whether key r of block kb is in the call's range and its slot in the cache.
+__device__ __forceinline__ bool block_key_ok(const Params& p, const Request& rq, int kb, int r) {
+  const int j = kb * BN + r;
+  if (j < rq.lo || j >= rq.hi) return false;
+  return key_slot(p, rq.ip0, j) >= 0;
+}
+
+// Wait (bounded) until the pack kernel has published all 32 units of block
+// kb of request b for this call: lane l watches unit l's flag with acquire
+// loads.  Whole warp; false on a timeout or an earlier abort.
+__device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsigned tag,
+                                            volatile int* abort, int* err) {
+  const int lane = threadIdx.x & 31;
+  const unsigned* flag = p.pack_sync + PACK_SYNC_HEADER +
+                         32 * (static_cast<size_t>(b) * p.packed_max_blocks + kb) + lane;
+  const long long t0 = clock64();
+  while (true) {   // every exit decision is warp-uniform
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
+    if (__all_sync(0xffffffffu, v == tag)) break;
+    if (__any_sync(0xffffffffu, *abort != 0)) return false;
+    if (__any_sync(0xffffffffu, clock64() - t0 > WAIT_LIMIT)) {
+      if (lane == 0) {
+        *abort = 1;
+        atomicOr(err, ERR_TIMEOUT);
+      }
+      __syncwarp();
+      return false;
+    }
+  }
+  // The packed bytes were written through the generic proxy; the bulk copies
+  // that follow read them through the async proxy.
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+  return true;
+}
+
+// Every CTA takes one ticket when it is done; the last one of the grid
+// advances the epoch, so the next call's pack kernel publishes a new tag.
+// The epoch stays below 2^32 - 1, so the tag (epoch + 1) is never 0 -- the
+// value of a flag no call has written -- and consecutive tags differ.
+__device__ __forceinline__ void finish_call(const Params& p) {
+  __threadfence();
+  const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+  if (atomicAdd(p.pack_sync + 1, 1u) == total - 1) {
+    p.pack_sync[1] = 0;
+    const unsigned e = *reinterpret_cast<volatile unsigned*>(p.pack_sync);
+    *reinterpret_cast<volatile unsigned*>(p.pack_sync) = e + 1u == 0xffffffffu ? 0u : e + 1u;
+  }
+}
+
+// Column maxima of a warp's 32 x 32 tile (lane = key, v[c] = column c) in 31
+// shuffles: each step halves the columns a lane holds and swaps the other
+// half with the partner lane, so lane l ends with the maximum of column l
+// over all 32 lanes in v[0].
+__device__ __forceinline__ void transpose_max32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+    }
+  }
+}
+
+__device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split, int row0, int tid) {
+  const float nan = __int_as_float(0x7fc00000);
+  const size_t ws_row = ws_base(p, b, split);
+  for (int i = tid; i < BM * D_V; i += NTHREADS) {
+    const int lr = i / D_V, d = i - lr * D_V;
+    const int gr = row0 + lr;
+    if (gr >= p.R) continue;
+    if (p.nsplit == 1) {
+      const size_t o = (static_cast<size_t>(b) * p.R + gr) * D_V + d;
+      if (p.out_bf16) reinterpret_cast<uint16_t*>(p.out)[o] = 0x7fc0;
+      else reinterpret_cast<float*>(p.out)[o] = nan;
+      if (d == 0) p.lse[static_cast<size_t>(b) * p.R + gr] = nan;
+    } else {
+      p.ws_o[(ws_row + gr) * D_V + d] = nan;
+      if (d == 0) p.ws_lse[ws_row + gr] = nan;
+    }
+  }
+}
+
+// Shared-memory descriptors of the packed block (dim-major, two atoms).
+// S^T k-step ks (dims 16 ks .. +15) of A = keys x dims, MN-major: the two
+// 64-key atoms are the M halves (leading byte offset = the atom stride).
+__device__ __forceinline__ uint64_t desc_keys(uint32_t kv, int ks) {
+  return tc::desc_sw128(kv + ks * 2048, PK_ATOM, 1024);
+}
+// V^T rows dim0 .. dim0+127, k-step j (keys 16 j .. +15), K-major: the
+// source of the tensor-memory copies and the A operand of O^T tile 3.
+__device__ __forceinline__ uint64_t desc_vals(uint32_t kv, int dim0, int j) {
+  return tc::desc_sw128(kv + (j >> 2) * PK_ATOM + dim0 * 128 + (j & 3) * 32, 16, 1024);
+}
+// P^T k-step j (keys 16 j .. +15): rows of 64 query rows in the rope region
+// of each atom, MN-major.
+__device__ __forceinline__ uint64_t desc_p(uint32_t kv, int j) {
+  return tc::desc_sw128(kv + (j >> 2) * PK_ATOM + ROPE_ROW * 128 + (j & 3) * 2048, 8192, 1024);
+}
+
+// Copy group g of a packed block: dims 128 g .. +127 of both atoms (g < 4)
+// or the rope dims 512 .. 575 (g = 4).
+__device__ __forceinline__ void copy_group(uint32_t kv_smem, const uint8_t* src, int g, uint32_t mbar) {
+  const uint32_t row0 = 128u * g, bytes = (g < 4 ? 128u : 64u) * 128u;
+  // One expect for both atoms, then the two copies.
+  asm volatile(
+      "{\n.reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}\n" ::"r"(mbar), "r"(2 * bytes)
+      : "memory");
+#pragma unroll
+  for (int a = 0; a < 2; ++a) {
+    const uint32_t off = a * PK_ATOM + row0 * 128;
+    asm volatile(
+        "{\n.reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}\n"
+        ::"r"(kv_smem + off), "l"(src + off), "r"(bytes), "r"(mbar)
+        : "memory");
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) partial_tv_kernel(const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int split = blockIdx.x, rt = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3;       // TMEM lanes 32*quad .. +32 are this warp's
+  const int row0 = rt * BM;
+
+  float* s_red = reinterpret_cast<float*>(smem + OFF_RED);
+  float* s_mref = reinterpret_cast<float*>(smem + OFF_MREF);
+  float* s_l = reinterpret_cast<float*>(smem + OFF_L);
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + OFF_MASK);
+  int* s_tofr = reinterpret_cast<int*>(smem + OFF_TOFR);
+  int* s_par = reinterpret_cast<int*>(smem + OFF_PAR);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t kv = sbase + OFF_KV;
+  const uint32_t mbar0 = sbase + OFF_MBAR;
+  auto mbar = [&](int i) { return mbar0 + 8u * static_cast<uint32_t>(i); };
+
+  // Q tile: 64 rows x 9 swizzled chunks (rows beyond R zero), loaded by the
+  // softmax warps first -- its address needs nothing from the request, so
+  // the load overlaps the request lookup.  Every exit drains it.
+  if (warp < SOFTMAX_WARPS) {
+    const uint16_t* qb = p.q + static_cast<size_t>(b) * p.R * D_QK;
+#pragma unroll 1
+    for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
+      const int r = e / ROW_CHUNKS, q = e - r * ROW_CHUNKS;
+      const int gr = row0 + r;
+      const bool in = gr < p.R;
+      cp_async16(sbase + OFF_Q + (q >> 3) * Q_CHUNK + r * 128 + (((q & 7) ^ (r & 7)) << 4),
+                 in ? qb + static_cast<size_t>(gr) * D_QK + q * 8 : p.q, in ? 16 : 0);
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  }
+
+  const Request rq = load_request(p, b);
+  if (!rq.ok) {
+    if (split == 0 && rt == 0 && tid == 0)
+      atomicOr(p.err, (rq.n < p.T || rq.n > p.max_kv_len) ? ERR_LEN : ERR_INDPTR);
+    write_nan_rows(p, b, split, row0, tid);
+    if (tid == 0) finish_call(p);
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    return;
+  }
+  if (sbase & 1023) {   // swizzled operand tiles need a 1024-byte aligned base
+    if (tid == 0) {
+      atomicOr(p.err, ERR_INTERNAL);
+      finish_call(p);
+    }
+    write_nan_rows(p, b, split, row0, tid);
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    return;
+  }
+
+  int kb0, kb1;
+  split_blocks(rq, BN, split, p.nsplit, kb0, kb1);
+  const int nb = kb1 - kb0;
+
+  // Parents in one parallel load; the softmax warps walk the chains in
+  // shared memory.
+  if (tid < p.T) s_par[tid] = p.draft_parent[b * p.T + tid];
+  if (tid < BM) s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 1);
+    tc::mbar_init(mbar(MB_S), 1);
+    tc::mbar_init(mbar(MB_P), SOFTMAX_WARPS);
+    tc::mbar_init(mbar(MB_Q), SOFTMAX_WARPS);
+    tc::mbar_init(mbar(MB_DONE), 1);
+    tc::mbar_init(mbar(MB_SFREE), SOFTMAX_WARPS);
+    for (int i = 0; i < 4; ++i) tc::mbar_init(mbar(MB_OT + i), 1);
+    for (int i = 0; i < 3; ++i) tc::mbar_init(mbar(MB_VCP + i), 1);
+    tc::mbar_fence_init();
+    *s_abort = 0;
+  }
+  if (warp == MMA_WARP) tc::tmem_alloc<TMEM_COLS>(smem_u32(s_tmem));
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == COPY_WARP) {
+    // ======================= packed-block producer ==========================
+    // The whole warp runs the loop; one elected lane issues each copy.  A
+    // group of block k+1 goes into the shared memory its block-k
+    // counterpart leaves: dims 0..383 once that tile is in tensor memory,
+    // dims 384..511 once O^T(k) tile 3 has read them, the rope dims once
+    // O^T(k) has read P^T(k) from their place.
+    const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PK_BLOCK;
+    const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
+    if (!p.pack_flags) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    int issued = 0;   // groups issued, in (block, g) order
+#pragma unroll 1
+    for (int it = 0; it < nb; ++it) {
+      const uint8_t* src = blocks + static_cast<size_t>(kb0 + it) * PK_BLOCK;
+      const uint32_t prev = static_cast<uint32_t>((it - 1) & 1);
+      if (p.pack_flags && !wait_packed(p, b, kb0 + it, tag, s_abort, p.err)) break;
+      for (int g = 0; g < 5; ++g) {
+        if (it > 0) {
+          const int gate = g < 3 ? MB_VCP + g : (g == 3 ? MB_OT + 3 : MB_OT + 2);
+          wait_warp(mbar(gate), prev, s_abort, p.err);
+        }
+        if (*s_abort) break;
+        copy_group(kv, src, g, mbar(MB_CHUNK + g));
+        ++issued;
+      }
+      if (*s_abort) break;
+    }
+    // After an abort the last copy into each group may still be in flight:
+    // let it land before shared memory is reused or released.
+    if (*s_abort) {
+      for (int g = 0; g < 5 && g < issued; ++g)
+        wait_drain(mbar(MB_CHUNK + g), static_cast<uint32_t>(((issued - 1 - g) / 5) & 1), p.err);
+      __syncwarp();
+    }
+  } else if (warp == MMA_WARP) {
+    // ============================ MMA issuer ===============================
+    if (nb > 0) {
+      wait_warp(mbar(MB_Q), 0, s_abort, p.err);
+      tc::fence_after_sync();
+      // O^T(blk): tile 3 (A = dims 384..511 in shared memory) first, then
+      // tiles 0..2 (A = V^T in tensor memory); B = P^T.
+      auto o_products = [&](int blk) {
+        const uint32_t acc_first = blk > 0 ? 1u : 0u;
+        for (int j = 0; j < BN / 16; ++j)
+          tc::mma_ss(tmem + 3 * BM, desc_vals(kv, 384, j), desc_p(kv, j), IDESC_O, (acc_first || j > 0) ? 1u : 0u);
+        tc::commit(mbar(MB_OT + 3));
+        for (int d = 0; d < 3; ++d) {
+          for (int j = 0; j < BN / 16; ++j)
+            tc::mma_ts(tmem + d * BM, tmem + TM_V + 64 * d + 8 * j, desc_p(kv, j), IDESC_O,
+                       (acc_first || j > 0) ? 1u : 0u);
+          tc::commit(mbar(MB_OT + d));
+        }
+      };
+#pragma unroll 1
+      for (int it = 0; it < nb; ++it) {
+        const uint32_t par = static_cast<uint32_t>(it & 1), prev = static_cast<uint32_t>((it - 1) & 1);
+        // S^T(it) over dims 0..383, once the softmax of it-1 holds its scores.
+        if (it > 0) wait_warp(mbar(MB_SFREE), prev, s_abort, p.err);
+        for (int g = 0; g < 3; ++g) {
+          wait_warp(mbar(MB_CHUNK + g), par, s_abort, p.err);
+          tc::fence_after_sync();
+          for (int ks = 8 * g; ks < 8 * g + 8; ++ks)
+            tc::mma_ss(tmem + TM_S, desc_keys(kv, ks),
+                       tc::desc_sw128(sbase + OFF_Q + (ks >> 2) * Q_CHUNK + (ks & 3) * 32, 16, 1024),
+                       IDESC_S, ks > 0);
+        }
+        if (it > 0) {
+          wait_warp(mbar(MB_P), prev, s_abort, p.err);
+          tc::fence_after_sync();
+          o_products(it - 1);
+        }
+        // V^T(it) tiles 0..2 into tensor memory, each once O^T(it-1) has read
+        // the tile it replaces.
+        for (int d = 0; d < 3; ++d) {
+          if (it > 0) {
+            wait_warp(mbar(MB_OT + d), prev, s_abort, p.err);
+            tc::fence_after_sync();
+          }
+          for (int j = 0; j < BN / 16; ++j)
+            tc::cp_128x256b(tmem + TM_V + 64 * d + 8 * j, desc_vals(kv, 128 * d, j));
+          tc::commit(mbar(MB_VCP + d));
+        }
+        // S^T(it) over dims 384..575.
+        for (int g = 3; g < 5; ++g) {
+          wait_warp(mbar(MB_CHUNK + g), par, s_abort, p.err);
+          tc::fence_after_sync();
+          const int k1 = g == 3 ? 32 : 36;
+          for (int ks = 8 * g; ks < k1; ++ks)
+            tc::mma_ss(tmem + TM_S, desc_keys(kv, ks),
+                       tc::desc_sw128(sbase + OFF_Q + (ks >> 2) * Q_CHUNK + (ks & 3) * 32, 16, 1024),
+                       IDESC_S, 1u);
+        }
+        tc::commit(mbar(MB_S));
+      }
+      wait_warp(mbar(MB_P), static_cast<uint32_t>((nb - 1) & 1), s_abort, p.err);
+      tc::fence_after_sync();
+      o_products(nb - 1);
+      // After an abort the waits above returned early: let every tcgen05 op
+      // this CTA issued finish before TMEM is freed.
+      if (__any_sync(0xffffffffu, *s_abort != 0)) {
+        tc::commit(mbar(MB_DONE));
+        wait_drain(mbar(MB_DONE), 0, p.err);
+      }
+    }
+  } else {
+    // ============================= softmax =================================
+    if (nb > 0) {
+      if (tid < p.T) s_mask[tid] = ancestor_mask(s_par, tid, p.err);
+      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+      named_sync(1, SOFTMAX_WARPS * 32);
+      bool bad = false;
+#pragma unroll 1
+      for (int e = tid; e < BM * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
+        uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_Q + e * 16);
+        *ptr = widen_bf16x8(*ptr, bad);
+      }
+      report_range(bad, p.err);
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(mbar(MB_Q));
+    } else {
+      asm volatile("cp.async.wait_all;\n" ::: "memory");   // no key block: Q unused
+    }
+    const int j = quad * 32 + lane;     // key of this thread = TMEM lane
+    const int hc = warp >> 2;           // query-row columns hc*32 .. +32
+    const int c0 = hc * HALF;
+    const bool all_rows = row0 + BM <= p.R;
+    const float scale2 = p.scale_log2;
+    float mrow = -INFINITY;             // running max (base 2) of row c0 + lane
+    float* w_m = reinterpret_cast<float*>(smem + OFF_WARP) + warp * 64;   // [32] row max, fully masked -> 0
+    float* w_a = w_m + 32;                                                // [32] rescale factor
+    float lpart[HALF];                  // this key's share of its rows' sums
+#pragma unroll
+    for (int c = 0; c < HALF; ++c) lpart[c] = 0.f;
+    // This key's P^T row (64 query rows, 128 bytes) in the rope region of its atom.
+    uint8_t* prow = smem + OFF_KV + (j >> 6) * PK_ATOM + (ROPE_ROW + (j & 63)) * 128;
+    bool next_ok = nb > 0 ? block_key_ok(p, rq, kb0, j) : false;
+#pragma unroll 1
+    for (int it = 0; it < nb; ++it) {
+      const int kb = kb0 + it;
+      const uint32_t par = static_cast<uint32_t>(it & 1);
+      const bool key_ok = next_ok;
+      if (it + 1 < nb) next_ok = block_key_ok(p, rq, kb + 1, j);
+      const int jg = kb * BN + j;
+      wait_warp(mbar(MB_S), par, s_abort, p.err);
+      tc::fence_after_sync();
+      uint32_t sr[HALF];
+      tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + TM_S + c0, sr);
+      tc::tmem_wait_ld();
+      // The scores are in registers: the next block's S^T may overwrite them.
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(mbar(MB_SFREE));
+      float* s = reinterpret_cast<float*>(sr);   // scores overwrite the raw bits in place
+      if (!key_ok) {
+#pragma unroll
+        for (int c = 0; c < HALF; ++c) s[c] = -INFINITY;
+      } else if (jg < rq.P && all_rows) {
+#pragma unroll
+        for (int c = 0; c < HALF; ++c) s[c] = __uint_as_float(sr[c]) * scale2;
+      } else {
+        const int di = jg - rq.P;   // draft index when >= 0
+#pragma unroll
+        for (int c = 0; c < HALF; ++c) {
+          const int t = s_tofr[c0 + c];
+          bool vis = t >= 0;
+          if (vis && di >= 0) vis = (s_mask[t] >> di) & 1u;
+          s[c] = vis ? __uint_as_float(sr[c]) * scale2 : -INFINITY;
+        }
+      }
+      // Column (query row) max: over this warp's 32 keys (lane l ends with
+      // column c0 + l), then over the four quads.
+      {
+        float v[HALF];
+#pragma unroll
+        for (int c = 0; c < HALF; ++c) v[c] = s[c];
+        transpose_max32(v, lane);
+        s_red[(c0 + lane) * 4 + quad] = v[0];
+      }
+      named_sync(1, 256);
+      bool moved;
+      {
+        const float4 q4 = *reinterpret_cast<const float4*>(s_red + (c0 + lane) * 4);
+        const float bm = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
+        float alpha = 1.f;
+        if (bm > mrow) {
+          if (mrow != -INFINITY) alpha = ex2(mrow - bm);
+          mrow = bm;
+        }
+        moved = __any_sync(0xffffffffu, alpha != 1.f);
+        w_m[lane] = mrow == -INFINITY ? 0.f : mrow;   // a fully masked row: every p = ex2(-inf) = 0
+        w_a[lane] = alpha;
+        __syncwarp();
+      }
+      // This key's P^T entries for the half's 32 query rows as fp16 (four
+      // 16-byte granules of its 128-byte swizzled row).
+      uint32_t pk[HALF / 2];
+      if (moved) {
+#pragma unroll
+        for (int c = 0; c < HALF; c += 2) {
+          const float2 m = *reinterpret_cast<const float2*>(w_m + c);
+          const float2 al = *reinterpret_cast<const float2*>(w_a + c);
+          const float p0 = ex2(s[c] - m.x), p1 = ex2(s[c + 1] - m.y);
+          lpart[c] = lpart[c] * al.x + p0;
+          lpart[c + 1] = lpart[c + 1] * al.y + p1;
+          __half2 h = __floats2half2_rn(p0, p1);
+          pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < HALF; c += 2) {
+          const float2 m = *reinterpret_cast<const float2*>(w_m + c);
+          const float p0 = ex2(s[c] - m.x), p1 = ex2(s[c + 1] - m.y);
+          lpart[c] += p0;
+          lpart[c + 1] += p1;
+          __half2 h = __floats2half2_rn(p0, p1);
+          pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int gg = hc * 4 + g;
+        *reinterpret_cast<uint4*>(prow + ((gg ^ (j & 7)) << 4)) =
+            make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+      }
+      // Rescale this half's O^T columns if any of its rows' max moved
+      // (O^T(k-1) is complete: the S^T(k) commit came after it).
+      if (moved) {
+#pragma unroll 1
+        for (int d = 0; d < 4; d += 2) {
+          const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + c0;
+          uint32_t v0[HALF], v1[HALF];
+          tc::tmem_ld32(ta, v0);
+          tc::tmem_ld32(ta + BM, v1);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < HALF; ++c) {
+            const float al = w_a[c];
+            v0[c] = __float_as_uint(__uint_as_float(v0[c]) * al);
+            v1[c] = __float_as_uint(__uint_as_float(v1[c]) * al);
+          }
+          tc::tmem_st32(ta, v0);
+          tc::tmem_st32(ta + BM, v1);
+        }
+        tc::tmem_wait_st();
+      }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(mbar(MB_P));
+    }
+    if (nb > 0) {
+      // O^T(nb-1) done: tile 2 is the last one issued.
+      wait_warp(mbar(MB_OT + 2), static_cast<uint32_t>((nb - 1) & 1), s_abort, p.err);
+      tc::fence_after_sync();
+    }
+    if (quad == 0) s_mref[c0 + lane] = mrow;
+    // Row sums over all keys: this warp's 32 keys, then 4 quads.
+#pragma unroll
+    for (int c = 0; c < HALF; ++c) {
+      float v = lpart[c];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (c == lane) s_red[quad * BM + c0 + c] = v;
+    }
+    named_sync(1, 256);
+    if (tid < BM) {
+      const float l = s_red[tid] + s_red[BM + tid] + s_red[2 * BM + tid] + s_red[3 * BM + tid];
+      s_l[tid] = l > 0.f ? 1.f / l : 0.f;
+      const int gr = row0 + tid;
+      if (gr < p.R) {
+        const float lse = l > 0.f ? (s_mref[tid] + log2f(l)) * kLn2 : -INFINITY;
+        if (p.nsplit == 1) p.lse[static_cast<size_t>(b) * p.R + gr] = lse;
+        else p.ws_lse[ws_base(p, b, split) + gr] = lse;
+      }
+    }
+  }
+
+  // ---- normalised O out of TMEM (thread = value dim), staged row-major in
+  // the idle key-block buffer, then one bulk store per row.
+  tc::fence_before_sync();
+  __syncthreads();
+  // The combine may be scheduled now; it waits for this grid to complete.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  tc::fence_after_sync();
+  if (*s_abort != 0) {
+    write_nan_rows(p, b, split, row0, tid);
+  } else {
+    const int nrows = min(BM, p.R - row0);
+    const bool out16 = p.nsplit == 1 && p.out_bf16;
+    uint8_t* stage = smem + OFF_KV;            // [64 rows][512 dims] fp32 or bf16
+    if (warp < SOFTMAX_WARPS) {
+      const int h = warp >> 2;
+#pragma unroll 1
+      for (int d = 0; d < 4; d += 2) {
+        uint32_t v0[32], v1[32];
+        if (nb > 0) {
+          const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + h * 32;
+          tc::tmem_ld32(ta, v0);
+          tc::tmem_ld32(ta + BM, v1);
+          tc::tmem_wait_ld();
+        }
+        const int dim0 = d * 128 + quad * 32 + lane, dim1 = dim0 + 128;
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 inv4 = *reinterpret_cast<const float4*>(s_l + h * 32 + c);
+          const float inv[4] = {inv4.x, inv4.y, inv4.z, inv4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = h * 32 + c + e;
+            const bool ok = inv[e] > 0.f && nb > 0;
+            const float o0 = ok ? __uint_as_float(v0[c + e]) * inv[e] : 0.f;
+            const float o1 = ok ? __uint_as_float(v1[c + e]) * inv[e] : 0.f;
+            if (out16) {
+              reinterpret_cast<__nv_bfloat16*>(stage)[r * D_V + dim0] = __float2bfloat16_rn(o0);
+              reinterpret_cast<__nv_bfloat16*>(stage)[r * D_V + dim1] = __float2bfloat16_rn(o1);
+            } else {
+              reinterpret_cast<float*>(stage)[r * D_V + dim0] = o0;
+              reinterpret_cast<float*>(stage)[r * D_V + dim1] = o1;
+            }
+          }
+        }
+      }
+      tc::fence_async_smem();
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t row_bytes = out16 ? D_V * 2 : D_V * 4;
+      for (int r = lane; r < nrows; r += 32) {
+        const size_t grow = static_cast<size_t>(b) * p.R + row0 + r;
+        void* dst = p.nsplit == 1
+                        ? static_cast<void*>(static_cast<uint8_t*>(p.out) + grow * row_bytes)
+                        : static_cast<void*>(p.ws_o + (ws_base(p, b, split) + row0 + r) * D_V);
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
+                     "r"(sbase + OFF_KV + r * row_bytes), "r"(row_bytes)
+                     : "memory");
+      }
+      asm volatile("cp.async.bulk.commit_group;\ncp.async.bulk.wait_group 0;\n" ::: "memory");
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == MMA_WARP) tc::tmem_dealloc<TMEM_COLS>(tmem);
+  if (tid == 0) finish_call(p);
+}
+
+}  // namespace
+
+cudaError_t partial_tv_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(partial_tv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(partial_tv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
+cudaError_t launch_partial_tv(const Params& p, cudaStream_t stream, bool overlap) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nsplit, (p.R + BM - 1) / BM, p.batch);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, partial_tv_kernel, p);
+}
+
+}  // namespace mlav

@@ -46,6 +46,28 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// Same MMA with the A operand in tensor memory (lanes = M rows, K packed
+// two 16-bit values per 32-bit column): D (+)= A[a_tmem] . B[b].
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\n.reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// Copy 128 rows x 32 bytes from shared memory (descriptor `src`, K-major:
+// one row per TMEM lane) into 8 consecutive TMEM columns at `taddr`.  Runs
+// on the tensor pipe in issue order with the MMAs of the issuing thread.
+__device__ __forceinline__ void cp_128x256b(uint32_t taddr, uint64_t src) {
+  asm volatile(
+      "{\n.reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n}\n" ::"r"(taddr), "l"(src));
+}
+
 // Arrive once on the mbarrier when every MMA the elected lane issued so far
 // is done.
 __device__ __forceinline__ void commit(uint32_t mbar) {
