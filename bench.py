@@ -76,7 +76,7 @@ def load_peaks():
 def kernel_source_hash():
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "paged_mla_speculative_gb300", "csrc")
-    for name in ("common.cuh", "tc_ptx.cuh", "partial_tv.cu"):
+    for name in ("common.cuh", "tc_ptx.cuh", "partial_tc.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -91,7 +91,7 @@ def profiled_traffic(workload):
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d.get("partial_tv_kernel", {})
+        e = d.get("partial_tc_kernel", {})
         if e.get("source_sha1") == kernel_source_hash() and e.get("workload") == workload:
             return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -137,9 +137,8 @@ def compaction_timing(mb, plan, inp, w, flush, stream, steps):
             "frac_of_hbm": gbs / hbm, "bound": "hbm", "launches": 2}
 
 
-PACK_NAMES = {1: "whole", 2: "idle_sms", 3: "resident", 4: "none"}
-PACK_KERNELS = {"whole": "pack_kv_kernel", "idle_sms": "pack_kv_overlap_kernel",
-                "resident": "pack_kv_resident_kernel"}
+PACK_NAMES = {1: "whole", 2: "idle_sms", 4: "none"}
+PACK_KERNELS = {"whole": "pack_kv_kernel", "idle_sms": "pack_kv_overlap_kernel"}
 
 
 def kernels_of(kernel, ns, schedule="whole"):
@@ -147,7 +146,7 @@ def kernels_of(kernel, ns, schedule="whole"):
     the key-pack schedule, "none" when the attention CTAs gather their own
     keys)."""
     from paged_mla_speculative_gb300 import binding as mb
-    tc = ["partial_tc_kernel"] if schedule == "none" else [PACK_KERNELS[schedule], "partial_tv_kernel"]
+    tc = ["partial_tc_kernel"] if schedule == "none" else [PACK_KERNELS[schedule], "partial_tc_kernel"]
     names = {mb.KERNEL_TC: tc, mb.KERNEL_MMA: ["partial_mma_kernel"]}[kernel]
     return " + ".join(names + (["combine_kernel"] if ns > 1 else []))
 
@@ -595,7 +594,7 @@ def run_gb300(args):
             "partial_us", "combine_us")}},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak, "traffic": profiled_traffic(head),
-                     "kernel": "partial_tv_kernel", "workload": head,
+                     "kernel": "partial_tc_kernel", "workload": head,
                      "peak_source": f"{st['peak_src']} bf16 burst (fp16 has the same tensor rate)"},
         "clocks": clk.summary(), "gpu_launches": launches,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,

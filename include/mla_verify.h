@@ -156,12 +156,9 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* plan, int batch, in
  * Key-pack schedule of the TC family, for tuning and tests (the automatic
  * choice otherwise).  WHOLE: the whole pack runs first.  IDLE_SMS: the
  * two-phase pack above on the SMs the attention grid leaves idle (WHOLE when
- * it leaves none).  RESIDENT: one small pack CTA per SM runs beside the
- * attention CTAs for the whole call, publishing each block as it is packed,
- * so the pack overlaps the attention kernel even when the attention grid
- * fills every SM (mla_verify_plan_get_pack_schedule then reports *wide = 0,
- * *stay = the SM count).  Calls with profiling events always pack WHOLE;
- * calls with one row tile per request never pack.  MLA_VERIFY_ERR_ARG for an
+ * it leaves none).  NONE: no pack -- every attention CTA gathers its own key
+ * blocks from the cache (the automatic choice with one row tile per
+ * request).  Calls with profiling events pack WHOLE unless NONE applies.  MLA_VERIFY_ERR_ARG for an
  * unknown schedule.  mla_verify_plan_get_pack_mode returns the schedule a
  * call with `batch` requests uses (MLA_VERIFY_PACK_NONE when it packs
  * nothing), or < 0.
@@ -169,7 +166,6 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* plan, int batch, in
 #define MLA_VERIFY_PACK_AUTO          0
 #define MLA_VERIFY_PACK_WHOLE         1
 #define MLA_VERIFY_PACK_IDLE_SMS      2
-#define MLA_VERIFY_PACK_RESIDENT      3
 #define MLA_VERIFY_PACK_NONE          4
 int mla_verify_plan_set_pack_schedule(mla_verify_plan* plan, int schedule);
 int mla_verify_plan_get_pack_mode(const mla_verify_plan* plan, int batch);

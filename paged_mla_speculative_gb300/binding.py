@@ -25,7 +25,6 @@ KERNEL_TC = 2
 PACK_AUTO = 0
 PACK_WHOLE = 1
 PACK_IDLE_SMS = 2
-PACK_RESIDENT = 3
 PACK_NONE = 4
 FAULT_NONE = 0
 FAULT_SKIP_PACK = 1
@@ -185,7 +184,7 @@ class Plan:
         return wide.value, stay.value
 
     def set_pack_schedule(self, schedule: int):
-        """Force a key-pack schedule (PACK_WHOLE / PACK_IDLE_SMS / PACK_RESIDENT)
+        """Force a key-pack schedule (PACK_WHOLE / PACK_IDLE_SMS / PACK_NONE)
         or PACK_AUTO."""
         _check(load_library().mla_verify_plan_set_pack_schedule(self.handle, schedule),
                "set_pack_schedule")

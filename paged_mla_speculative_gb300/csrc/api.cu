@@ -82,7 +82,7 @@ constexpr long long kDirectMaxTiles = 1;   // 2 tiles measured slower (each bloc
 // its first block.  When that needs more than half the positions, or
 // otherwise, the whole pack runs first (stay = 0).
 struct PackSchedule {
-  int mode;       // MLA_VERIFY_PACK_WHOLE, _IDLE_SMS or _RESIDENT
+  int mode;       // MLA_VERIFY_PACK_WHOLE or _IDLE_SMS
   int wide, stay;
 };
 constexpr int kMinPackSms = 16;
@@ -92,7 +92,6 @@ PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool ov
   const long long idle = pl->num_sms - attn;
   const PackSchedule whole{MLA_VERIFY_PACK_WHOLE, positions, 0};
   if (!overlap || pl->pack_mode == MLA_VERIFY_PACK_WHOLE) return whole;
-  if (pl->pack_mode == MLA_VERIFY_PACK_RESIDENT) return PackSchedule{MLA_VERIFY_PACK_RESIDENT, 0, pl->num_sms};
   const bool forced_idle = pl->pack_mode == MLA_VERIFY_PACK_IDLE_SMS;
   if (idle < (forced_idle ? 1 : kMinPackSms)) return whole;
   const double per_block_us = 3.4, lead_us = 5.0, blocks_per_us_per_sm = 0.15;
@@ -112,12 +111,18 @@ PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, boo
   return pack_plan(pl, p.batch, p.nsplit, overlap, p.num_shards);
 }
 
+// The attention CTAs gather their own key blocks (no pack): one row tile per
+// request, or forced.
+bool gathers_directly(const mla_verify_plan* pl) {
+  return pl->pack_mode == MLA_VERIFY_PACK_NONE || ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles;
+}
+
 // What the pack leaves on a call's critical path, in attention block steps
 // (~3.4 us): the wide phase (~9 us) when it overlaps, else the whole gather
 // of up to batch x max_kv_len rows (1152 B read + 1152 B written each at
 // ~4.5 TB/s, plus ~3 us); nothing when the attention CTAs gather directly.
 double pack_steps(const mla_verify_plan* pl, int batch, int nsplit, int shards) {
-  if (ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles) return 0.0;
+  if (gathers_directly(pl)) return 0.0;
   const PackSchedule ps = pack_plan(pl, batch, nsplit, true, shards);
   if (ps.mode != MLA_VERIFY_PACK_WHOLE) return 9.0 / 3.4;
   return (2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0) / 3.4;
@@ -238,7 +243,7 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
   if (mlav::partial_mma_prepare() != cudaSuccess || mlav::partial_tc_prepare() != cudaSuccess ||
-      mlav::partial_tv_prepare() != cudaSuccess || mlav::pack_kv_prepare() != cudaSuccess)
+      mlav::pack_kv_prepare() != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
 
   mla_verify_plan* pl = new (std::nothrow) mla_verify_plan();
@@ -342,8 +347,7 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int*
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
   *wide = 0;
   *stay = 0;
-  if (pl->kernel != MLA_VERIFY_KERNEL_TC || ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles)
-    return MLA_VERIFY_OK;
+  if (pl->kernel != MLA_VERIFY_KERNEL_TC || gathers_directly(pl)) return MLA_VERIFY_OK;
   mlav::Params p{};
   p.batch = batch;
   p.R = pl->R;
@@ -358,7 +362,7 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int*
 int mla_verify_plan_set_pack_schedule(mla_verify_plan* pl, int schedule) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (schedule != MLA_VERIFY_PACK_AUTO && schedule != MLA_VERIFY_PACK_WHOLE &&
-      schedule != MLA_VERIFY_PACK_IDLE_SMS && schedule != MLA_VERIFY_PACK_RESIDENT)
+      schedule != MLA_VERIFY_PACK_IDLE_SMS && schedule != MLA_VERIFY_PACK_NONE)
     return MLA_VERIFY_ERR_ARG;
   pl->pack_mode = schedule;
   return MLA_VERIFY_OK;
@@ -367,8 +371,7 @@ int mla_verify_plan_set_pack_schedule(mla_verify_plan* pl, int schedule) {
 int mla_verify_plan_get_pack_mode(const mla_verify_plan* pl, int batch) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
-  if (pl->kernel != MLA_VERIFY_KERNEL_TC || ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles)
-    return MLA_VERIFY_PACK_NONE;
+  if (pl->kernel != MLA_VERIFY_KERNEL_TC || gathers_directly(pl)) return MLA_VERIFY_PACK_NONE;
   return pack_plan(pl, batch, effective_nsplit(pl, batch), true).mode;
 }
 
@@ -473,8 +476,7 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
   // One row tile per request: each key block is read by one attention CTA,
   // which gathers it itself instead of going through the pack (which writes
   // every block and reads it back).
-  const bool direct = pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack &&
-                      ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles;
+  const bool direct = pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack && gathers_directly(pl);
   bool attn_overlap = overlap;
   if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && skip_pack) {
     p.pack_flags = 1;   // injected: nothing sets the flags the attention kernel waits for
@@ -484,9 +486,7 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
   } else if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC) {
     const PackSchedule ps = pack_schedule(pl, p, overlap);
     p.pack_flags = ps.mode != MLA_VERIFY_PACK_WHOLE;
-    le = ps.mode == MLA_VERIFY_PACK_RESIDENT
-             ? mlav::launch_pack_kv_resident(p, pl->packed, pl->pack_blocks, pl->num_sms, s)
-         : ps.mode == MLA_VERIFY_PACK_IDLE_SMS
+    le = ps.mode == MLA_VERIFY_PACK_IDLE_SMS
              ? mlav::launch_pack_kv_overlap(p, pl->packed, pl->pack_blocks, pl->num_sms, ps.wide, ps.stay, s)
              : mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
   }
@@ -494,8 +494,7 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)
     le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
-         : direct                            ? mlav::launch_partial_tc(p, s, attn_overlap)
-                                             : mlav::launch_partial_tv(p, s, attn_overlap);
+                                             : mlav::launch_partial_tc(p, s, attn_overlap);
   if (packed && le != cudaSuccess) pl->pack_flags_dirty = true;   // the epoch did not advance
   if (le == cudaSuccess && pl->ev_after_partial) le = cudaEventRecord(pl->ev_after_partial, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;

@@ -163,46 +163,6 @@ __device__ __forceinline__ uint4 widen_bf16x8(uint4 v, bool& bad) {
   return make_uint4(widen_bf16x2(v.x, bad), widen_bf16x2(v.y, bad), widen_bf16x2(v.z, bad),
                     widen_bf16x2(v.w, bad));
 }
-// Transpose of an 8 x 8 tile of 16-bit values held by the 8 lanes whose ids
-// differ only in bits 0..2 (all 32 lanes call it; the four groups of 8 each
-// transpose their own tile): on entry lane r holds row r (word w = columns
-// 2w, 2w+1, low half first), on return column r.  Three butterfly stages
-// exchange half of the remaining data with the lane 4, 2, then 1 apart.
-__device__ __forceinline__ uint4 transpose8x8_b16(uint4 v, int lane) {
-  const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
-  uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w;
-  // lanes r, r^4: the low lane keeps columns 0-3 of both rows, the high one 4-7
-  const uint32_t t0 = __shfl_xor_sync(0xffffffffu, b2 ? w0 : w2, 4);
-  const uint32_t t1 = __shfl_xor_sync(0xffffffffu, b2 ? w1 : w3, 4);
-  if (b2) { w0 = t0; w1 = t1; } else { w2 = t0; w3 = t1; }
-  // lanes r, r^2: one column pair of four rows each
-  const uint32_t p0 = __shfl_xor_sync(0xffffffffu, b1 ? w0 : w1, 2);
-  const uint32_t p1 = __shfl_xor_sync(0xffffffffu, b1 ? w2 : w3, 2);
-  if (b1) { w0 = p0; w2 = p1; } else { w1 = p0; w3 = p1; }
-  // lanes r, r^1: keep the half of column r, send the other half
-  const uint32_t s0 = b0 ? __byte_perm(w0, w1, 0x5410) : __byte_perm(w0, w1, 0x7632);
-  const uint32_t s1 = b0 ? __byte_perm(w2, w3, 0x5410) : __byte_perm(w2, w3, 0x7632);
-  const uint32_t r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
-  const uint32_t r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
-  if (b0)
-    return make_uint4(__byte_perm(r0, w0, 0x7610), __byte_perm(r0, w1, 0x7632), __byte_perm(r1, w2, 0x7610),
-                      __byte_perm(r1, w3, 0x7632));
-  return make_uint4(__byte_perm(w0, r0, 0x5410), __byte_perm(w1, r0, 0x7610), __byte_perm(w2, r1, 0x5410),
-                    __byte_perm(w3, r1, 0x7610));
-}
-
-// Packed key block, dim-major: 128 keys x 576 dims fp16 in two 72 KB atoms
-// (keys 0-63, 64-127), each 576 rows (one per dim) of 128 bytes holding the
-// atom's 64 keys, the 16-byte granule of keys 8k..8k+7 stored at granule
-// position k ^ (dim & 7) -- the 128-byte swizzle, read as an MN-major
-// operand (keys on M) by the score MMAs and as a K-major one (keys on K) by
-// the value copies into tensor memory.
-constexpr int PK_ATOM = 576 * 128;             // bytes per 64-key atom
-constexpr int PK_BLOCK = 2 * PK_ATOM;          // bytes per 128-key block
-__device__ __forceinline__ uint32_t pk_offset(int dim, int key_granule /*0..15*/) {
-  return static_cast<uint32_t>((key_granule >> 3) * PK_ATOM + dim * 128 + (((key_granule & 7) ^ (dim & 7)) << 4));
-}
-
 // One atomic per warp for a per-thread range flag (all lanes must call).
 __device__ __forceinline__ void report_range(bool bad, int* err) {
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(err, ERR_RANGE);

@@ -12,9 +12,7 @@ int partial_mma_smem_bytes();
 cudaError_t partial_mma_prepare();
 cudaError_t launch_partial_mma(const Params& p, cudaStream_t stream);
 
-// Split-KV partial kernel on tcgen05 tensor cores with TMEM accumulators,
-// for one row tile per request: its CTAs gather their key rows themselves
-// (Params::direct_all = 1).
+// Split-KV partial kernel on tcgen05 tensor cores with TMEM accumulators.
 cudaError_t partial_tc_prepare();
 // `overlap`: launch with programmatic stream serialisation, so the kernel's
 // CTAs may start while the previous kernel on the stream (the pack) runs;
@@ -22,12 +20,6 @@ cudaError_t partial_tc_prepare();
 // call's tag (Params::pack_flags = 1), or after griddepcontrol.wait, which
 // waits for the whole pack grid (pack_flags = 0).
 cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap);
-
-// Split-KV partial kernel over packed (dim-major) key blocks with the value
-// tiles copied into tensor memory: the TC family's kernel whenever a pack
-// runs.  Same `overlap` semantics as launch_partial_tc.
-cudaError_t partial_tv_prepare();
-cudaError_t launch_partial_tv(const Params& p, cudaStream_t stream, bool overlap);
 
 // Per-call gather of the key rows into packed fp16 operand tiles.
 size_t packed_block_bytes();
@@ -40,11 +32,6 @@ cudaError_t launch_pack_kv(const Params& p, void* packed, int max_blocks, cudaSt
 cudaError_t pack_kv_prepare();
 cudaError_t launch_pack_kv_overlap(const Params& p, void* packed, int max_blocks, int num_ctas,
                                    int wide_positions, int stay, cudaStream_t stream);
-
-// The pack as one small CTA per SM (num_ctas = the SM count) running
-// beside the attention CTAs for the whole call (pack_flags = 1).
-cudaError_t launch_pack_kv_resident(const Params& p, void* packed, int max_blocks, int num_ctas,
-                                    cudaStream_t stream);
 
 // LSE combine of the split partials into out/lse (`overlap`: may be
 // scheduled early; it waits for the partial kernel with griddepcontrol.wait).

@@ -11,18 +11,11 @@
 // kernel then streams each block with plain bulk copies.
 //
 // Layout: block kb of request b occupies 147456 contiguous bytes at
-// packed + (b * max_blocks + kb) * 147456, dim-major (common.cuh: PK_*):
-// two 72 KB atoms of 64 keys, each 576 rows of 128 bytes (one row per dim,
-// the atom's 64 keys), 16-byte granules of 8 keys permuted by XOR with
-// (dim & 7) -- the 128-byte swizzle.  Keys past the end of the call's range,
-// or whose slot lies outside the cache (reported), are zero.
-//
-// Work unit: 8 consecutive keys x one half of the 576 dims (36 of the 72
-// 16-byte granules of each row).  Lane (r, s) = (lane & 7, lane >> 3) loads
-// granules s, s+4, .. of the half of key r (nine 16-byte loads in flight),
-// widens them to fp16, and the 8 lanes of each s transpose their 8 x 8
-// tiles (keys x dims) so that lane r ends with dim 8g + r of the 8 keys --
-// one granule of the dim-major layout.
+// packed + (b * max_blocks + kb) * 147456: nine 16 KB chunk tiles (dims
+// 64c .. 64c+63), each [128 keys][128 bytes] with the 16-byte granules of
+// key j permuted by XOR with (j & 7) -- the 128-byte-swizzled operand tile
+// tcgen05 reads.  Keys past the end of the request, or whose slot lies
+// outside the cache (reported), are zero.
 //
 // Two kernels, same layout:
 //  * pack_kv_kernel: one 256-thread CTA per quarter block (every thread has
@@ -53,10 +46,7 @@ namespace {
 constexpr int BN = 128;
 constexpr int NTHREADS = 256;           // pack_kv_kernel
 constexpr int OV_THREADS = 1024;        // pack_kv_overlap_kernel
-constexpr int BLOCK_BYTES = PK_BLOCK;
-constexpr int HALF_GRANULES = ROW_CHUNKS / 2;   // 36 granules per dim half
-constexpr int PER_LANE = HALF_GRANULES / 4;     // 9 granules per lane
-static_assert(PER_LANE * 4 * 2 == ROW_CHUNKS, "four lanes per key and dim half");
+constexpr int BLOCK_BYTES = 9 * BN * 128;
 
 // The key rows are read exactly once per call: load them past L1 and mark
 // them first to leave L2, so the packed blocks the attention kernel reads
@@ -76,37 +66,9 @@ __device__ __forceinline__ uint4 load_row_granule(const uint4* src, uint64_t pol
 
 constexpr int QUARTER = BN / 4;   // keys per CTA of pack_kv_kernel
 
-// Loads the nine granules of lane (r, s) for key slot `slot` and dim half h
-// (zeros when slot < 0).
-__device__ __forceinline__ void load_half(const Params& p, int slot, int h, int lane, uint4 (&v)[PER_LANE]) {
-#pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) v[i] = make_uint4(0, 0, 0, 0);
-  if (slot >= 0) {   // streamed once
-    const uint4* src = reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(slot) * D_QK) +
-                       HALF_GRANULES * h + (lane >> 3);
-    const uint64_t pol = evict_first_policy();
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) v[i] = load_row_granule(src + 4 * i, pol);
-  }
-}
-
-// Widen, transpose and store the unit (8 keys from key 8 * octet of the
-// block, dim half h).  All 32 lanes of the warp take part.
-__device__ __forceinline__ void store_half(uint8_t* block, int octet, int h, int lane,
-                                           const uint4 (&v)[PER_LANE], bool& bad) {
-  const int r = lane & 7;
-#pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) {
-    const int g = HALF_GRANULES * h + (lane >> 3) + 4 * i;   // dims 8g .. 8g+7
-    const uint4 t = transpose8x8_b16(widen_bf16x8(v[i], bad), lane);
-    *reinterpret_cast<uint4*>(block + pk_offset(8 * g + r, octet)) = t;
-  }
-}
-
-// One CTA packs a quarter block (32 keys): warp w takes keys 8 (w & 3) .. +7
-// of the quarter and dim half w >> 2, every lane with its nine 16-byte loads
-// in flight at once; several CTAs per SM keep enough bytes in flight to
-// cover DRAM latency.
+// One CTA packs a quarter block (32 keys x 72 granules): every thread has
+// its nine 16-byte loads in flight at once, and several CTAs per SM keep
+// enough bytes in flight to cover DRAM latency.
 __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8_t* packed,
                                                            int max_blocks) {
   __shared__ int s_slot[QUARTER];
@@ -128,17 +90,33 @@ __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8
     s_slot[tid] = static_cast<int>(s);
   }
   __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31;
-  const int octet = quarter * 4 + (warp & 3), h = warp >> 2;
-  uint4 v[PER_LANE];
-  load_half(p, s_slot[(warp & 3) * 8 + (lane & 7)], h, lane, v);
+  uint8_t* dst = packed + (static_cast<size_t>(b) * max_blocks + kb) * BLOCK_BYTES;
+  constexpr int PER_THREAD = QUARTER * ROW_CHUNKS / NTHREADS;   // 9
+  static_assert(QUARTER * ROW_CHUNKS == PER_THREAD * NTHREADS, "even split");
+  const uint64_t pol = evict_first_policy();
+  uint4 v[PER_THREAD];
+  int off[PER_THREAD];
+#pragma unroll
+  for (int u = 0; u < PER_THREAD; ++u) {
+    const int e = tid + u * NTHREADS;
+    const int jl = e / ROW_CHUNKS, q = e - jl * ROW_CHUNKS;
+    const int j = key0 + jl;                // key within the block
+    const int slot = s_slot[jl];
+    off[u] = (q >> 3) * (BN * 128) + j * 128 + (((q & 7) ^ (j & 7)) << 4);
+    v[u] = slot >= 0 ? load_row_granule(reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(slot) * D_QK) + q, pol)
+                     : make_uint4(0, 0, 0, 0);
+  }
   bool bad = false;
-  store_half(packed + (static_cast<size_t>(b) * max_blocks + kb) * BLOCK_BYTES, octet, h, lane, v, bad);
+#pragma unroll
+  for (int u = 0; u < PER_THREAD; ++u) *reinterpret_cast<uint4*>(dst + off[u]) = widen_bf16x8(v[u], bad);
   report_range(bad, p.err);
 }
 
-constexpr int UNITS_PER_BLOCK = 32;   // (key octet, dim half) units: one ready flag each
-static_assert(UNITS_PER_BLOCK == 2 * BN / 8, "16 octets x 2 halves");
+constexpr int UNIT_KEYS = 4;                        // keys per warp unit
+constexpr int UNITS_PER_BLOCK = BN / UNIT_KEYS;     // 32: one ready flag each
+constexpr int PER_LANE = ROW_CHUNKS / 8;               // 9 granules per lane (8 lanes per key)
+static_assert(UNIT_KEYS * 8 == 32 && PER_LANE * 8 == ROW_CHUNKS, "8 lanes per key");
+static_assert(UNITS_PER_BLOCK == 32, "one flag per lane of the reader's warp");
 
 // Packed blocks whose descriptions every pack CTA tabulates in shared memory
 // (16 bytes each); larger calls describe each block as they reach it.
@@ -164,10 +142,9 @@ __device__ __noinline__ int4 block_info(const Params& p, int q, int max_blocks) 
   return make_int4(b * max_blocks + kb, rq.ip0, kb * BN, rq.hi);
 }
 
-// Unit u: unit u % 32 of block u / 32 of the pack order -- key octet
-// (u % 32) >> 1, dim half u & 1.  blk: the packed block, or -1 (nothing to
-// pack).  slot: lanes 0..7 hold the cache slot of key `lane` of the octet
-// (-1: none / outside).
+// Unit u: 4-key group u % 32 of block u / 32 of the pack order.  blk: the
+// packed block, or -1 (nothing to pack).  slot: lanes 0..3 hold the cache
+// slot of key `lane` of the unit (-1: none / outside).
 struct Unit {
   int blk, slot;
 };
@@ -179,22 +156,36 @@ __device__ __forceinline__ Unit locate(const Params& p, const int4* s_tab, int m
   const int4 e = s_tab ? s_tab[u / UNITS_PER_BLOCK] : block_info(p, u / UNITS_PER_BLOCK, max_blocks);
   t.blk = e.x;
   t.slot = -1;
-  const int j = e.z + (grp >> 1) * 8 + lane;
-  if (e.x >= 0 && lane < 8 && j < e.w) {
+  const int j = e.z + grp * UNIT_KEYS + lane;
+  if (e.x >= 0 && lane < UNIT_KEYS && j < e.w) {
     const long long s = key_slot(p, e.y, j);
-    if (s < 0 && (grp & 1) == 0) atomicOr(p.err, ERR_SLOT);   // reported once per key
+    if (s < 0) atomicOr(p.err, ERR_SLOT);
     t.slot = static_cast<int>(s);
   }
   return t;
 }
 
-__device__ __forceinline__ void load_unit(const Params& p, const Unit& t, int grp, int lane, uint4 (&v)[PER_LANE]) {
-  load_half(p, __shfl_sync(0xffffffffu, t.slot, lane & 7), grp & 1, lane, v);
+// Lane l moves granules l % 8, l % 8 + 8, .. of key l / 8 of the unit:
+// granule l % 8 of each of the nine 64-dim chunks.
+__device__ __forceinline__ void load_unit(const Params& p, const Unit& t, int lane, uint4 (&v)[PER_LANE]) {
+  const int sk = __shfl_sync(0xffffffffu, t.slot, lane >> 3);
+  const uint4* src = reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(sk) * D_QK) + (lane & 7);
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) v[i] = make_uint4(0, 0, 0, 0);
+  if (sk >= 0) {   // streamed once
+    const uint64_t pol = evict_first_policy();
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) v[i] = load_row_granule(src + 8 * i, pol);
+  }
 }
 
 __device__ __forceinline__ void store_unit(uint8_t* packed, const Unit& t, int grp, int lane,
                                            const uint4 (&v)[PER_LANE], bool& bad) {
-  store_half(packed + static_cast<size_t>(t.blk) * BLOCK_BYTES, grp >> 1, grp & 1, lane, v, bad);
+  const int j = grp * UNIT_KEYS + (lane >> 3);   // key within the block
+  uint8_t* dst = packed + static_cast<size_t>(t.blk) * BLOCK_BYTES + j * 128 +
+                 (((lane & 7) ^ (j & 7)) << 4);
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) *reinterpret_cast<uint4*>(dst + i * (BN * 128)) = widen_bf16x8(v[i], bad);
 }
 
 // Pack units first, first + stride, .. below `end`.  Per round a warp
@@ -208,7 +199,7 @@ __device__ __forceinline__ void pack_units(const Params& p, const int4* s_tab, u
   bool bad = false;
   Unit cur = locate(p, s_tab, max_blocks, u, lane);
   uint4 v[PER_LANE];
-  if (cur.blk >= 0) load_unit(p, cur, u & (UNITS_PER_BLOCK - 1), lane, v);
+  if (cur.blk >= 0) load_unit(p, cur, lane, v);
 #pragma unroll 1
   for (; u < end; u += stride) {
     const bool more = u + stride < end;
@@ -218,7 +209,7 @@ __device__ __forceinline__ void pack_units(const Params& p, const int4* s_tab, u
       // The stores must reach the reader's bulk copies (async proxy).
       asm volatile("fence.proxy.async.global;\n" ::: "memory");
     }
-    if (more && nxt.blk >= 0) load_unit(p, nxt, (u + stride) & (UNITS_PER_BLOCK - 1), lane, v);
+    if (more && nxt.blk >= 0) load_unit(p, nxt, lane, v);
     if (cur.blk >= 0) {
       // Publish unit k: the release store orders the warp's stores (made
       // visible to lane 0 by the warp barrier) before the flag.
@@ -265,26 +256,6 @@ __global__ void __maxnreg__(64) pack_kv_overlap_kernel(const Params p, uint8_t* 
   pack_units(p, s_tab, packed, max_blocks, first, wide ? wide_end : units, (wide ? n : stay) * WPC, lane, tag);
 }
 
-// One small CTA per SM beside the attention kernel's CTAs for the whole call
-// (128 threads, at most 112 registers and no dynamic shared memory: it fits
-// in what an attention CTA leaves of an SM), so the pack overlaps the
-// attention kernel even when the attention grid fills every SM.  Warp w of
-// CTA c takes units w * n + c, w * n + c + 4 n, .. in split-position order;
-// each unit is published through its ready flag as in the two-phase pack.
-constexpr int RES_THREADS = 128;
-__global__ void __maxnreg__(112) pack_kv_resident_kernel(const Params p, uint8_t* packed,
-                                                         int max_blocks, int per_split) {
-  // The attention kernel may be scheduled as soon as every pack CTA runs.
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nq = p.nsplit * p.batch * per_split;     // blocks in the pack order
-  const int units = UNITS_PER_BLOCK * nq;            // < 2^31 (host check)
-  const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
-  const int n = gridDim.x;
-  pack_units(p, nullptr, packed, max_blocks, warp * n + static_cast<int>(blockIdx.x), units,
-             n * (RES_THREADS / 32), lane, tag);
-}
-
 }  // namespace
 
 size_t packed_block_bytes() { return BLOCK_BYTES; }
@@ -296,21 +267,8 @@ cudaError_t pack_kv_prepare() {
   cudaError_t e = cudaFuncSetAttribute(pack_kv_overlap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sizeof(int4)) * TABLE_BLOCKS);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(pack_kv_overlap_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(pack_kv_resident_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+  return cudaFuncSetAttribute(pack_kv_overlap_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                               cudaSharedmemCarveoutMaxShared);
-}
-
-cudaError_t launch_pack_kv_resident(const Params& p, void* packed, int max_blocks, int num_ctas,
-                                    cudaStream_t stream) {
-  const int per_split = (max_blocks + p.nsplit - 1) / p.nsplit;
-  const long long nq = 1LL * p.nsplit * p.batch * per_split;
-  if (UNITS_PER_BLOCK * nq > 0x7fffffffLL || num_ctas < 1) return cudaErrorInvalidConfiguration;
-  pack_kv_resident_kernel<<<num_ctas, RES_THREADS, 0, stream>>>(p, static_cast<uint8_t*>(packed),
-                                                                max_blocks, per_split);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_pack_kv(const Params& p, void* packed, int max_blocks, cudaStream_t stream) {

@@ -1,15 +1,11 @@
-// Split-KV partial kernel on the sm_103a tensor cores (tcgen05 + TMEM) for
-// one row tile per request (T*H <= 64): its CTAs gather their own key rows.
+// Split-KV partial kernel on the sm_103a tensor cores (tcgen05 + TMEM),
+// warp-specialised and pipelined.
 //
 // One CTA = one request b, one tile of 64 query rows (r = t*H + h), one key
 // split: the KV-split "partial" half of the partial + reduce design in "The
 // Decisive A/B: When Benchmarking Honesty Reveals the Real Bottleneck"
 // (sections "The Context" and "What This Reveals About the Bottleneck": KV
 // split for occupancy, 128-bit vector loads of scattered page_size=1 rows).
-// With a single row tile every key block is read by one CTA, so gathering
-// it once through a pack kernel (pack_kv.cu, partial_tv.cu) would only add a
-// write and a read-back of every block: the softmax warps gather each block
-// straight from the cache with 16-byte cp.async loads.
 //
 // The products are taken transposed so that every MMA has M = 128:
 //     S^T[key, row] = K_block[128 x 576] . Q_tile[64 x 576]^T          (fp16)
@@ -17,25 +13,34 @@
 // O^T lives in tensor memory for the whole split (4 tiles of 128 dims x 64
 // rows = columns 0..255) and S^T in columns 256..319.  With one thread per
 // key the softmax reduces each query row across the 128 TMEM lanes (a
-// shuffle transpose-reduce per warp, shared memory across four warps).  The
-// running row max is exact, so P <= 1 and the key holding the max has P = 1
-// exactly; O^T columns are rescaled in TMEM only for the 32-row groups whose
-// max moved.  P is fp16 and the values are fp16 (widened in shared memory),
-// because P in bf16 costs more than the 1e-2 output tolerance allows.
+// shuffle transpose-reduce per warp, shared memory across four warps).  The running row
+// max is exact, so P <= 1 and the key holding the max has P = 1 exactly (a
+// lazily moved max would round the dominant key's weight too, which doubles
+// the worst-case output error on spiky keys); O^T columns are rescaled in
+// TMEM only for the 32-row groups whose max moved.  P is fp16 and the values
+// are fp16 (widened by the pack), because P in bf16 costs more than the 1e-2
+// output tolerance allows.
+//
+// The key blocks come from the per-call pack (pack_kv.cu): 147456 contiguous
+// bytes per 128-key block, already fp16 and already in the 128-byte-swizzled
+// operand layout, so each chunk pair arrives with one 32 KB bulk copy.  The
+// pack may still be running: the copy warp then waits for each block's
+// ready flags (tagged with the call's epoch) instead of the whole pack grid,
+// and the last CTA to finish advances the epoch.
 //
 // Roles (10 warps):
 //   warps 0-7  softmax: one thread per (key of the block, half of the 64 query
-//              rows); warps w and w+4 share TMEM lane quadrant w.  They load
-//              the Q tile (issued at entry) and each key block: 16-byte
-//              cp.async gathers into the swizzled key-major chunk tiles, once
-//              O^T of the previous block has read them, widened to fp16 in
-//              place;
+//              rows); warps w and w+4 share TMEM lane quadrant w.  First they
+//              load the Q tile (issued at entry) and widen it to fp16;
 //   warp 8     issues the MMAs (one elected lane of the converged warp); it
 //              owns the TMEM allocation;
-//   warp 9     idle (kept so the warp-to-lane-quadrant mapping matches the
-//              packed kernel's).
-// Per 128-key block k: gather -> S^T(k) chunk pair by chunk pair -> softmax
-// (mask, max, P^T(k) into the rope chunk tile) -> O^T(k) tile by tile.
+//   warp 9     streams the packed blocks with cp.async.bulk (elected lane).
+// Pipeline over 128-key blocks k (mbarriers, all waits bounded):
+//   producer: chunk pair d of block k+1 is copied as soon as O^T(k) tile d has
+//             finished with it; the rope chunk (which holds P^T(k)) last;
+//   MMA:      S^T(k) chunk pair by chunk pair as the pairs land, then, once
+//             softmax(k) is done, O^T(k) tile by tile;
+//   softmax:  after S^T(k): mask, max, P^T(k) into the rope chunk tile.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -54,6 +59,7 @@ constexpr int SOFTMAX_WARPS = 8, MMA_WARP = 8, COPY_WARP = 9;
 constexpr int HALF = BM / 2;    // query-row columns per softmax thread
 constexpr int Q_CHUNK = BM * 128;   // one 64-dim chunk of the Q tile
 constexpr int KV_CHUNK = BN * 128;  // one 64-dim chunk of the key block
+constexpr int PACKED_BLOCK = 9 * KV_CHUNK;       // one packed 128-key block
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + 9 * Q_CHUNK;
 constexpr int OFF_P = OFF_KV + 8 * KV_CHUNK;   // rope chunk tile, reused for P^T
@@ -66,7 +72,7 @@ constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -
 constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [16] mbarriers
 constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, abort flag
 constexpr int OFF_PAR = OFF_MISC + 16;          // int [32] draft parents
-constexpr int OFF_SLOTK = OFF_PAR + MAX_T * 4;  // int [128] slots of the block being gathered
+constexpr int OFF_SLOTK = OFF_PAR + MAX_T * 4;  // int [128] slots of the block being gathered (direct mode)
 constexpr int SMEM_TOTAL = OFF_SLOTK + BN * 4;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -142,6 +148,35 @@ __device__ __forceinline__ int block_slot(const Params& p, const Request& rq, in
   return static_cast<int>(s);
 }
 
+// Wait (bounded) until the pack kernel has published all 32 four-key units
+// of block kb of request b for this call: lane l watches unit l's flag with
+// acquire loads.  Whole warp; false on a timeout or an earlier abort.
+__device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsigned tag,
+                                            volatile int* abort, int* err) {
+  const int lane = threadIdx.x & 31;
+  const unsigned* flag = p.pack_sync + PACK_SYNC_HEADER +
+                         32 * (static_cast<size_t>(b) * p.packed_max_blocks + kb) + lane;
+  const long long t0 = clock64();
+  while (true) {   // every exit decision is warp-uniform
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
+    if (__all_sync(0xffffffffu, v == tag)) break;
+    if (__any_sync(0xffffffffu, *abort != 0)) return false;
+    if (__any_sync(0xffffffffu, clock64() - t0 > WAIT_LIMIT)) {
+      if (lane == 0) {
+        *abort = 1;
+        atomicOr(err, ERR_TIMEOUT);
+      }
+      __syncwarp();
+      return false;
+    }
+  }
+  // The packed bytes were written through the generic proxy; the bulk copies
+  // that follow read them through the async proxy.
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+  return true;
+}
+
 // Every CTA takes one ticket when it is done; the last one of the grid
 // advances the epoch, so the next call's pack kernel publishes a new tag.
 // The epoch stays below 2^32 - 1, so the tag (epoch + 1) is never 0 -- the
@@ -155,6 +190,10 @@ __device__ __forceinline__ void finish_call(const Params& p) {
     *reinterpret_cast<volatile unsigned*>(p.pack_sync) = e + 1u == 0xffffffffu ? 0u : e + 1u;
   }
 }
+
+// Rows whose O^T columns one softmax warp rescales one by one (their loads
+// overlapping the P computation); more moved rows take the whole-half pass.
+constexpr int FEW_MOVED = 4;
 
 // Column maxima of a warp's 32 x 32 tile (lane = key, v[c] = column c) in 31
 // shuffles: each step halves the columns a lane holds and swaps the other
@@ -237,7 +276,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     asm volatile("cp.async.wait_all;\n" ::: "memory");
     return;
   }
-  if ((sbase & 1023) || !p.direct_all) {   // aligned swizzled tiles; gather mode only
+  if (sbase & 1023) {   // swizzled operand tiles need a 1024-byte aligned base
     if (tid == 0) {
       atomicOr(p.err, ERR_INTERNAL);
       finish_call(p);
@@ -271,8 +310,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == COPY_WARP) {
-    // idle: the softmax warps gather the key blocks
+  if (warp == COPY_WARP && p.direct_all) {
+    // direct mode: the softmax warps gather the key blocks themselves
+  } else if (warp == COPY_WARP) {
+    // ======================= packed-block producer ==========================
+    // The whole warp runs the loop; one elected lane issues each copy.
+    const uint8_t* blocks = p.packed + static_cast<size_t>(b) * p.packed_max_blocks * PACKED_BLOCK;
+    // The packed blocks come from the pack kernel just before this one on
+    // the stream, which may still be running: with per-unit flags each block
+    // is read once its 32 units carry this call's tag, else after the whole
+    // pack grid (a no-op when launched without overlap).
+    const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
+    if (!p.pack_flags) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    int issued = 0;   // copies issued, in (block, g) order
+#pragma unroll 1
+    for (int it = 0; it < nb; ++it) {
+      const uint8_t* src = blocks + static_cast<size_t>(kb0 + it) * PACKED_BLOCK;
+      const uint32_t prev = static_cast<uint32_t>((it - 1) & 1);
+      if (p.pack_flags && !wait_packed(p, b, kb0 + it, tag, s_abort, p.err)) break;
+      for (int g = 0; g < 5; ++g) {
+        // Pair g of this block overwrites pair g of the previous one (and
+        // the rope chunk its P^T): wait until O^T(k-1) has read them.
+        if (it > 0 && g < 4) wait_warp(mbar(MB_OT + g), prev, s_abort, p.err);
+        if (*s_abort) break;
+        const uint32_t bytes = g < 4 ? 2 * KV_CHUNK : KV_CHUNK;
+        const uint32_t off = g < 4 ? 2 * g * KV_CHUNK : 8 * KV_CHUNK;
+        tc::bulk_copy_expect(sbase + OFF_KV + off, src + off, bytes, mbar(MB_CHUNK + g));
+        ++issued;
+      }
+      if (*s_abort) break;
+    }
+    // After an abort the last copy into each slot may still be in flight:
+    // let it land before shared memory is reused or released.
+    if (*s_abort) {
+      for (int g = 0; g < 5 && g < issued; ++g)
+        wait_drain(mbar(MB_CHUNK + g), static_cast<uint32_t>(((issued - 1 - g) / 5) & 1), p.err);
+      __syncwarp();
+    }
   } else if (warp == MMA_WARP) {
     // ============================ MMA issuer ===============================
     // The whole warp runs the loop (warp-uniform operands); one elected lane
@@ -346,15 +420,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
     float lpart[HALF];                  // this key's share of its rows' sums
 #pragma unroll
     for (int c = 0; c < HALF; ++c) lpart[c] = 0.f;
-    // Out-of-cache slots are reported here.
-    int slot_next = nb > 0 ? block_slot(p, rq, kb0, j, true) : -1;
+    // Direct mode: out-of-cache slots are reported here (else by the pack).
+    const bool direct = p.direct_all != 0;
+    int slot_next = nb > 0 ? block_slot(p, rq, kb0, j, direct) : -1;
     bool next_ok = slot_next >= 0;
 #pragma unroll 1
     for (int it = 0; it < nb; ++it) {
       const int kb = kb0 + it;
       const uint32_t par = static_cast<uint32_t>(it & 1);
       const bool key_ok = next_ok;
-      {
+      if (direct) {
         // Gather block kb: 128 scattered rows straight from the cache into
         // the swizzled chunk tiles (absent or invalid keys zero-filled),
         // once O^T(kb-1) has read the previous block and its P^T; widen to
@@ -391,6 +466,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         named_sync(1, SOFTMAX_WARPS * 32);
         if (tid == 0)
           for (int g = 0; g < 5; ++g) tc::mbar_arrive(mbar(MB_CHUNK + g));
+      } else if (it + 1 < nb) {
+        next_ok = block_slot(p, rq, kb + 1, j, false) >= 0;
       }
       const int jg = kb * BN + j;
       wait_warp(mbar(MB_S), par, s_abort, p.err);
@@ -427,6 +504,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       }
       named_sync(1, 256);
       bool moved;
+      uint32_t moved_rows;
       {
         const float4 q4 = *reinterpret_cast<const float4*>(s_red + (c0 + lane) * 4);
         const float bm = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
@@ -435,10 +513,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
           if (mrow != -INFINITY) alpha = ex2(mrow - bm);
           mrow = bm;
         }
-        moved = __any_sync(0xffffffffu, alpha != 1.f);
+        moved_rows = __ballot_sync(0xffffffffu, alpha != 1.f);
+        moved = moved_rows != 0;
         w_m[lane] = mrow == -INFINITY ? 0.f : mrow;   // a fully masked row: every p = ex2(-inf) = 0
         w_a[lane] = alpha;
         __syncwarp();
+      }
+      // Rescale of the O^T columns of this half's rows whose max moved
+      // (O^T(k-1) is complete: S^T(k) finished after it on the in-order
+      // tensor pipe).  A few rows: their columns of the four tiles are loaded
+      // now, while P is computed, then scaled and stored; many: the whole
+      // half after P.
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + c0;
+      const int cnt = __popc(moved_rows);
+      const bool few = moved && cnt <= FEW_MOVED;
+      uint32_t rv[FEW_MOVED][4];
+      uint32_t cols[FEW_MOVED];
+      if (few) {
+        uint32_t m = moved_rows;
+#pragma unroll
+        for (int i = 0; i < FEW_MOVED; ++i) {
+          const int c = m ? __ffs(m) - 1 : 0;
+          m &= m - 1;
+          cols[i] = static_cast<uint32_t>(c);
+          if (i < cnt)
+#pragma unroll
+            for (int d = 0; d < 4; ++d) rv[i][d] = tc::tmem_ld1(lane_base + d * BM + c);
+        }
       }
       // This key's P^T entries for the half's 32 query rows as fp16 (four
       // 16-byte granules of the key's 128-byte swizzled row), into the rope
@@ -473,21 +574,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         *reinterpret_cast<uint4*>(prow + ((gg ^ (j & 7)) << 4)) =
             make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
       }
-      // Rescale this half's O^T columns if any of its rows' max moved (O^T(k-1)
-      // is complete: S^T(k) finished after it on the in-order tensor pipe).
-      if (moved) {
+      if (few) {
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < FEW_MOVED; ++i)
+          if (i < cnt) {
+            const float a = w_a[cols[i]];
+#pragma unroll
+            for (int d = 0; d < 4; ++d)
+              tc::tmem_st1(lane_base + d * BM + cols[i], __float_as_uint(__uint_as_float(rv[i][d]) * a));
+          }
+        tc::tmem_wait_st();
+      } else if (moved) {
 #pragma unroll 1
         for (int d = 0; d < 4; d += 2) {
-          const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + d * BM + c0;
+          const uint32_t ta = lane_base + d * BM;
           uint32_t v0[HALF], v1[HALF];
           tc::tmem_ld32(ta, v0);
           tc::tmem_ld32(ta + BM, v1);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < HALF; ++c) {
-            const float al = w_a[c];
-            v0[c] = __float_as_uint(__uint_as_float(v0[c]) * al);
-            v1[c] = __float_as_uint(__uint_as_float(v1[c]) * al);
+            const float a = w_a[c];
+            v0[c] = __float_as_uint(__uint_as_float(v0[c]) * a);
+            v1[c] = __float_as_uint(__uint_as_float(v1[c]) * a);
           }
           tc::tmem_st32(ta, v0);
           tc::tmem_st32(ta + BM, v1);

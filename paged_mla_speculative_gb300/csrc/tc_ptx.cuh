@@ -46,28 +46,6 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
-// Same MMA with the A operand in tensor memory (lanes = M rows, K packed
-// two 16-bit values per 32-bit column): D (+)= A[a_tmem] . B[b].
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\n.reg .pred e;\n"
-      "elect.sync _|e, 0xffffffff;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
-}
-
-// Copy 128 rows x 32 bytes from shared memory (descriptor `src`, K-major:
-// one row per TMEM lane) into 8 consecutive TMEM columns at `taddr`.  Runs
-// on the tensor pipe in issue order with the MMAs of the issuing thread.
-__device__ __forceinline__ void cp_128x256b(uint32_t taddr, uint64_t src) {
-  asm volatile(
-      "{\n.reg .pred e;\n"
-      "elect.sync _|e, 0xffffffff;\n"
-      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n}\n" ::"r"(taddr), "l"(src));
-}
-
 // Arrive once on the mbarrier when every MMA the elected lane issued so far
 // is done.
 __device__ __forceinline__ void commit(uint32_t mbar) {
@@ -135,6 +113,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
       "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
       "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+// One TMEM column for the warp's 32 lanes.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n" : "=r"(r) : "r"(taddr));
+  return r;
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n" ::"r"(taddr), "r"(v));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }

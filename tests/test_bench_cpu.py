@@ -14,9 +14,9 @@ from paged_mla_speculative_gb300 import binding as mb  # noqa: E402
 
 def test_kernel_list_follows_the_pack_schedule():
     assert bench.kernels_of(mb.KERNEL_TC, 2, "idle_sms") == \
-        "pack_kv_overlap_kernel + partial_tv_kernel + combine_kernel"
-    assert bench.kernels_of(mb.KERNEL_TC, 2, "whole") == "pack_kv_kernel + partial_tv_kernel + combine_kernel"
-    assert bench.kernels_of(mb.KERNEL_TC, 1, "resident") == "pack_kv_resident_kernel + partial_tv_kernel"
+        "pack_kv_overlap_kernel + partial_tc_kernel + combine_kernel"
+    assert bench.kernels_of(mb.KERNEL_TC, 2, "whole") == "pack_kv_kernel + partial_tc_kernel + combine_kernel"
+    assert bench.kernels_of(mb.KERNEL_TC, 1, "whole") == "pack_kv_kernel + partial_tc_kernel"
     assert bench.kernels_of(mb.KERNEL_TC, 3, "none") == "partial_tc_kernel + combine_kernel"
     assert bench.kernels_of(mb.KERNEL_MMA, 3) == "partial_mma_kernel + combine_kernel"
 
@@ -35,7 +35,7 @@ def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch)
     prof = tmp_path / "profiles"
     prof.mkdir()
     entry = {"workload": "decode_batch", "dram_bytes_per_launch": 123.0, "source_sha1": src_hash}
-    (prof / "traffic.json").write_text(json.dumps({"partial_tv_kernel": entry}))
+    (prof / "traffic.json").write_text(json.dumps({"partial_tc_kernel": entry}))
     # the hash is taken from the real sources; only the traffic file is redirected
     real_root = bench.ROOT
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: src_hash)
@@ -43,6 +43,6 @@ def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch)
     assert bench.profiled_traffic("decode_batch") == 123.0
     assert bench.profiled_traffic("tree") is None
     entry["source_sha1"] = "0" * 40
-    (prof / "traffic.json").write_text(json.dumps({"partial_tv_kernel": entry}))
+    (prof / "traffic.json").write_text(json.dumps({"partial_tc_kernel": entry}))
     assert bench.profiled_traffic("decode_batch") is None
     monkeypatch.setattr(bench, "ROOT", real_root)

@@ -4,9 +4,9 @@ Static buffers are captured once; between replays the metadata (kv_lens,
 indices, parents), q and the cache change, so a replay that baked any device
 value into the graph would give the wrong answer.  Every replay must equal
 an eager call on the same buffers bit for bit, and match the oracle.  Each
-key-pack schedule the library picks (pack overlapping the attention kernel,
-whole pack first, one pack CTA per SM beside the attention CTAs, attention
-CTAs gathering directly), page size 64, bf16 output, the mma.sync family and
+key-pack schedule (pack overlapping the attention kernel on idle SMs, whole
+pack first, attention CTAs gathering directly -- automatic with one row tile,
+forced with several), page size 64, bf16 output, the mma.sync family and
 full-size workloads are captured.
 """
 import dataclasses
@@ -42,8 +42,7 @@ CASES = {
     "idle_sms_one_split": (8, 16, 1, torch.float32, mb.KERNEL_TC, 1, mb.PACK_IDLE_SMS, mb.PACK_IDLE_SMS),
     "whole": (8, 64, 1, torch.float32, mb.KERNEL_TC, 6, mb.PACK_WHOLE, mb.PACK_WHOLE),
     "whole_ps64_bf16": (8, 64, 64, torch.bfloat16, mb.KERNEL_TC, 6, mb.PACK_WHOLE, mb.PACK_WHOLE),
-    "resident": (8, 64, 1, torch.float32, mb.KERNEL_TC, 6, mb.PACK_RESIDENT, mb.PACK_RESIDENT),
-    "resident_ps64_bf16": (8, 16, 64, torch.bfloat16, mb.KERNEL_TC, 3, mb.PACK_RESIDENT, mb.PACK_RESIDENT),
+    "forced_no_pack": (8, 64, 1, torch.float32, mb.KERNEL_TC, 3, mb.PACK_NONE, mb.PACK_NONE),
     "auto": (8, 32, 1, torch.float32, mb.KERNEL_TC, 0, mb.PACK_AUTO, None),
     "direct": (4, 16, 1, torch.float32, mb.KERNEL_TC, 4, mb.PACK_AUTO, mb.PACK_NONE),
     "direct_ps64_bf16": (4, 16, 64, torch.bfloat16, mb.KERNEL_TC, 3, mb.PACK_AUTO, mb.PACK_NONE),
