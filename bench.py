@@ -58,6 +58,10 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--calls-only", choices=["attn", "index", "compact"], default=None,
+                    help="no timing: issue --steps calls of one workload (a target for a profiler)")
+    ap.add_argument("--kernel", choices=["auto", "tc", "mma"], default="auto")
+    ap.add_argument("--pack-schedule", choices=["auto", "whole", "idle_sms", "none"], default="auto")
     return ap.parse_args(argv)
 
 
@@ -634,8 +638,44 @@ def run_gb300(args):
     return 0
 
 
+def run_calls_only(args):
+    """Issue --steps calls of one workload and check the device word: no
+    timing, no extra passes (a short, fixed launch sequence to profile)."""
+    import torch
+    from paged_mla_speculative_gb300 import binding as mb
+    from paged_mla_speculative_gb300 import build as mbuild
+    from paged_mla_speculative_gb300 import workloads as W
+    mbuild.build()
+    name = HEADLINE if args.workload == CURVE_NAME else args.workload
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, device="cuda")
+    plan = mb.Plan(w.batch, w.num_drafts, w.num_heads, w.page_size, w.num_slots, max(inp.kv_lens.tolist()))
+    plan.set_kernel({"auto": mb.KERNEL_AUTO, "tc": mb.KERNEL_TC, "mma": mb.KERNEL_MMA}[args.kernel])
+    plan.set_pack_schedule({"auto": mb.PACK_AUTO, "whole": mb.PACK_WHOLE, "idle_sms": mb.PACK_IDLE_SMS,
+                            "none": mb.PACK_NONE}[args.pack_schedule])
+    stream = torch.cuda.current_stream()
+    for _ in range(args.steps):
+        if args.calls_only == "attn":
+            mb.mla_verify_attn(plan, inp.q, inp.kv_cache, inp.kv_indices, inp.kv_indptr, inp.kv_lens,
+                               inp.draft_parent, inp.scale)
+        elif args.calls_only == "index":
+            index_builder_timing(mb, plan, inp, w, torch.empty(1 << 20, dtype=torch.uint8, device="cuda"),
+                                 stream, 1)
+        else:
+            compaction_timing(mb, plan, inp, w, torch.empty(1 << 20, dtype=torch.uint8, device="cuda"),
+                              stream, 1)
+    torch.cuda.synchronize()
+    assert plan.get_error() == 0
+    print(json.dumps({"calls_only": args.calls_only, "workload": name, "calls": args.steps,
+                      "nsplit": plan.nsplit(w.batch), "pack_schedule": PACK_NAMES[plan.pack_mode(w.batch)]}))
+    plan.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.calls_only:
+        return run_calls_only(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gb300(args)
