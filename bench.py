@@ -60,7 +60,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--calls-only", choices=["attn", "index", "compact"], default=None,
                     help="no timing: issue --steps calls of one workload (a target for a profiler)")
-    ap.add_argument("--kernel", choices=["auto", "tc", "mma"], default="auto")
+    ap.add_argument("--kernel", choices=["auto", "pair", "tc", "mma"], default="auto")
     ap.add_argument("--pack-schedule", choices=["auto", "whole", "idle_sms", "none"], default="auto")
     return ap.parse_args(argv)
 
@@ -77,16 +77,20 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+PARTIAL_SOURCES = {"partial_tc_kernel": "partial_tc.cu", "partial_pair_kernel": "partial_pair.cu",
+                   "partial_mma_kernel": "partial_mma.cu"}
+
+
+def kernel_source_hash(kernel="partial_pair_kernel"):
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "paged_mla_speculative_gb300", "csrc")
-    for name in ("common.cuh", "tc_ptx.cuh", "partial_tc.cu"):
+    for name in ("common.cuh", "tc_ptx.cuh", PARTIAL_SOURCES[kernel]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, kernel="partial_pair_kernel"):
     """DRAM bytes per launch of the attention kernel from a committed ncu
     summary, if it was taken on the current kernel source and workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -95,8 +99,8 @@ def profiled_traffic(workload):
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d.get("partial_tc_kernel", {})
-        if e.get("source_sha1") == kernel_source_hash() and e.get("workload") == workload:
+        e = d.get(kernel, {})
+        if e.get("source_sha1") == kernel_source_hash(kernel) and e.get("workload") == workload:
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -143,6 +147,7 @@ def compaction_timing(mb, plan, inp, w, flush, stream, steps):
 
 PACK_NAMES = {1: "whole", 2: "idle_sms", 4: "none"}
 PACK_KERNELS = {"whole": "pack_kv_kernel", "idle_sms": "pack_kv_overlap_kernel"}
+PARTIAL_NAMES = {1: "partial_mma_kernel", 2: "partial_tc_kernel", 3: "partial_pair_kernel"}
 
 
 def kernels_of(kernel, ns, schedule="whole"):
@@ -151,7 +156,8 @@ def kernels_of(kernel, ns, schedule="whole"):
     keys)."""
     from paged_mla_speculative_gb300 import binding as mb
     tc = ["partial_tc_kernel"] if schedule == "none" else [PACK_KERNELS[schedule], "partial_tc_kernel"]
-    names = {mb.KERNEL_TC: tc, mb.KERNEL_MMA: ["partial_mma_kernel"]}[kernel]
+    pair = [PACK_KERNELS.get(schedule, "pack_kv_kernel"), "partial_pair_kernel"]
+    names = {mb.KERNEL_TC: tc, mb.KERNEL_MMA: ["partial_mma_kernel"], mb.KERNEL_PAIR: pair}[kernel]
     return " + ".join(names + (["combine_kernel"] if ns > 1 else []))
 
 
@@ -409,7 +415,10 @@ def run_reference(args):
     return 0
 
 
-def measure_workload(mb, W, name, flush, steps, clocks=None):
+KERNEL_IDS = {"auto": 0, "mma": 1, "tc": 2, "pair": 3}   # MLA_VERIFY_KERNEL_*
+
+
+def measure_workload(mb, W, name, flush, steps, clocks=None, kernel="auto"):
     """µs per call of one workload: `steps` CUDA-graph replays (the capture-
     safe production path), each after an L2 flush, bracketed by events on the
     replay stream; then eager calls, and eager calls with the library's
@@ -420,6 +429,7 @@ def measure_workload(mb, W, name, flush, steps, clocks=None):
     work = W.algorithmic_work(inp.prefix, w.num_drafts, w.num_heads)
     plan = mb.Plan(w.batch, w.num_drafts, w.num_heads, w.page_size, w.num_slots,
                    max(inp.kv_lens.tolist()))
+    plan.set_kernel(KERNEL_IDS[kernel])
     ns = plan.nsplit(w.batch)
     out, lse = plan.new_outputs(w.batch)
     st = torch.cuda.Stream()
@@ -434,7 +444,8 @@ def measure_workload(mb, W, name, flush, steps, clocks=None):
             flush.zero_()
             call()
     st.synchronize()
-    assert plan.get_error() == 0, f"{name}: device error word set during warm-up"
+    err = plan.get_error()
+    assert err == 0, f"{name}: device error word {err:#x} set during warm-up"
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=st):
         call()
@@ -475,7 +486,8 @@ def measure_workload(mb, W, name, flush, steps, clocks=None):
     k2 = min(steps, 100)
     eager_ms = timed(k2, call)
     pack_ms, part_ms, comb_ms, ser_ms = timed(k2, call, events=True)
-    assert plan.get_error() == 0, f"{name}: device error word set while timing"
+    err = plan.get_error()
+    assert err == 0, f"{name}: device error word {err:#x} set while timing"
     peaks, peak_src = load_peaks()
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     tc = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
@@ -498,7 +510,8 @@ def measure_workload(mb, W, name, flush, steps, clocks=None):
         "partial_tflops": work["flops"] / (part_us * 1e-6) / 1e12,
         "partial_frac_of_tensor_peak": work["flops"] / (part_us * 1e-6) / 1e12 / tc,
         "keys": work["keys"], "kv_bytes": work["kv_bytes"], "flops": work["flops"],
-        "nsplit": ns, "pack_schedule": sched, "kernels": kernels_of(plan.kernel(), ns, sched),
+        "nsplit": ns, "pack_schedule": sched, "kernels": kernels_of(plan.call_kernel(w.batch), ns, sched),
+        "partial_kernel": PARTIAL_NAMES[plan.call_kernel(w.batch)],
         "calls_timed": len(graph_ms),
     }
     state = {"inp": inp, "plan": plan, "out": out, "lse": lse, "work": work, "wall": wall,
@@ -533,7 +546,7 @@ def run_gb300(args):
     barrier(ws)
     torch.cuda.synchronize()
     clk = ClockSampler(uuid)
-    res, st = measure_workload(mb, W, head, flush, K, clocks=clk)
+    res, st = measure_workload(mb, W, head, flush, K, clocks=clk, kernel=args.kernel)
     barrier(ws)
     plan, inp, out, work = st["plan"], st["inp"], st["out"], st["work"]
     w = W.WORKLOADS[head]
@@ -597,8 +610,8 @@ def run_gb300(args):
             "pack_schedule", "kernels", "us_p10_p50_p90", "eager_us_per_call", "pack_us",
             "partial_us", "combine_us")}},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tc_peak, "traffic": profiled_traffic(head),
-                     "kernel": "partial_tc_kernel", "workload": head,
+                     "frac": achieved / tc_peak, "traffic": profiled_traffic(head, res["partial_kernel"]),
+                     "kernel": res["partial_kernel"], "workload": head,
                      "peak_source": f"{st['peak_src']} bf16 burst (fp16 has the same tensor rate)"},
         "clocks": clk.summary(), "gpu_launches": launches,
         "e2e": {"value": e2e_us, "unit": "us/call", "h2d_bytes_per_step": h2d,
@@ -615,7 +628,7 @@ def run_gb300(args):
     if others:
         curve = {head: {**res}}
         for n in others:
-            r, s2 = measure_workload(mb, W, n, flush, min(args.other_steps, K))
+            r, s2 = measure_workload(mb, W, n, flush, min(args.other_steps, K), kernel=args.kernel)
             s2["plan"].close()
             del s2
             torch.cuda.empty_cache()
@@ -650,7 +663,7 @@ def run_calls_only(args):
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w, device="cuda")
     plan = mb.Plan(w.batch, w.num_drafts, w.num_heads, w.page_size, w.num_slots, max(inp.kv_lens.tolist()))
-    plan.set_kernel({"auto": mb.KERNEL_AUTO, "tc": mb.KERNEL_TC, "mma": mb.KERNEL_MMA}[args.kernel])
+    plan.set_kernel(KERNEL_IDS[args.kernel])
     plan.set_pack_schedule({"auto": mb.PACK_AUTO, "whole": mb.PACK_WHOLE, "idle_sms": mb.PACK_IDLE_SMS,
                             "none": mb.PACK_NONE}[args.pack_schedule])
     stream = torch.cuda.current_stream()

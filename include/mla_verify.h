@@ -99,12 +99,23 @@ extern "C" {
 #define MLA_VERIFY_OUT_F32            0
 #define MLA_VERIFY_OUT_BF16           1
 
-/* Kernel family for the partial (split-KV) step; AUTO = TC. */
+/* Kernel family for the partial (split-KV) step; AUTO = PAIR. */
 #define MLA_VERIFY_KERNEL_AUTO        0
 #define MLA_VERIFY_KERNEL_MMA         1   /* warp-level mma.sync, O in registers   */
-#define MLA_VERIFY_KERNEL_TC          2   /* tcgen05 MMAs, O^T in tensor memory;
-                                             key rows gathered once per call by a
-                                             pack kernel, streamed by bulk copies */
+#define MLA_VERIFY_KERNEL_TC          2   /* tcgen05 MMAs on one SM, 64 query rows
+                                             per CTA, O^T in tensor memory; key
+                                             rows gathered once per call by a pack
+                                             kernel, streamed by bulk copies (or,
+                                             with one 64-row tile per request,
+                                             gathered by the attention CTAs)     */
+#define MLA_VERIFY_KERNEL_PAIR        3   /* tcgen05 MMAs on a pair of SMs (one
+                                             cluster, cta_group::2), 128 query rows
+                                             per pair, 256 keys per step, O^T split
+                                             by value dim across the two SMs' tensor
+                                             memory; packed keys as TC.  With one
+                                             64-row tile per request (T*H <= 64) or
+                                             the pack schedule forced to NONE, calls
+                                             run the TC family's direct gather.  */
 
 typedef struct mla_verify_plan mla_verify_plan;
 
@@ -170,11 +181,16 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* plan, int batch, in
 int mla_verify_plan_set_pack_schedule(mla_verify_plan* plan, int schedule);
 int mla_verify_plan_get_pack_mode(const mla_verify_plan* plan, int batch);
 
-/* Select the partial-kernel family (MLA_VERIFY_KERNEL_*; AUTO = TC). */
+/* Select the partial-kernel family (MLA_VERIFY_KERNEL_*; AUTO = PAIR). */
 int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
 
-/* The kernel family calls will run (AUTO resolved), or < 0. */
+/* The kernel family selected (AUTO resolved to PAIR), or < 0.  A PAIR plan
+ * whose calls gather directly (see MLA_VERIFY_KERNEL_PAIR) runs the TC
+ * kernel: mla_verify_plan_get_call_kernel reports which. */
 int mla_verify_plan_get_kernel(const mla_verify_plan* plan);
+/* The partial kernel a call with `batch` requests launches: MLA_VERIFY_KERNEL_
+ * MMA, TC or PAIR, or < 0 (null plan, batch outside [1, max_batch]). */
+int mla_verify_plan_get_call_kernel(const mla_verify_plan* plan, int batch);
 
 /*
  * Profiling hook.  Later mla_verify_attn calls record `after_pack` (if not

@@ -22,6 +22,7 @@ OUT_BF16 = 1
 KERNEL_AUTO = 0
 KERNEL_MMA = 1
 KERNEL_TC = 2
+KERNEL_PAIR = 3
 PACK_AUTO = 0
 PACK_WHOLE = 1
 PACK_IDLE_SMS = 2
@@ -60,6 +61,7 @@ SIGNATURES = {
     "mla_verify_plan_get_pack_mode": (_I, [_P, _I]),
     "mla_verify_plan_set_kernel": (_I, [_P, _I]),
     "mla_verify_plan_get_kernel": (_I, [_P]),
+    "mla_verify_plan_get_call_kernel": (_I, [_P, _I]),
     "mla_verify_plan_workspace_bytes": (ctypes.c_size_t, [_P]),
     "mla_verify_plan_set_profile_events": (_I, [_P, _P, _P]),
     "mla_verify_attn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]),
@@ -205,10 +207,18 @@ class Plan:
         _check(load_library().mla_verify_plan_set_kernel(self.handle, kernel), "set_kernel")
 
     def kernel(self) -> int:
-        """The kernel family calls run (KERNEL_MMA or KERNEL_TC)."""
+        """The kernel family selected (KERNEL_MMA, KERNEL_TC or KERNEL_PAIR)."""
         v = load_library().mla_verify_plan_get_kernel(self.handle)
         if v < 0:
             raise MlaVerifyError(v, "get_kernel")
+        return v
+
+    def call_kernel(self, batch: int) -> int:
+        """The partial kernel a call with `batch` requests launches
+        (KERNEL_MMA, KERNEL_TC or KERNEL_PAIR)."""
+        v = load_library().mla_verify_plan_get_call_kernel(self.handle, batch)
+        if v < 0:
+            raise MlaVerifyError(v, "get_call_kernel")
         return v
 
     def set_profile_events(self, after_pack=None, after_partial=None):

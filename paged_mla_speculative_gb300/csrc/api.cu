@@ -59,14 +59,26 @@ struct mla_verify_plan {
   cudaEvent_t done_ev;
   bool done_recorded;
   cudaStream_t aux;
+  // TMA descriptors of `packed` for the CTA-pair kernel.
+  mlav::PackMaps pack_maps;
 };
 
 namespace {
 
 constexpr int kRowsPerTile = 64;
 
-// Keys per block of the partial kernel the plan runs.
-int keys_per_block(int kernel) { return kernel == MLA_VERIFY_KERNEL_MMA ? 64 : 128; }
+// Keys one split step takes in each partial kernel: 64 (mma.sync), one
+// 128-key block (TC), a 256-key pair block (PAIR).
+int keys_per_block(int kernel) {
+  return kernel == MLA_VERIFY_KERNEL_MMA ? 64 : kernel == MLA_VERIFY_KERNEL_PAIR ? 256 : 128;
+}
+// Query rows one unit of the grid (a CTA, or a CTA pair for PAIR) takes, and
+// its CTAs.
+int rows_per_unit(int kernel) { return kernel == MLA_VERIFY_KERNEL_PAIR ? 128 : kRowsPerTile; }
+int ctas_per_unit(int kernel) { return kernel == MLA_VERIFY_KERNEL_PAIR ? 2 : 1; }
+// Measured time of one split step on GB300 (us): a 128-key block of a TC CTA,
+// a 256-key pair block of a PAIR cluster.
+double step_us(int kernel) { return kernel == MLA_VERIFY_KERNEL_PAIR ? 3.0 : 3.4; }
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
@@ -86,15 +98,22 @@ struct PackSchedule {
   int wide, stay;
 };
 constexpr int kMinPackSms = 16;
+int call_family(const mla_verify_plan* pl);
 PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool overlap, int shards = 1) {
-  const int positions = static_cast<int>(ceil_div(ceil_div(pl->pack_blocks, shards), nsplit));
-  const long long attn = 1LL * nsplit * ceil_div(pl->R, kRowsPerTile) * batch;
+  const int fam = call_family(pl);
+  const bool pairs = fam == MLA_VERIFY_KERNEL_PAIR;
+  // Block positions per split (pairs of positions when splits take pairs).
+  const long long shard_blocks = ceil_div(pl->pack_blocks, shards);
+  const int positions = static_cast<int>(pairs ? 2 * ceil_div(ceil_div(shard_blocks, 2), nsplit)
+                                               : ceil_div(shard_blocks, nsplit));
+  const long long attn = 1LL * nsplit * ceil_div(pl->R, rows_per_unit(fam)) * batch * ctas_per_unit(fam);
   const long long idle = pl->num_sms - attn;
   const PackSchedule whole{MLA_VERIFY_PACK_WHOLE, positions, 0};
   if (!overlap || pl->pack_mode == MLA_VERIFY_PACK_WHOLE) return whole;
   const bool forced_idle = pl->pack_mode == MLA_VERIFY_PACK_IDLE_SMS;
   if (idle < (forced_idle ? 1 : kMinPackSms)) return whole;
-  const double per_block_us = 3.4, lead_us = 5.0, blocks_per_us_per_sm = 0.15;
+  const double per_block_us = pairs ? step_us(fam) / 2 : step_us(fam), lead_us = 5.0,
+               blocks_per_us_per_sm = 0.15;
   const double narrow_us = static_cast<double>(nsplit) * batch / (idle * blocks_per_us_per_sm);
   // Position q >= wide is ready after (q - wide + 1) narrow steps and needed
   // after lead + q attention steps; with narrow steps the slower, the last
@@ -117,15 +136,23 @@ bool gathers_directly(const mla_verify_plan* pl) {
   return pl->pack_mode == MLA_VERIFY_PACK_NONE || ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles;
 }
 
+// The partial kernel calls launch: the PAIR family falls back to the TC
+// kernel's direct gather when there is no pack.
+int call_family(const mla_verify_plan* pl) {
+  if (pl->kernel == MLA_VERIFY_KERNEL_PAIR && gathers_directly(pl)) return MLA_VERIFY_KERNEL_TC;
+  return pl->kernel;
+}
+
 // What the pack leaves on a call's critical path, in attention block steps
 // (~3.4 us): the wide phase (~9 us) when it overlaps, else the whole gather
 // of up to batch x max_kv_len rows (1152 B read + 1152 B written each at
 // ~4.5 TB/s, plus ~3 us); nothing when the attention CTAs gather directly.
 double pack_steps(const mla_verify_plan* pl, int batch, int nsplit, int shards) {
   if (gathers_directly(pl)) return 0.0;
+  const double st = step_us(call_family(pl));
   const PackSchedule ps = pack_plan(pl, batch, nsplit, true, shards);
-  if (ps.mode != MLA_VERIFY_PACK_WHOLE) return 9.0 / 3.4;
-  return (2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0) / 3.4;
+  if (ps.mode != MLA_VERIFY_PACK_WHOLE) return 9.0 / st;
+  return (2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0) / st;
 }
 
 // Keys a request can hold in a call covering one of `shards` shards: a
@@ -138,20 +165,26 @@ long long call_keys(const mla_verify_plan* pl, int shards) {
 // per CTA) plus the cost of moving the split partials through the combine,
 // in units of one CTA key-block step.
 int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel, int shards = 1) {
-  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, kRowsPerTile);
-  const long long max_blocks = ceil_div(call_keys(pl, shards), keys_per_block(kernel));
+  const int rows = rows_per_unit(kernel), per_unit = ctas_per_unit(kernel);
+  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, rows);
+  // A pair block of a range with an odd block count may hold one block.
+  const long long max_blocks = kernel == MLA_VERIFY_KERNEL_PAIR
+                                   ? ceil_div(ceil_div(call_keys(pl, shards), 128), 2)
+                                   : ceil_div(call_keys(pl, shards), keys_per_block(kernel));
   const int cap = static_cast<int>(std::min<long long>(mlav::MAX_NSPLIT, max_blocks));
-  // Bytes one CTA block-step is worth (about 2 us of HBM time at 6 TB/s).
-  const double bytes_per_step = 12e6;
+  // Bytes one block-step is worth (about 2 us of HBM time at 6 TB/s for a
+  // 3.4 us step).
+  const double bytes_per_step = 12e6 * step_us(kernel) / 3.4;
+  const long long slots = pl->num_sms / per_unit;   // units resident at once
   auto best_split = [&](bool with_pack) {
     int best = 1;
     double best_cost = 1e300;
     for (int ns = 1; ns <= cap; ++ns) {
       const long long ctas = units * ns;
-      const double waves = static_cast<double>(ceil_div(ctas, pl->num_sms));
+      const double waves = static_cast<double>(ceil_div(ctas, slots));
       const double steps = static_cast<double>(ceil_div(max_blocks, ns));
       double cost = waves * steps;
-      if (ns > 1) cost += 1.0 + static_cast<double>(units) * kRowsPerTile * ns * 4096.0 / bytes_per_step;
+      if (ns > 1) cost += 1.0 + static_cast<double>(units) * rows * ns * 4096.0 / bytes_per_step;
       if (with_pack) cost += pack_steps(pl, batch, ns, shards);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
@@ -166,15 +199,18 @@ int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel, int shards = 1
   // can win: tree, 4 x 16 row tiles x 16k keys, 278 -> 256 us).  Single-wave
   // choices are kept: beside a running pack the attention blocks take longer
   // than the planner's step, and weighing the pack picked worse splits there.
-  if (kernel == MLA_VERIFY_KERNEL_TC && units * best > pl->num_sms) return best_split(true);
+  if (kernel != MLA_VERIFY_KERNEL_MMA && units * best > slots) return best_split(true);
   return best;
 }
 
-// Forced counts are clamped to the number of key blocks a request can have.
+// Forced counts are clamped to the number of split steps a request can have.
 int effective_nsplit(const mla_verify_plan* pl, int batch, int shards = 1) {
-  if (!pl->forced_nsplit) return auto_nsplit(pl, batch, pl->kernel, shards);
-  return static_cast<int>(std::min<long long>(
-      pl->forced_nsplit, ceil_div(call_keys(pl, shards), keys_per_block(pl->kernel))));
+  const int fam = call_family(pl);
+  if (!pl->forced_nsplit) return auto_nsplit(pl, batch, fam, shards);
+  const long long steps = fam == MLA_VERIFY_KERNEL_PAIR
+                              ? ceil_div(ceil_div(call_keys(pl, shards), 128), 2)
+                              : ceil_div(call_keys(pl, shards), keys_per_block(fam));
+  return static_cast<int>(std::min<long long>(pl->forced_nsplit, steps));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -243,7 +279,7 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
   if (mlav::partial_mma_prepare() != cudaSuccess || mlav::partial_tc_prepare() != cudaSuccess ||
-      mlav::pack_kv_prepare() != cudaSuccess)
+      mlav::partial_pair_prepare() != cudaSuccess || mlav::pack_kv_prepare() != cudaSuccess)
     return MLA_VERIFY_ERR_CUDA;
 
   mla_verify_plan* pl = new (std::nothrow) mla_verify_plan();
@@ -258,14 +294,14 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   pl->max_kv_len = max_kv_len;
   pl->out_dtype = out_dtype;
   pl->num_sms = sms;
-  pl->kernel = MLA_VERIFY_KERNEL_TC;
+  pl->kernel = MLA_VERIFY_KERNEL_PAIR;
 
   // Workspace capacity in request-splits: enough for the automatic choice at
   // every batch size, and for forced split counts up to a 64 MB floor.
   const long long max_blocks = ceil_div(max_kv_len, 64);
   long long cap = 0;
   for (int b = 1; b <= max_batch; ++b)
-    for (int k : {MLA_VERIFY_KERNEL_MMA, MLA_VERIFY_KERNEL_TC})
+    for (int k : {MLA_VERIFY_KERNEL_MMA, MLA_VERIFY_KERNEL_TC, MLA_VERIFY_KERNEL_PAIR})
       cap = std::max<long long>(cap, 1LL * b * auto_nsplit(pl, b, k));
   const long long floor_rs = (64LL << 20) / (1LL * pl->R * (mlav::D_V + 1) * 4);
   cap = std::max(cap, std::min(1LL * max_batch * std::min<long long>(mlav::MAX_NSPLIT, max_blocks),
@@ -291,6 +327,7 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   const size_t packed_bytes =
       static_cast<size_t>(max_batch) * pl->pack_blocks * mlav::packed_block_bytes();
   ok = ok && cudaMalloc(&pl->packed, packed_bytes) == cudaSuccess;
+  ok = ok && mlav::make_pack_maps(&pl->pack_maps, pl->packed, packed_bytes) == cudaSuccess;
   const size_t sync_bytes =
       (mlav::PACK_SYNC_HEADER + static_cast<size_t>(max_batch) * pl->pack_blocks * 32) * sizeof(unsigned);
   ok = ok && cudaMalloc(&pl->pack_sync, sync_bytes) == cudaSuccess;
@@ -347,7 +384,7 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int*
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
   *wide = 0;
   *stay = 0;
-  if (pl->kernel != MLA_VERIFY_KERNEL_TC || gathers_directly(pl)) return MLA_VERIFY_OK;
+  if (pl->kernel == MLA_VERIFY_KERNEL_MMA || gathers_directly(pl)) return MLA_VERIFY_OK;
   mlav::Params p{};
   p.batch = batch;
   p.R = pl->R;
@@ -371,7 +408,7 @@ int mla_verify_plan_set_pack_schedule(mla_verify_plan* pl, int schedule) {
 int mla_verify_plan_get_pack_mode(const mla_verify_plan* pl, int batch) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
-  if (pl->kernel != MLA_VERIFY_KERNEL_TC || gathers_directly(pl)) return MLA_VERIFY_PACK_NONE;
+  if (pl->kernel == MLA_VERIFY_KERNEL_MMA || gathers_directly(pl)) return MLA_VERIFY_PACK_NONE;
   return pack_plan(pl, batch, effective_nsplit(pl, batch), true).mode;
 }
 
@@ -385,15 +422,21 @@ int mla_verify_plan_inject_fault(mla_verify_plan* pl, int fault) {
 int mla_verify_plan_set_kernel(mla_verify_plan* pl, int kernel) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (kernel != MLA_VERIFY_KERNEL_AUTO && kernel != MLA_VERIFY_KERNEL_MMA &&
-      kernel != MLA_VERIFY_KERNEL_TC)
+      kernel != MLA_VERIFY_KERNEL_TC && kernel != MLA_VERIFY_KERNEL_PAIR)
     return MLA_VERIFY_ERR_ARG;
-  pl->kernel = kernel == MLA_VERIFY_KERNEL_AUTO ? MLA_VERIFY_KERNEL_TC : kernel;
+  pl->kernel = kernel == MLA_VERIFY_KERNEL_AUTO ? MLA_VERIFY_KERNEL_PAIR : kernel;
   return MLA_VERIFY_OK;
 }
 
 int mla_verify_plan_get_kernel(const mla_verify_plan* pl) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   return pl->kernel;
+}
+
+int mla_verify_plan_get_call_kernel(const mla_verify_plan* pl, int batch) {
+  if (!pl) return MLA_VERIFY_ERR_NULL;
+  if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
+  return call_family(pl);
 }
 
 int mla_verify_plan_set_profile_events(mla_verify_plan* pl, void* after_pack, void* after_partial) {
@@ -427,6 +470,8 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
     return MLA_VERIFY_ERR_ARG;
   const int dev_status = check_device(pl);
   if (dev_status != MLA_VERIFY_OK) return dev_status;
+  const int fam = call_family(pl);
+  const bool packs = fam != MLA_VERIFY_KERNEL_MMA;   // TC and PAIR read packed key blocks
   const int ns = effective_nsplit(pl, batch, num_shards);
   if (1LL * batch * ns > pl->ws_capacity) return MLA_VERIFY_ERR_SHAPE;
 
@@ -459,12 +504,13 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
   p.packed = static_cast<const uint8_t*>(pl->packed);
   p.packed_max_blocks = pl->pack_blocks;
   p.pack_sync = pl->pack_sync;
+  p.split_pairs = fam == MLA_VERIFY_KERNEL_PAIR ? 1 : 0;
   // Each kernel may start while the one before it finishes (programmatic
   // dependent launch), except when profiling events sit between them: then
   // the kernels run back to back so that each event brackets one kernel.
   const bool overlap = !pl->ev_after_pack && !pl->ev_after_partial;
   cudaError_t le = cudaSuccess;
-  if (pl->kernel == MLA_VERIFY_KERNEL_TC && pl->pack_flags_dirty) {
+  if (packs && pl->pack_flags_dirty) {
     // Zero the flags, keep the epoch and the (reset) ticket: no tag is 0.
     const size_t head = mlav::PACK_SYNC_HEADER * sizeof(unsigned);
     le = cudaMemsetAsync(reinterpret_cast<uint8_t*>(pl->pack_sync) + head, 0, pl->pack_sync_bytes - head, s);
@@ -476,25 +522,26 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
   // One row tile per request: each key block is read by one attention CTA,
   // which gathers it itself instead of going through the pack (which writes
   // every block and reads it back).
-  const bool direct = pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack && gathers_directly(pl);
+  const bool direct = fam == MLA_VERIFY_KERNEL_TC && !skip_pack && gathers_directly(pl);
   bool attn_overlap = overlap;
-  if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && skip_pack) {
+  if (le == cudaSuccess && packs && skip_pack) {
     p.pack_flags = 1;   // injected: nothing sets the flags the attention kernel waits for
   } else if (le == cudaSuccess && direct) {
     p.direct_all = 1;
     attn_overlap = false;   // the first kernel of the call: no programmatic overlap with the last call
-  } else if (le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC) {
+  } else if (le == cudaSuccess && packs) {
     const PackSchedule ps = pack_schedule(pl, p, overlap);
     p.pack_flags = ps.mode != MLA_VERIFY_PACK_WHOLE;
     le = ps.mode == MLA_VERIFY_PACK_IDLE_SMS
              ? mlav::launch_pack_kv_overlap(p, pl->packed, pl->pack_blocks, pl->num_sms, ps.wide, ps.stay, s)
              : mlav::launch_pack_kv(p, pl->packed, pl->pack_blocks, s);
   }
-  const bool packed = le == cudaSuccess && pl->kernel == MLA_VERIFY_KERNEL_TC && !skip_pack && !direct;
+  const bool packed = le == cudaSuccess && packs && !skip_pack && !direct;
   if (le == cudaSuccess && pl->ev_after_pack) le = cudaEventRecord(pl->ev_after_pack, s);
   if (le == cudaSuccess)
-    le = pl->kernel == MLA_VERIFY_KERNEL_MMA ? mlav::launch_partial_mma(p, s)
-                                             : mlav::launch_partial_tc(p, s, attn_overlap);
+    le = fam == MLA_VERIFY_KERNEL_MMA    ? mlav::launch_partial_mma(p, s)
+         : fam == MLA_VERIFY_KERNEL_PAIR ? mlav::launch_partial_pair(p, pl->pack_maps, s, attn_overlap)
+                                         : mlav::launch_partial_tc(p, s, attn_overlap);
   if (packed && le != cudaSuccess) pl->pack_flags_dirty = true;   // the epoch did not advance
   if (le == cudaSuccess && pl->ev_after_partial) le = cudaEventRecord(pl->ev_after_partial, s);
   if (le != cudaSuccess) return MLA_VERIFY_ERR_CUDA;

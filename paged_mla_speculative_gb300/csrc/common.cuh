@@ -58,6 +58,9 @@ struct Params {
   // dealt out evenly over num_shards and the call covers shard `shard` only
   // (0 and 1 for a whole call).
   int shard, num_shards;
+  // 1: splits divide a request's 128-key blocks in pairs (the CTA-pair
+  // kernel works on 256-key pair blocks); 0: block by block.
+  int split_pairs;
   // Workspace row of split s of request b, query row r:
   // b * ws_stride_b + s * ws_stride_s + r (rows of 512 floats / one lse).
   long long ws_stride_b, ws_stride_s;
@@ -110,6 +113,23 @@ __device__ __forceinline__ void split_blocks(const Request& rq, int bn, int spli
   const long long nb = z > a ? z - a : 0;
   kb0 = a + static_cast<int>(nb * split / nsplit);
   kb1 = a + static_cast<int>(nb * (split + 1) / nsplit);
+}
+
+// The 128-key blocks [kb0, kb1) that split `split` takes of the request's
+// range: its blocks divided evenly, or its pairs of blocks when the
+// attention kernel works on pair blocks (a range with an odd block count
+// ends on a lone block).  The pack and the attention kernel both use it, so
+// the pack order follows the order the attention kernel reads blocks in.
+__device__ __forceinline__ void split_range(const Params& p, const Request& rq, int split, int& kb0,
+                                            int& kb1) {
+  if (!p.split_pairs) {
+    split_blocks(rq, 128, split, p.nsplit, kb0, kb1);
+    return;
+  }
+  const int a = rq.lo / 128, z = (rq.hi + 127) / 128;
+  const long long npb = z > a ? (z - a + 1) / 2 : 0;
+  kb0 = a + 2 * static_cast<int>(npb * split / p.nsplit);
+  kb1 = min(z, a + 2 * static_cast<int>(npb * (split + 1) / p.nsplit));
 }
 
 // First workspace row of split s of request b.

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI and the kernels.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (a plain struct; the library does not link the driver)
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -20,6 +21,19 @@ cudaError_t partial_tc_prepare();
 // call's tag (Params::pack_flags = 1), or after griddepcontrol.wait, which
 // waits for the whole pack grid (pack_flags = 0).
 cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap);
+
+// Split-KV partial kernel on CTA pairs (cta_group::2), 128 query rows and
+// 256 keys per step, over the packed blocks (Params::split_pairs = 1);
+// `overlap` as for launch_partial_tc.  The packed buffer is read through two
+// TMA tensor maps (make_pack_maps): rows of 128 bytes, boxes of 256 rows (a
+// chunk pair) and of 128 rows (one chunk).
+struct PackMaps {
+  CUtensorMap pair;    // box 64 x 256 fp16
+  CUtensorMap chunk;   // box 64 x 128 fp16
+};
+cudaError_t make_pack_maps(PackMaps* maps, void* packed, size_t packed_bytes);
+cudaError_t partial_pair_prepare();
+cudaError_t launch_partial_pair(const Params& p, const PackMaps& maps, cudaStream_t stream, bool overlap);
 
 // Per-call gather of the key rows into packed fp16 operand tiles.
 size_t packed_block_bytes();

@@ -136,7 +136,7 @@ __device__ __noinline__ int4 block_info(const Params& p, int q, int max_blocks) 
   const Request rq = load_request(p, b);
   if (!rq.ok) return make_int4(-1, 0, 0, 0);
   int kb0, kb1;   // the attention kernel's division of the call's keys
-  split_blocks(rq, BN, split, p.nsplit, kb0, kb1);
+  split_range(p, rq, split, kb0, kb1);
   const int kb = kb0 + pos;
   if (kb >= kb1) return make_int4(-1, 0, 0, 0);
   return make_int4(b * max_blocks + kb, rq.ip0, kb * BN, rq.hi);
@@ -279,8 +279,10 @@ cudaError_t launch_pack_kv(const Params& p, void* packed, int max_blocks, cudaSt
 
 cudaError_t launch_pack_kv_overlap(const Params& p, void* packed, int max_blocks, int num_ctas,
                                    int wide_positions, int stay, cudaStream_t stream) {
-  // Positions per split: at most ceil(max_blocks / nsplit) blocks.
-  const int per_split = (max_blocks + p.nsplit - 1) / p.nsplit;
+  // Positions per split: at most ceil(max_blocks / nsplit) blocks, or twice
+  // ceil(pairs / nsplit) when splits take pairs of blocks.
+  const int per_split = p.split_pairs ? 2 * (((max_blocks + 1) / 2 + p.nsplit - 1) / p.nsplit)
+                                      : (max_blocks + p.nsplit - 1) / p.nsplit;
   const long long nq = 1LL * p.nsplit * p.batch * per_split;
   if (UNITS_PER_BLOCK * nq > 0x7fffffffLL || stay < 1 || stay >= num_ctas)
     return cudaErrorInvalidConfiguration;

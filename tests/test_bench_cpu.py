@@ -19,6 +19,10 @@ def test_kernel_list_follows_the_pack_schedule():
     assert bench.kernels_of(mb.KERNEL_TC, 1, "whole") == "pack_kv_kernel + partial_tc_kernel"
     assert bench.kernels_of(mb.KERNEL_TC, 3, "none") == "partial_tc_kernel + combine_kernel"
     assert bench.kernels_of(mb.KERNEL_MMA, 3) == "partial_mma_kernel + combine_kernel"
+    assert bench.kernels_of(mb.KERNEL_PAIR, 19, "whole") == \
+        "pack_kv_kernel + partial_pair_kernel + combine_kernel"
+    assert bench.kernels_of(mb.KERNEL_PAIR, 2, "idle_sms") == \
+        "pack_kv_overlap_kernel + partial_pair_kernel + combine_kernel"
 
 
 def test_peaks_fall_back_without_a_measurement(tmp_path, monkeypatch):
@@ -31,18 +35,20 @@ def test_peaks_fall_back_without_a_measurement(tmp_path, monkeypatch):
 
 
 def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch):
-    src_hash = bench.kernel_source_hash()
+    src_hash = bench.kernel_source_hash("partial_pair_kernel")
+    assert src_hash != bench.kernel_source_hash("partial_tc_kernel")
     prof = tmp_path / "profiles"
     prof.mkdir()
     entry = {"workload": "decode_batch", "dram_bytes_per_launch": 123.0, "source_sha1": src_hash}
-    (prof / "traffic.json").write_text(json.dumps({"partial_tc_kernel": entry}))
+    (prof / "traffic.json").write_text(json.dumps({"partial_pair_kernel": entry}))
     # the hash is taken from the real sources; only the traffic file is redirected
     real_root = bench.ROOT
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: src_hash)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel="partial_pair_kernel": src_hash)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.profiled_traffic("decode_batch") == 123.0
-    assert bench.profiled_traffic("tree") is None
+    assert bench.profiled_traffic("decode_batch", "partial_pair_kernel") == 123.0
+    assert bench.profiled_traffic("decode_batch", "partial_tc_kernel") is None
+    assert bench.profiled_traffic("tree", "partial_pair_kernel") is None
     entry["source_sha1"] = "0" * 40
-    (prof / "traffic.json").write_text(json.dumps({"partial_tc_kernel": entry}))
-    assert bench.profiled_traffic("decode_batch") is None
+    (prof / "traffic.json").write_text(json.dumps({"partial_pair_kernel": entry}))
+    assert bench.profiled_traffic("decode_batch", "partial_pair_kernel") is None
     monkeypatch.setattr(bench, "ROOT", real_root)

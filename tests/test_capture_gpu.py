@@ -6,8 +6,8 @@ value into the graph would give the wrong answer.  Every replay must equal
 an eager call on the same buffers bit for bit, and match the oracle.  Each
 key-pack schedule (pack overlapping the attention kernel on idle SMs, whole
 pack first, attention CTAs gathering directly -- automatic with one row tile,
-forced with several), page size 64, bf16 output, the mma.sync family and
-full-size workloads are captured.
+forced with several), page size 64, bf16 output, the CTA-pair and mma.sync
+families and full-size workloads are captured.
 """
 import dataclasses
 
@@ -48,6 +48,9 @@ CASES = {
     "direct_ps64_bf16": (4, 16, 64, torch.bfloat16, mb.KERNEL_TC, 3, mb.PACK_AUTO, mb.PACK_NONE),
     "direct_one_split": (4, 16, 1, torch.float32, mb.KERNEL_TC, 1, mb.PACK_AUTO, mb.PACK_NONE),
     "mma": (8, 16, 1, torch.float32, mb.KERNEL_MMA, 3, mb.PACK_AUTO, mb.PACK_NONE),
+    "pair_idle_sms": (8, 16, 1, torch.float32, mb.KERNEL_PAIR, 4, mb.PACK_IDLE_SMS, mb.PACK_IDLE_SMS),
+    "pair_whole_ps64_bf16": (8, 64, 64, torch.bfloat16, mb.KERNEL_PAIR, 6, mb.PACK_WHOLE, mb.PACK_WHOLE),
+    "pair_auto": (8, 32, 1, torch.float32, mb.KERNEL_AUTO, 0, mb.PACK_AUTO, None),
 }
 
 

@@ -61,7 +61,8 @@ def run_shards(inp, S, kernel=mb.KERNEL_AUTO, out_dtype=torch.float32, check_par
     return out, lse
 
 
-@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_MMA, id="mma")])
+@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_PAIR, id="pair"), pytest.param(mb.KERNEL_TC, id="tc"),
+                                    pytest.param(mb.KERNEL_MMA, id="mma")])
 @pytest.mark.parametrize("S", [1, 2, 3, 7])
 def test_shards_merge_to_the_oracle(kernel, S):
     w = W.Workload(name="cp", batch=3, num_drafts=8, num_heads=16, prefix=(900, 130, 0),

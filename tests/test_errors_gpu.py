@@ -144,14 +144,16 @@ def test_host_entry_point_matches_device_entry_point():
     assert torch.equal(out, o_dev.cpu()) and torch.equal(lse, l_dev.cpu())
 
 
+@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_PAIR, id="pair"), pytest.param(mb.KERNEL_TC, id="tc")])
 @pytest.mark.parametrize("nsplit", [1, 2])
-def test_bounded_wait_runs_out_and_reports_timeout(nsplit):
+def test_bounded_wait_runs_out_and_reports_timeout(nsplit, kernel):
     """Fault injected on the host: the attention kernel waits for ready flags
     that nothing sets.  Every wait gives up after its cycle limit (about a
     second): the rows are NaN, the status word reports the timeout, and the
     context stays usable -- the next call is correct."""
-    inp = _case(seed=7, prefix=(300, 77))
-    with G.make_plan(inp, nsplit=nsplit) as plan:
+    inp = _case(seed=7, prefix=(300, 77), num_heads=32)
+    with G.make_plan(inp, nsplit=nsplit, kernel=kernel) as plan:
+        assert plan.call_kernel(inp.workload.batch) == kernel
         plan.inject_fault(mb.FAULT_SKIP_PACK)
         out, lse = G.run(plan, inp)
         assert plan.get_error() & mb.DEV_TIMEOUT
@@ -170,13 +172,13 @@ def test_unknown_fault_is_rejected():
 
 
 @pytest.mark.parametrize("where", ["key", "query"])
-@pytest.mark.parametrize("mode", ["packed", "direct", "mma"])
+@pytest.mark.parametrize("mode", ["pair", "packed", "direct", "mma"])
 def test_value_outside_fp16_range_sets_the_range_bit(where, mode):
     """A bf16 value of 1e5 has no fp16 counterpart: the kernel that widens it
     reports MLA_VERIFY_DEV_RANGE; an unaffected call leaves the bit clear."""
     H = 16 if mode == "direct" else 32          # one 64-row tile -> direct gather
     inp = _case(seed=40, num_heads=H, tree="chain")
-    kernel = mb.KERNEL_MMA if mode == "mma" else mb.KERNEL_TC
+    kernel = {"mma": mb.KERNEL_MMA, "pair": mb.KERNEL_PAIR}.get(mode, mb.KERNEL_TC)
     with G.make_plan(inp, kernel=kernel) as plan:
         G.run(plan, inp)
         assert plan.get_error() == 0

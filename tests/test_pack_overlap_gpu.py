@@ -31,32 +31,53 @@ def _sms():
 
 
 def _attention_ctas(plan, batch, rows):
+    if plan.call_kernel(batch) == mb.KERNEL_PAIR:
+        return plan.nsplit(batch) * ((rows + 127) // 128) * batch * 2
     return plan.nsplit(batch) * ((rows + 63) // 64) * batch
 
 
-def test_decode_batch_shape_overlaps():
-    """8 requests x 512 rows x 4104 keys: the attention grid leaves SMs idle,
-    so the pack keeps those and packs only the leading positions first."""
+def _positions(plan, batch, blocks):
+    """Block positions per split: one per 128-key block, or two per pair
+    block when the splits take pairs of blocks."""
+    ns = plan.nsplit(batch)
+    if plan.call_kernel(batch) == mb.KERNEL_PAIR:
+        return 2 * (-(-(-(-blocks // 2)) // ns))
+    return -(-blocks // ns)
+
+
+@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_PAIR, id="pair")])
+def test_decode_batch_shape_schedule(kernel):
+    """8 requests x 512 rows x 4104 keys.  The pack either runs whole first
+    (stay 0, every position wide) or keeps the SMs the attention grid leaves
+    idle and packs only the leading positions first.  The single-SM family
+    leaves enough SMs idle for the second; the pair family's split steps
+    take two blocks each, and the planner runs the whole pack first."""
     plan = mb.Plan(8, 8, 64, 1, 65536, 4104)
+    plan.set_kernel(kernel)
+    assert plan.call_kernel(8) == kernel
     wide, stay = plan.pack_schedule(8)
     idle = _sms() - _attention_ctas(plan, 8, 512)
-    positions = -(-33 // plan.nsplit(8))
-    if idle < 16:
-        assert stay == 0 and wide == positions
+    positions = _positions(plan, 8, 33)
+    if stay == 0:
+        assert wide == positions
     else:
-        assert stay == idle
+        assert stay == idle and idle >= 16
         assert 1 <= wide and 2 * wide <= positions
+    if kernel == mb.KERNEL_TC and idle >= 16:
+        assert stay == idle
     plan.set_kernel(mb.KERNEL_MMA)
     assert plan.pack_schedule(8) == (0, 0)
     plan.close()
 
 
-def test_overlapping_pack_repeated_calls():
+@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_PAIR, id="pair")])
+def test_overlapping_pack_repeated_calls(kernel):
     w = W.Workload(name="ov", batch=4, num_drafts=8, num_heads=64, prefix=(1500, 900, 2000, 33),
                    tree="random", num_slots=8192, spike_frac=0.01, seed=610)
     inp = W.make_inputs(w)
     g = G.to_cuda(inp)
-    with G.make_plan(g) as plan:
+    with G.make_plan(g, kernel=kernel) as plan:
+        plan.set_pack_schedule(mb.PACK_IDLE_SMS)
         wide, stay = plan.pack_schedule(4)
         assert stay > 0, (wide, stay)
         first = None
@@ -71,7 +92,8 @@ def test_overlapping_pack_repeated_calls():
     G.assert_parity(first[0].cpu().numpy(), first[1].cpu().numpy(), ref_o, ref_l)
 
 
-def test_overlapping_pack_new_data_each_call():
+@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_PAIR, id="pair")])
+def test_overlapping_pack_new_data_each_call(kernel):
     """Same buffers, different keys and lengths every call: a block packed by
     the previous call must never be read as this call's."""
     cases = [W.make_inputs(W.Workload(name="ovd", batch=3, num_drafts=4, num_heads=32,
@@ -86,7 +108,9 @@ def test_overlapping_pack_new_data_each_call():
     lens = torch.empty(3, dtype=torch.int32, device=dev)
     par = torch.empty((3, 4), dtype=torch.int32, device=dev)
     plan = mb.Plan(3, 4, 32, 1, 8192, 1904)
-    plan.set_nsplit(2)   # 8 block positions per split: the overlapping schedule
+    plan.set_kernel(kernel)
+    plan.set_nsplit(2)
+    plan.set_pack_schedule(mb.PACK_IDLE_SMS)
     assert plan.pack_schedule(3)[1] > 0
     for c in cases + cases[::-1]:
         q.copy_(c.q)
@@ -113,8 +137,8 @@ def test_whole_pack_when_no_sm_is_idle():
     g = G.to_cuda(inp)
     with G.make_plan(g, nsplit=1) as plan:
         wide, stay = plan.pack_schedule(batch)
-        if _sms() - batch * tiles < 16:
-            assert stay == 0 and wide == 1
+        if _sms() - _attention_ctas(plan, batch, 512) < 16:
+            assert stay == 0 and wide == _positions(plan, batch, 1)
         out, lse = G.run(plan, g)
         assert plan.get_error() == 0
     ref_o, ref_l = G.oracle_full(inp)
@@ -139,18 +163,21 @@ def test_profiling_events_use_the_whole_pack():
 
 @pytest.mark.parametrize("page_size,out_dtype", [(64, torch.float32), (1, torch.bfloat16),
                                                  (64, torch.bfloat16)])
-def test_overlapping_pack_pages_and_bf16(page_size, out_dtype):
+@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_PAIR, id="pair")])
+def test_overlapping_pack_pages_and_bf16(page_size, out_dtype, kernel):
     """The overlapping schedule with a 64-row page table and with bf16 output
     (bf16 must equal the fp32 result rounded)."""
     w = W.Workload(name="ovp", batch=4, num_drafts=8, num_heads=64, prefix=(1500, 900, 2000, 33),
                    tree="random", num_slots=16384, page_size=page_size, spike_frac=0.01, seed=640)
     inp = W.make_inputs(w)
     g = G.to_cuda(inp)
-    with G.make_plan(g, out_dtype=out_dtype) as plan:
+    with G.make_plan(g, out_dtype=out_dtype, kernel=kernel) as plan:
+        plan.set_pack_schedule(mb.PACK_IDLE_SMS)
         assert plan.pack_schedule(4)[1] > 0
         out, lse = G.run(plan, g)
         assert plan.get_error() == 0
-    with G.make_plan(g) as plan32:
+    with G.make_plan(g, kernel=kernel) as plan32:
+        plan32.set_pack_schedule(mb.PACK_IDLE_SMS)
         o32, l32 = G.run(plan32, g)
     if out_dtype == torch.bfloat16:
         assert torch.equal(out, o32.to(torch.bfloat16)) and torch.equal(lse, l32)

@@ -44,7 +44,8 @@ def check_full(inp, **plan_kw):
     return G.assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
 
 
-KERNELS = [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_MMA, id="mma")]
+KERNELS = [pytest.param(mb.KERNEL_PAIR, id="pair"), pytest.param(mb.KERNEL_TC, id="tc"),
+           pytest.param(mb.KERNEL_MMA, id="mma")]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
