@@ -99,7 +99,9 @@ extern "C" {
 #define MLA_VERIFY_OUT_F32            0
 #define MLA_VERIFY_OUT_BF16           1
 
-/* Kernel family for the partial (split-KV) step; AUTO = PAIR. */
+/* Kernel family for the partial (split-KV) step.  AUTO picks TC or PAIR per
+ * call from the plan's shape and the batch (TC's smaller fixed cost for short
+ * contexts, PAIR's faster steps for long ones). */
 #define MLA_VERIFY_KERNEL_AUTO        0
 #define MLA_VERIFY_KERNEL_MMA         1   /* warp-level mma.sync, O in registers   */
 #define MLA_VERIFY_KERNEL_TC          2   /* tcgen05 MMAs on one SM, 64 query rows
@@ -181,12 +183,11 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* plan, int batch, in
 int mla_verify_plan_set_pack_schedule(mla_verify_plan* plan, int schedule);
 int mla_verify_plan_get_pack_mode(const mla_verify_plan* plan, int batch);
 
-/* Select the partial-kernel family (MLA_VERIFY_KERNEL_*; AUTO = PAIR). */
+/* Select the partial-kernel family (MLA_VERIFY_KERNEL_*; the default is AUTO). */
 int mla_verify_plan_set_kernel(mla_verify_plan* plan, int kernel);
 
-/* The kernel family selected (AUTO resolved to PAIR), or < 0.  A PAIR plan
- * whose calls gather directly (see MLA_VERIFY_KERNEL_PAIR) runs the TC
- * kernel: mla_verify_plan_get_call_kernel reports which. */
+/* The kernel family selected (possibly AUTO), or < 0.  The kernel a call
+ * actually launches is reported by mla_verify_plan_get_call_kernel. */
 int mla_verify_plan_get_kernel(const mla_verify_plan* plan);
 /* The partial kernel a call with `batch` requests launches: MLA_VERIFY_KERNEL_
  * MMA, TC or PAIR, or < 0 (null plan, batch outside [1, max_batch]). */

@@ -76,13 +76,22 @@ int keys_per_block(int kernel) {
 // its CTAs.
 int rows_per_unit(int kernel) { return kernel == MLA_VERIFY_KERNEL_PAIR ? 128 : kRowsPerTile; }
 int ctas_per_unit(int kernel) { return kernel == MLA_VERIFY_KERNEL_PAIR ? 2 : 1; }
-// Measured time of one split step on GB300 (us): a 128-key block of a TC CTA,
-// a 256-key pair block of a PAIR cluster.
-double step_us(int kernel) { return kernel == MLA_VERIFY_KERNEL_PAIR ? 3.0 : 3.4; }
+// Measured on GB300 (us): one split step (a 128-key block of a TC CTA, a
+// 256-key pair block of a PAIR cluster) and a CTA's fixed cost (prologue,
+// pipeline fill, epilogue), from the attention kernel's time over contexts
+// of 1k to 93k keys.
+double step_us(int kernel) { return kernel == MLA_VERIFY_KERNEL_PAIR ? 4.8 : 3.4; }
+double fixed_us(int kernel) { return kernel == MLA_VERIFY_KERNEL_PAIR ? 20.0 : 16.0; }
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 constexpr long long kDirectMaxTiles = 1;   // 2 tiles measured slower (each block gathered twice)
+
+// The attention CTAs gather their own key blocks (no pack): one row tile per
+// request, or forced.
+bool gathers_directly(const mla_verify_plan* pl) {
+  return pl->pack_mode == MLA_VERIFY_PACK_NONE || ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles;
+}
 
 // Pack schedule (see pack_kv.cu).  When the kernels may overlap and the
 // attention grid leaves at least kMinPackSms SMs idle, the two-phase pack:
@@ -90,7 +99,7 @@ constexpr long long kDirectMaxTiles = 1;   // 2 tiles measured slower (each bloc
 // others first pack the `wide` leading block positions of every split.
 // `wide` is the fewest positions that keep the narrow phase ahead of the
 // attention kernel, from rates measured on GB300: ~0.15 blocks/us per
-// packing SM, one 128-key block per ~3.4 us per attention CTA, ~5 us before
+// packing SM, one split step per step_us per attention unit, ~5 us before
 // its first block.  When that needs more than half the positions, or
 // otherwise, the whole pack runs first (stay = 0).
 struct PackSchedule {
@@ -98,9 +107,8 @@ struct PackSchedule {
   int wide, stay;
 };
 constexpr int kMinPackSms = 16;
-int call_family(const mla_verify_plan* pl);
-PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool overlap, int shards = 1) {
-  const int fam = call_family(pl);
+PackSchedule pack_plan(const mla_verify_plan* pl, int fam, int batch, int nsplit, bool overlap,
+                       int shards = 1) {
   const bool pairs = fam == MLA_VERIFY_KERNEL_PAIR;
   // Block positions per split (pairs of positions when splits take pairs).
   const long long shard_blocks = ceil_div(pl->pack_blocks, shards);
@@ -126,33 +134,15 @@ PackSchedule pack_plan(const mla_verify_plan* pl, int batch, int nsplit, bool ov
   return PackSchedule{MLA_VERIFY_PACK_IDLE_SMS, std::min(wide, positions), static_cast<int>(idle)};
 }
 
-PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, bool overlap) {
-  return pack_plan(pl, p.batch, p.nsplit, overlap, p.num_shards);
-}
-
-// The attention CTAs gather their own key blocks (no pack): one row tile per
-// request, or forced.
-bool gathers_directly(const mla_verify_plan* pl) {
-  return pl->pack_mode == MLA_VERIFY_PACK_NONE || ceil_div(pl->R, kRowsPerTile) <= kDirectMaxTiles;
-}
-
-// The partial kernel calls launch: the PAIR family falls back to the TC
-// kernel's direct gather when there is no pack.
-int call_family(const mla_verify_plan* pl) {
-  if (pl->kernel == MLA_VERIFY_KERNEL_PAIR && gathers_directly(pl)) return MLA_VERIFY_KERNEL_TC;
-  return pl->kernel;
-}
-
-// What the pack leaves on a call's critical path, in attention block steps
-// (~3.4 us): the wide phase (~9 us) when it overlaps, else the whole gather
-// of up to batch x max_kv_len rows (1152 B read + 1152 B written each at
-// ~4.5 TB/s, plus ~3 us); nothing when the attention CTAs gather directly.
-double pack_steps(const mla_verify_plan* pl, int batch, int nsplit, int shards) {
-  if (gathers_directly(pl)) return 0.0;
-  const double st = step_us(call_family(pl));
-  const PackSchedule ps = pack_plan(pl, batch, nsplit, true, shards);
-  if (ps.mode != MLA_VERIFY_PACK_WHOLE) return 9.0 / st;
-  return (2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0) / st;
+// What the pack leaves on a call's critical path (us): the wide phase
+// (~9 us) when it overlaps, else the whole gather of up to batch x
+// max_kv_len rows (1152 B read + 1152 B written each at ~4.5 TB/s, plus
+// ~3 us); nothing when the attention CTAs gather directly.
+double pack_us(const mla_verify_plan* pl, int fam, int batch, int nsplit, int shards) {
+  if (fam == MLA_VERIFY_KERNEL_MMA || gathers_directly(pl)) return 0.0;
+  const PackSchedule ps = pack_plan(pl, fam, batch, nsplit, true, shards);
+  if (ps.mode != MLA_VERIFY_PACK_WHOLE) return 9.0;
+  return 2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0;
 }
 
 // Keys a request can hold in a call covering one of `shards` shards: a
@@ -161,31 +151,37 @@ long long call_keys(const mla_verify_plan* pl, int shards) {
   return std::min<long long>(pl->max_kv_len, ceil_div(ceil_div(pl->max_kv_len, 128), shards) * 128);
 }
 
-// Split count for `batch` requests: minimise (waves of CTAs) x (key blocks
-// per CTA) plus the cost of moving the split partials through the combine,
-// in units of one CTA key-block step.
+// Split steps a request can have: pair blocks of a range with an odd block
+// count may hold one block.
+long long max_steps(const mla_verify_plan* pl, int kernel, int shards) {
+  return kernel == MLA_VERIFY_KERNEL_PAIR ? ceil_div(ceil_div(call_keys(pl, shards), 128), 2)
+                                          : ceil_div(call_keys(pl, shards), keys_per_block(kernel));
+}
+
+// Moving the split partials through the combine (us): a launch, and the
+// partials' bytes at ~3.5 TB/s.
+double combine_us(const mla_verify_plan* pl, int kernel, int batch, int ns) {
+  if (ns <= 1) return 0.0;
+  const double units = static_cast<double>(batch) * ceil_div(pl->R, rows_per_unit(kernel));
+  return 3.4 + units * rows_per_unit(kernel) * ns * 4096.0 / 3.5e6;
+}
+
+// Split count for `batch` requests: minimise (waves of units) x (steps per
+// unit) plus the combine, in units of one split step.
 int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel, int shards = 1) {
-  const int rows = rows_per_unit(kernel), per_unit = ctas_per_unit(kernel);
-  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, rows);
-  // A pair block of a range with an odd block count may hold one block.
-  const long long max_blocks = kernel == MLA_VERIFY_KERNEL_PAIR
-                                   ? ceil_div(ceil_div(call_keys(pl, shards), 128), 2)
-                                   : ceil_div(call_keys(pl, shards), keys_per_block(kernel));
-  const int cap = static_cast<int>(std::min<long long>(mlav::MAX_NSPLIT, max_blocks));
-  // Bytes one block-step is worth (about 2 us of HBM time at 6 TB/s for a
-  // 3.4 us step).
-  const double bytes_per_step = 12e6 * step_us(kernel) / 3.4;
-  const long long slots = pl->num_sms / per_unit;   // units resident at once
+  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, rows_per_unit(kernel));
+  const long long steps_max = max_steps(pl, kernel, shards);
+  const int cap = static_cast<int>(std::min<long long>(mlav::MAX_NSPLIT, steps_max));
+  const long long slots = pl->num_sms / ctas_per_unit(kernel);   // units resident at once
+  const double st = step_us(kernel);
   auto best_split = [&](bool with_pack) {
     int best = 1;
     double best_cost = 1e300;
     for (int ns = 1; ns <= cap; ++ns) {
-      const long long ctas = units * ns;
-      const double waves = static_cast<double>(ceil_div(ctas, slots));
-      const double steps = static_cast<double>(ceil_div(max_blocks, ns));
-      double cost = waves * steps;
-      if (ns > 1) cost += 1.0 + static_cast<double>(units) * rows * ns * 4096.0 / bytes_per_step;
-      if (with_pack) cost += pack_steps(pl, batch, ns, shards);
+      const double waves = static_cast<double>(ceil_div(units * ns, slots));
+      const double steps = static_cast<double>(ceil_div(steps_max, ns));
+      double cost = waves * steps + combine_us(pl, kernel, batch, ns) / st;
+      if (with_pack) cost += pack_us(pl, kernel, batch, ns, shards) / st;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best = ns;
@@ -204,13 +200,45 @@ int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel, int shards = 1
 }
 
 // Forced counts are clamped to the number of split steps a request can have.
-int effective_nsplit(const mla_verify_plan* pl, int batch, int shards = 1) {
-  const int fam = call_family(pl);
+int family_nsplit(const mla_verify_plan* pl, int fam, int batch, int shards) {
   if (!pl->forced_nsplit) return auto_nsplit(pl, batch, fam, shards);
-  const long long steps = fam == MLA_VERIFY_KERNEL_PAIR
-                              ? ceil_div(ceil_div(call_keys(pl, shards), 128), 2)
-                              : ceil_div(call_keys(pl, shards), keys_per_block(fam));
-  return static_cast<int>(std::min<long long>(pl->forced_nsplit, steps));
+  return static_cast<int>(std::min<long long>(pl->forced_nsplit, max_steps(pl, fam, shards)));
+}
+
+// Estimated time (us) of a call of family `fam`: waves of units, each its
+// fixed cost plus its split steps, then the combine and what the pack leaves
+// on the critical path.
+double call_estimate_us(const mla_verify_plan* pl, int fam, int batch, int shards) {
+  const int ns = family_nsplit(pl, fam, batch, shards);
+  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, rows_per_unit(fam));
+  const double waves = static_cast<double>(ceil_div(units * ns, pl->num_sms / ctas_per_unit(fam)));
+  const double steps = static_cast<double>(ceil_div(max_steps(pl, fam, shards), ns));
+  return waves * (fixed_us(fam) + steps * step_us(fam)) + combine_us(pl, fam, batch, ns) +
+         pack_us(pl, fam, batch, ns, shards);
+}
+
+// The partial kernel a call launches.  One row tile per request, or no
+// pack: the TC kernel's direct gather (PAIR always reads packed blocks).
+// AUTO: the TC or PAIR kernel, whichever call_estimate_us expects faster
+// (short contexts favour TC's smaller fixed cost, long ones PAIR's faster
+// steps).
+int call_family(const mla_verify_plan* pl, int batch, int shards = 1) {
+  if (pl->kernel == MLA_VERIFY_KERNEL_MMA) return MLA_VERIFY_KERNEL_MMA;
+  if (gathers_directly(pl)) return MLA_VERIFY_KERNEL_TC;
+  if (pl->kernel != MLA_VERIFY_KERNEL_AUTO) return pl->kernel;
+  return call_estimate_us(pl, MLA_VERIFY_KERNEL_TC, batch, shards) <=
+                 call_estimate_us(pl, MLA_VERIFY_KERNEL_PAIR, batch, shards)
+             ? MLA_VERIFY_KERNEL_TC
+             : MLA_VERIFY_KERNEL_PAIR;
+}
+
+int effective_nsplit(const mla_verify_plan* pl, int batch, int shards = 1) {
+  return family_nsplit(pl, call_family(pl, batch, shards), batch, shards);
+}
+
+PackSchedule pack_schedule(const mla_verify_plan* pl, const mlav::Params& p, bool overlap) {
+  return pack_plan(pl, p.split_pairs ? MLA_VERIFY_KERNEL_PAIR : MLA_VERIFY_KERNEL_TC, p.batch, p.nsplit,
+                   overlap, p.num_shards);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -294,7 +322,7 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   pl->max_kv_len = max_kv_len;
   pl->out_dtype = out_dtype;
   pl->num_sms = sms;
-  pl->kernel = MLA_VERIFY_KERNEL_PAIR;
+  pl->kernel = MLA_VERIFY_KERNEL_AUTO;
 
   // Workspace capacity in request-splits: enough for the automatic choice at
   // every batch size, and for forced split counts up to a 64 MB floor.
@@ -385,12 +413,8 @@ int mla_verify_plan_get_pack_schedule(const mla_verify_plan* pl, int batch, int*
   *wide = 0;
   *stay = 0;
   if (pl->kernel == MLA_VERIFY_KERNEL_MMA || gathers_directly(pl)) return MLA_VERIFY_OK;
-  mlav::Params p{};
-  p.batch = batch;
-  p.R = pl->R;
-  p.nsplit = effective_nsplit(pl, batch);
-  p.num_shards = 1;
-  const PackSchedule ps = pack_schedule(pl, p, true);
+  const int fam = call_family(pl, batch);
+  const PackSchedule ps = pack_plan(pl, fam, batch, family_nsplit(pl, fam, batch, 1), true);
   *wide = ps.wide;
   *stay = ps.stay;
   return MLA_VERIFY_OK;
@@ -409,7 +433,8 @@ int mla_verify_plan_get_pack_mode(const mla_verify_plan* pl, int batch) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
   if (pl->kernel == MLA_VERIFY_KERNEL_MMA || gathers_directly(pl)) return MLA_VERIFY_PACK_NONE;
-  return pack_plan(pl, batch, effective_nsplit(pl, batch), true).mode;
+  const int fam = call_family(pl, batch);
+  return pack_plan(pl, fam, batch, family_nsplit(pl, fam, batch, 1), true).mode;
 }
 
 int mla_verify_plan_inject_fault(mla_verify_plan* pl, int fault) {
@@ -424,7 +449,7 @@ int mla_verify_plan_set_kernel(mla_verify_plan* pl, int kernel) {
   if (kernel != MLA_VERIFY_KERNEL_AUTO && kernel != MLA_VERIFY_KERNEL_MMA &&
       kernel != MLA_VERIFY_KERNEL_TC && kernel != MLA_VERIFY_KERNEL_PAIR)
     return MLA_VERIFY_ERR_ARG;
-  pl->kernel = kernel == MLA_VERIFY_KERNEL_AUTO ? MLA_VERIFY_KERNEL_PAIR : kernel;
+  pl->kernel = kernel;
   return MLA_VERIFY_OK;
 }
 
@@ -436,7 +461,7 @@ int mla_verify_plan_get_kernel(const mla_verify_plan* pl) {
 int mla_verify_plan_get_call_kernel(const mla_verify_plan* pl, int batch) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
   if (batch < 1 || batch > pl->max_batch) return MLA_VERIFY_ERR_BATCH;
-  return call_family(pl);
+  return call_family(pl, batch);
 }
 
 int mla_verify_plan_set_profile_events(mla_verify_plan* pl, void* after_pack, void* after_partial) {
@@ -470,9 +495,9 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
     return MLA_VERIFY_ERR_ARG;
   const int dev_status = check_device(pl);
   if (dev_status != MLA_VERIFY_OK) return dev_status;
-  const int fam = call_family(pl);
+  const int fam = call_family(pl, batch, num_shards);
   const bool packs = fam != MLA_VERIFY_KERNEL_MMA;   // TC and PAIR read packed key blocks
-  const int ns = effective_nsplit(pl, batch, num_shards);
+  const int ns = family_nsplit(pl, fam, batch, num_shards);
   if (1LL * batch * ns > pl->ws_capacity) return MLA_VERIFY_ERR_SHAPE;
 
   Params p{};
