@@ -78,7 +78,6 @@ constexpr int OFF_P = OFF_Q + 9 * Q_CHUNK;            // P^T [key half][128 keys
 constexpr int OFF_RING = OFF_P + 2 * CHUNK;
 constexpr int OFF_ROPE = OFF_RING + NSLOT * 2 * CHUNK;   // the rope chunk's own slot
 constexpr int OFF_RING_END = OFF_ROPE + CHUNK;
-constexpr int OFF_STAGE = OFF_P;                      // epilogue: [128 rows][256 dims] fp32
 constexpr int OFF_RED = OFF_RING_END;                 // float [128 rows][4 quads]
 constexpr int OFF_XMAX = OFF_RED + ROWS * 4 * 4;      // float [2][128] the peer's block row max
 constexpr int OFF_XSUM = OFF_XMAX + 2 * ROWS * 4;     // float [128] the peer's row sums
@@ -96,7 +95,6 @@ constexpr int SMEM_TOTAL = OFF_MISC + 16;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_P % 1024 == 0 && OFF_RING % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
-static_assert(ROWS * 256 * 4 <= OFF_RING_END - OFF_STAGE, "epilogue staging fits in P and the ring");
 
 // mbarrier indices (same offsets in both CTAs)
 constexpr int MB_FULL = 0;     // [3] even CTA: ring slot landed in both CTAs (bytes of both)
@@ -309,6 +307,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   }
 
+  // The draft parents load alongside the request lookup (independent
+  // global loads, each a memory latency).
+  if (tid < p.T) s_par[tid] = p.draft_parent[b * p.T + tid];
   // Both CTAs of the pair see the same request and take the same branches
   // up to the pair's first cluster barrier.
   const Request rq = load_request(p, b);
@@ -326,7 +327,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   split_range(p, rq, split, kb0, kb1);
   const int nb = (kb1 - kb0 + 1) >> 1;   // pair blocks; the last may hold one block
 
-  if (tid < p.T) s_par[tid] = p.draft_parent[b * p.T + tid];
   if (tid < ROWS) s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
   if (tid == 0) {
     for (int i = 0; i < NSLOT; ++i) {
@@ -744,54 +744,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
   }
 
-  // ---- normalised O out of TMEM: thread = value dim, staged [row][256
-  // dims of this CTA] in the idle P/ring area, then two bulk stores a row.
+  // ---- normalised O out of TMEM, thread = value dim, stored straight from
+  // registers: each warp store covers 32 consecutive dims of one row (128
+  // contiguous bytes of fp32).  Staging the tile in shared memory for 512-byte
+  // bulk stores measured ~4 us per CTA, against ~1 us for these stores.
   tc::fence_before_sync();
   __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   tc::fence_after_sync();
   if (*s_abort != 0) {
     write_nan_rows(p, b, split, row0, rank, tid);
-  } else {
-    const int nrows = min(ROWS, p.R - row0);
+  } else if (warp < SOFTMAX_WARPS) {
     const bool out16 = p.nsplit == 1 && p.out_bf16;
-    uint8_t* stage = smem + OFF_STAGE;
-    if (warp < SOFTMAX_WARPS) {
-      const int c0 = grp * 32;
+    const int c0 = grp * 32;
+    const size_t ws_row = ws_base(p, b, split);
 #pragma unroll 1
-      for (int t = 0; t < 2; ++t) {
-        uint32_t v[32];
-        if (nb > 0) {
-          tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + 128u * t + c0, v);
-          tc::tmem_wait_ld();
-        }
-        const int dl = t * 128 + quad * 32 + lane;   // local dim 0..255
+    for (int t = 0; t < 2; ++t) {
+      uint32_t v[32];
+      if (nb > 0) {
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + 128u * t + c0, v);
+        tc::tmem_wait_ld();
+      }
+      const int dim = t * 256 + static_cast<int>(rank) * 128 + quad * 32 + lane;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int r = c0 + c;
-          const float inv = s_l[r];
-          const float o = (inv > 0.f && nb > 0) ? __uint_as_float(v[c]) * inv : 0.f;
-          if (out16) reinterpret_cast<__nv_bfloat16*>(stage)[r * 256 + dl] = __float2bfloat16_rn(o);
-          else reinterpret_cast<float*>(stage)[r * 256 + dl] = o;
+      for (int c = 0; c < 32; ++c) {
+        const int r = c0 + c, gr = row0 + r;
+        if (gr >= p.R) continue;   // rows past R (warp-uniform)
+        const float inv = s_l[r];
+        const float o = (inv > 0.f && nb > 0) ? __uint_as_float(v[c]) * inv : 0.f;
+        if (p.nsplit > 1) {
+          p.ws_o[(ws_row + gr) * D_V + dim] = o;
+        } else {
+          const size_t e = (static_cast<size_t>(b) * p.R + gr) * D_V + dim;
+          if (out16) reinterpret_cast<__nv_bfloat16*>(p.out)[e] = __float2bfloat16_rn(o);
+          else reinterpret_cast<float*>(p.out)[e] = o;
         }
       }
-      tc::fence_async_smem();
-    }
-    __syncthreads();
-    if (warp < 8) {
-      const uint32_t seg = out16 ? 128 * 2 : 128 * 4;   // bytes of 128 dims
-      for (int e = tid; e < 2 * nrows; e += 256) {
-        const int r = e >> 1, t = e & 1;
-        const int d0 = t * 256 + static_cast<int>(rank) * 128;
-        const size_t grow = static_cast<size_t>(b) * p.R + row0 + r;
-        void* dst = p.nsplit == 1
-                        ? static_cast<void*>(static_cast<uint8_t*>(p.out) + (grow * D_V + d0) * (out16 ? 2 : 4))
-                        : static_cast<void*>(p.ws_o + (ws_base(p, b, split) + row0 + r) * D_V + d0);
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
-                     "r"(sbase + OFF_STAGE + r * 2 * seg + t * seg), "r"(seg)
-                     : "memory");
-      }
-      asm volatile("cp.async.bulk.commit_group;\ncp.async.bulk.wait_group 0;\n" ::: "memory");
     }
   }
   tc::fence_before_sync();
