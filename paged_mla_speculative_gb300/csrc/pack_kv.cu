@@ -23,16 +23,19 @@
 //    attention kernel, whose copy warp waits for it with griddepcontrol.wait.
 //  * pack_kv_overlap_kernel: when the attention grid leaves SMs idle
 //    (decode batches: 128 attention CTAs on 152 SMs), a persistent grid of
-//    1024-thread CTAs, one per SM, in two phases: the CTAs beyond the idle
+//    one 512-thread CTA per SM, in two phases: the CTAs beyond the idle
 //    count pack the first block positions of every split and exit -- their
 //    SMs take the attention CTAs (programmatic dependent launch) -- while
 //    the others pack the rest on the idle SMs as the attention kernel runs.
-//    Each warp packs 4-key units and publishes every unit with a release
-//    store of this call's tag (epoch + 1) into pack_sync, 32 flags per
-//    block, which the attention kernel's copy warp waits for block by block.
-//    Units run in split-position order (the i-th block of every (request,
-//    split) before any (i+1)-th), so every attention CTA finds its next
-//    block packed while it works on the last.
+//    Each warp packs 4-key units through three shared-memory stages (16-byte
+//    cp.async of the unit's rows, so two units' loads stay in flight while
+//    it widens and stores the third, without registers held per load) and
+//    publishes every unit with a release store of this call's tag (epoch +
+//    1) into pack_sync, 32 flags per block, which the attention kernel's
+//    copy warp waits for block by block.  Units run in split-position order
+//    (the i-th block of every (request, split) before any (i+1)-th), so
+//    every attention CTA finds its next block packed while it works on the
+//    last.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -45,7 +48,6 @@ namespace {
 
 constexpr int BN = 128;
 constexpr int NTHREADS = 256;           // pack_kv_kernel
-constexpr int OV_THREADS = 1024;        // pack_kv_overlap_kernel
 constexpr int BLOCK_BYTES = 9 * BN * 128;
 
 // The key rows are read exactly once per call: load them past L1 and mark
@@ -114,13 +116,20 @@ __global__ void __launch_bounds__(NTHREADS) pack_kv_kernel(const Params p, uint8
 
 constexpr int UNIT_KEYS = 4;                        // keys per warp unit
 constexpr int UNITS_PER_BLOCK = BN / UNIT_KEYS;     // 32: one ready flag each
-constexpr int PER_LANE = ROW_CHUNKS / 8;               // 9 granules per lane (8 lanes per key)
+constexpr int PER_LANE = ROW_CHUNKS / 8;            // 9 granules per lane (8 lanes per key)
 static_assert(UNIT_KEYS * 8 == 32 && PER_LANE * 8 == ROW_CHUNKS, "8 lanes per key");
 static_assert(UNITS_PER_BLOCK == 32, "one flag per lane of the reader's warp");
 
-// Packed blocks whose descriptions every pack CTA tabulates in shared memory
-// (16 bytes each); larger calls describe each block as they reach it.
-constexpr int TABLE_BLOCKS = 12288;
+// pack_kv_overlap_kernel: warps per CTA and units staged per warp.  Sixteen
+// warps of three stages fill shared memory; measured on GB300 (the narrow
+// phase alone, 93k scattered keys): ~31 GB/s of rows read per SM, against
+// ~23 with the units held in registers.  Fewer warps with deeper stages were
+// slower: every unit's publication waits for the warp's outstanding memory
+// operations, so the parallel warps, not the depth, carry the throughput.
+constexpr int OV_WARPS = 16;
+constexpr int OV_DEPTH = 3;
+constexpr int UNIT_BYTES = UNIT_KEYS * ROW_BYTES;   // 4608: a unit's rows as they are in the cache
+constexpr int OV_SMEM = OV_WARPS * OV_DEPTH * UNIT_BYTES;
 
 // Block q of the pack order: split q % nsplit, request (q / nsplit) %
 // batch, position q / nsplit / batch within the split.  Returns (packed
@@ -142,86 +151,104 @@ __device__ __noinline__ int4 block_info(const Params& p, int q, int max_blocks) 
   return make_int4(b * max_blocks + kb, rq.ip0, kb * BN, rq.hi);
 }
 
-// Unit u: 4-key group u % 32 of block u / 32 of the pack order.  blk: the
-// packed block, or -1 (nothing to pack).  slot: lanes 0..3 hold the cache
-// slot of key `lane` of the unit (-1: none / outside).
-struct Unit {
-  int blk, slot;
-};
-
-__device__ __forceinline__ Unit locate(const Params& p, const int4* s_tab, int max_blocks, int u,
-                                       int lane) {
-  Unit t;
-  const int grp = u & (UNITS_PER_BLOCK - 1);
-  const int4 e = s_tab ? s_tab[u / UNITS_PER_BLOCK] : block_info(p, u / UNITS_PER_BLOCK, max_blocks);
-  t.blk = e.x;
-  t.slot = -1;
-  const int j = e.z + grp * UNIT_KEYS + lane;
-  if (e.x >= 0 && lane < UNIT_KEYS && j < e.w) {
+// A warp's units u0, u0 + stride, .. in groups of eight: lane l describes
+// key l & 3 of unit l >> 2 of the group -- `blk` the packed block (-1:
+// nothing to pack, or past `end`), `slot` the key's cache slot (-1: none,
+// or outside the cache, which is reported).
+__device__ __forceinline__ void locate8(const Params& p, int max_blocks, int u0, int end, int stride, int lane,
+                                        int& blk, int& slot) {
+  const int u = u0 + (lane >> 2) * stride;
+  blk = -1;
+  slot = -1;
+  if (u >= end) return;
+  const int4 e = block_info(p, u / UNITS_PER_BLOCK, max_blocks);
+  blk = e.x;
+  const int j = e.z + (u & (UNITS_PER_BLOCK - 1)) * UNIT_KEYS + (lane & 3);
+  if (e.x >= 0 && j < e.w) {
     const long long s = key_slot(p, e.y, j);
     if (s < 0) atomicOr(p.err, ERR_SLOT);
-    t.slot = static_cast<int>(s);
-  }
-  return t;
-}
-
-// Lane l moves granules l % 8, l % 8 + 8, .. of key l / 8 of the unit:
-// granule l % 8 of each of the nine 64-dim chunks.
-__device__ __forceinline__ void load_unit(const Params& p, const Unit& t, int lane, uint4 (&v)[PER_LANE]) {
-  const int sk = __shfl_sync(0xffffffffu, t.slot, lane >> 3);
-  const uint4* src = reinterpret_cast<const uint4*>(p.kv + static_cast<long long>(sk) * D_QK) + (lane & 7);
-#pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) v[i] = make_uint4(0, 0, 0, 0);
-  if (sk >= 0) {   // streamed once
-    const uint64_t pol = evict_first_policy();
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) v[i] = load_row_granule(src + 8 * i, pol);
+    slot = static_cast<int>(s);
   }
 }
 
-__device__ __forceinline__ void store_unit(uint8_t* packed, const Unit& t, int grp, int lane,
-                                           const uint4 (&v)[PER_LANE], bool& bad) {
-  const int j = grp * UNIT_KEYS + (lane >> 3);   // key within the block
-  uint8_t* dst = packed + static_cast<size_t>(t.blk) * BLOCK_BYTES + j * 128 +
-                 (((lane & 7) ^ (j & 7)) << 4);
+// Start the copy of a unit's rows into a stage: lane l moves granules l % 8,
+// l % 8 + 8, .. of row l / 8 (slot `sk`; zero-filled when sk < 0).  The
+// rows are read once per call: marked first to leave L2.
+__device__ __forceinline__ void stage_unit(const Params& p, uint32_t stage, int sk, int lane, uint64_t pol) {
+  const uint16_t* src = p.kv + static_cast<long long>(sk < 0 ? 0 : sk) * D_QK + (lane & 7) * 8;
+  const uint32_t dst = stage + ((lane >> 3) * ROW_CHUNKS + (lane & 7)) * 16;
+  const int bytes = sk < 0 ? 0 : 16;
 #pragma unroll
-  for (int i = 0; i < PER_LANE; ++i) *reinterpret_cast<uint4*>(dst + i * (BN * 128)) = widen_bf16x8(v[i], bad);
+  for (int i = 0; i < PER_LANE; ++i)
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n"
+                 ::"r"(dst + 128 * i), "l"(src + 64 * i), "r"(bytes), "l"(pol)
+                 : "memory");
 }
 
-// Pack units first, first + stride, .. below `end`.  Per round a warp
-// locates unit k+1, stores unit k, issues the row loads of unit k+1 and only
-// then publishes unit k: the release waits for those loads, which the next
-// round needs anyway, so the fence does not sit between two row loads.
-__device__ __forceinline__ void pack_units(const Params& p, const int4* s_tab, uint8_t* packed,
-                                           int max_blocks, int u, int end, int stride, int lane,
-                                           unsigned tag) {
+// Pack this warp's units u, u + stride, .. below `end` through its
+// OV_DEPTH stages: unit k lands in stage k % OV_DEPTH while units k+1 and
+// k+2 are in flight; each lane widens and stores exactly the granules it
+// copied (its own cp.async data, visible to it after the group wait), into
+// chunk i of key j at the swizzled granule, then the warp publishes the unit.
+__device__ __forceinline__ void pack_units(const Params& p, uint8_t* packed, int max_blocks, int u, int end,
+                                           int stride, int lane, unsigned tag, uint32_t stages) {
   if (u >= end) return;
   bool bad = false;
-  Unit cur = locate(p, s_tab, max_blocks, u, lane);
-  uint4 v[PER_LANE];
-  if (cur.blk >= 0) load_unit(p, cur, lane, v);
-#pragma unroll 1
-  for (; u < end; u += stride) {
-    const bool more = u + stride < end;
-    const Unit nxt = locate(p, s_tab, max_blocks, more ? u + stride : u, lane);
-    if (cur.blk >= 0) {
-      store_unit(packed, cur, u & (UNITS_PER_BLOCK - 1), lane, v, bad);
-      // The stores must reach the reader's bulk copies (async proxy).
-      asm volatile("fence.proxy.async.global;\n" ::: "memory");
-    }
-    if (more && nxt.blk >= 0) load_unit(p, nxt, lane, v);
-    if (cur.blk >= 0) {
-      // Publish unit k: the release store orders the warp's stores (made
-      // visible to lane 0 by the warp barrier) before the flag.
-      __syncwarp();
-      if (lane == 0) {
-        unsigned* flag = p.pack_sync + PACK_SYNC_HEADER + UNITS_PER_BLOCK * static_cast<size_t>(cur.blk) +
-                         (u & (UNITS_PER_BLOCK - 1));
-        asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(flag), "r"(tag) : "memory");
-      }
-    }
-    cur = nxt;
+  const uint64_t pol = evict_first_policy();
+  int cur_blk, cur_slot, next_blk, next_slot;   // this group of eight units and the next
+  locate8(p, max_blocks, u, end, stride, lane, cur_blk, cur_slot);
+  locate8(p, max_blocks, u + 8 * stride, end, stride, lane, next_blk, next_slot);
+  // Packed block of units k .. k + OV_DEPTH - 2 (already issued).
+  int blk[OV_DEPTH - 1];
+#pragma unroll
+  for (int d = 0; d < OV_DEPTH - 1; ++d) {
+    blk[d] = __shfl_sync(0xffffffffu, cur_blk, 4 * d);
+    const int sk = __shfl_sync(0xffffffffu, cur_slot, 4 * d + (lane >> 3));
+    if (blk[d] >= 0) stage_unit(p, stages + d * UNIT_BYTES, sk, lane, pol);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
   }
+#pragma unroll 1
+  for (int k = 0; u < end; u += stride, ++k) {
+    // Issue unit k + OV_DEPTH - 1 into the stage unit k - 1 has left.
+    const int ka = k + OV_DEPTH - 1;
+    if ((ka & 7) == 0) {
+      cur_blk = next_blk;
+      cur_slot = next_slot;
+      locate8(p, max_blocks, u + (OV_DEPTH - 1 + 8) * stride, end, stride, lane, next_blk, next_slot);
+    }
+    const int ba = __shfl_sync(0xffffffffu, cur_blk, 4 * (ka & 7));
+    const int sa = __shfl_sync(0xffffffffu, cur_slot, 4 * (ka & 7) + (lane >> 3));
+    if (ba >= 0) stage_unit(p, stages + (ka % OV_DEPTH) * UNIT_BYTES, sa, lane, pol);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    const int cblk = blk[0];
+#pragma unroll
+    for (int d = 0; d < OV_DEPTH - 2; ++d) blk[d] = blk[d + 1];
+    blk[OV_DEPTH - 2] = ba;
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(OV_DEPTH - 1) : "memory");
+    if (cblk < 0) continue;
+    const int j = (u & (UNITS_PER_BLOCK - 1)) * UNIT_KEYS + (lane >> 3);   // key within the block
+    uint8_t* dst = packed + static_cast<size_t>(cblk) * BLOCK_BYTES + j * 128 + (((lane & 7) ^ (j & 7)) << 4);
+    const uint32_t src = stages + (k % OV_DEPTH) * UNIT_BYTES + ((lane >> 3) * ROW_CHUNKS + (lane & 7)) * 16;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      uint4 v;
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(src + 128 * i));
+      *reinterpret_cast<uint4*>(dst + i * (BN * 128)) = widen_bf16x8(v, bad);
+    }
+    // The stores must reach the reader's bulk copies (async proxy); the
+    // release store orders the warp's stores (made visible to lane 0 by the
+    // warp barrier) before the flag.
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      unsigned* flag = p.pack_sync + PACK_SYNC_HEADER + UNITS_PER_BLOCK * static_cast<size_t>(cblk) +
+                       (u & (UNITS_PER_BLOCK - 1));
+      asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(flag), "r"(tag) : "memory");
+    }
+  }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
   report_range(bad, p.err);
 }
 
@@ -230,30 +257,25 @@ __device__ __forceinline__ void pack_units(const Params& p, const int4* s_tab, u
 // CTA so that they all finish together, and exit: their SMs take attention
 // CTAs.  CTAs 0 .. stay-1 start on the rest at once and pack it while the
 // attention kernel runs.
-__global__ void __maxnreg__(64) pack_kv_overlap_kernel(const Params p, uint8_t* packed, int max_blocks,
-                                                       int per_split, int wide_units, int stay) {
-  extern __shared__ int4 s_tab_buf[];
+__global__ void __launch_bounds__(OV_WARPS * 32, 1)
+    pack_kv_overlap_kernel(const Params p, uint8_t* packed, int max_blocks, int per_split, int wide_units,
+                           int stay) {
+  extern __shared__ __align__(128) uint8_t ov_stages[];
   // The attention kernel may be scheduled as soon as every pack CTA runs:
   // its copy warp waits for each block's flags before reading it.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int cta = static_cast<int>(blockIdx.x);
   if (cta >= stay && cta - stay >= wide_units) return;   // no unit in the wide phase: free the SM
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nq = p.nsplit * p.batch * per_split;   // blocks in the pack order
-  const int4* s_tab = nullptr;
-  if (nq <= TABLE_BLOCKS) {
-    for (int q = threadIdx.x; q < nq; q += OV_THREADS) s_tab_buf[q] = block_info(p, q, max_blocks);
-    __syncthreads();
-    s_tab = s_tab_buf;
-  }
-  constexpr int WPC = OV_THREADS / 32;               // warps per CTA
+  const int nq = p.nsplit * p.batch * per_split;     // blocks in the pack order
   const int units = UNITS_PER_BLOCK * nq;            // < 2^31 (host check)
   const int wide_end = min(wide_units, units);
   const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
   const int n = gridDim.x - stay;     // CTAs of the wide phase: warp w of CTA c takes units
-  const bool wide = cta >= stay;      // w * n + c, w * n + c + 32 n, ..
-  const int first = wide ? warp * n + (cta - stay) : wide_end + cta * WPC + warp;
-  pack_units(p, s_tab, packed, max_blocks, first, wide ? wide_end : units, (wide ? n : stay) * WPC, lane, tag);
+  const bool wide = cta >= stay;      // w * n + c, w * n + c + 16 n, ..
+  const int first = wide ? warp * n + (cta - stay) : wide_end + cta * OV_WARPS + warp;
+  pack_units(p, packed, max_blocks, first, wide ? wide_end : units, (wide ? n : stay) * OV_WARPS, lane, tag,
+             smem_u32(ov_stages) + warp * OV_DEPTH * UNIT_BYTES);
 }
 
 }  // namespace
@@ -261,11 +283,11 @@ __global__ void __maxnreg__(64) pack_kv_overlap_kernel(const Params p, uint8_t* 
 size_t packed_block_bytes() { return BLOCK_BYTES; }
 
 cudaError_t pack_kv_prepare() {
-  // Room for the block table; the attention kernel's shared-memory
+  // Room for the warps' stages; the attention kernel's shared-memory
   // configuration (an SM whose carveout differs drains before the other
   // kernel's CTAs can start on it).
   cudaError_t e = cudaFuncSetAttribute(pack_kv_overlap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(sizeof(int4)) * TABLE_BLOCKS);
+                                       OV_SMEM);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(pack_kv_overlap_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                               cudaSharedmemCarveoutMaxShared);
@@ -288,8 +310,7 @@ cudaError_t launch_pack_kv_overlap(const Params& p, void* packed, int max_blocks
     return cudaErrorInvalidConfiguration;
   const int wide_units =
       static_cast<int>(1LL * UNITS_PER_BLOCK * p.nsplit * p.batch * std::min(wide_positions, per_split));
-  const size_t smem = nq <= TABLE_BLOCKS ? sizeof(int4) * nq : 0;
-  pack_kv_overlap_kernel<<<num_ctas, OV_THREADS, smem, stream>>>(p, static_cast<uint8_t*>(packed),
+  pack_kv_overlap_kernel<<<num_ctas, OV_WARPS * 32, OV_SMEM, stream>>>(p, static_cast<uint8_t*>(packed),
                                                                  max_blocks, per_split, wide_units, stay);
   return cudaGetLastError();
 }
