@@ -28,13 +28,17 @@
 // ready flags (tagged with the call's epoch) instead of the whole pack grid,
 // and the last CTA to finish advances the epoch.
 //
-// Roles (10 warps):
+// Roles (11 warps):
 //   warps 0-7  softmax: one thread per (key of the block, half of the 64 query
 //              rows); warps w and w+4 share TMEM lane quadrant w.  First they
 //              load the Q tile (issued at entry) and widen it to fp16;
 //   warp 8     issues the MMAs (one elected lane of the converged warp); it
 //              owns the TMEM allocation;
-//   warp 9     streams the packed blocks with cp.async.bulk (elected lane).
+//   warp 9     streams the packed blocks with cp.async.bulk (elected lane);
+//   warps 9-10 instead, with no pack (one row tile per request), gather each
+//              block's scattered rows themselves (16-byte cp.async), piece by
+//              piece in the producer order below; the softmax warps widen
+//              each piece in place while they wait for S^T.
 // Pipeline over 128-key blocks k (mbarriers, all waits bounded):
 //   producer: chunk pair d of block k+1 is copied as soon as O^T(k) tile d has
 //             finished with it; the rope chunk (which holds P^T(k)) last;
@@ -53,9 +57,10 @@ namespace {
 
 constexpr int BM = 64;          // query rows per CTA: MMA N
 constexpr int BN = 128;         // keys per block: MMA M of S^T
-constexpr int NWARPS = 10;
+constexpr int NWARPS = 11;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int SOFTMAX_WARPS = 8, MMA_WARP = 8, COPY_WARP = 9;
+constexpr int GATHER_WARPS = 2;   // direct mode: warps 9 and 10 gather keys 64w .. 64w+63 of each block
 constexpr int HALF = BM / 2;    // query-row columns per softmax thread
 constexpr int Q_CHUNK = BM * 128;   // one 64-dim chunk of the Q tile
 constexpr int KV_CHUNK = BN * 128;  // one 64-dim chunk of the key block
@@ -69,10 +74,12 @@ constexpr int OFF_WARP = OFF_MREF + 64 * 4;     // float [8][2][32] per-warp row
 constexpr int OFF_L = OFF_WARP + 8 * 64 * 4;    // float [64] reciprocal of the final row sums (0: none)
 constexpr int OFF_MASK = OFF_L + 64 * 4;        // uint32 [32] ancestor masks
 constexpr int OFF_TOFR = OFF_MASK + MAX_T * 4;  // int [64] draft of each row, -1 past R
-constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [16] mbarriers
-constexpr int OFF_MISC = OFF_MBAR + 16 * 8;     // tmem base, abort flag
+constexpr int NMBAR = 18;
+constexpr int OFF_MBAR = OFF_TOFR + 64 * 4;     // uint64 [NMBAR] mbarriers
+constexpr int OFF_MISC = OFF_MBAR + NMBAR * 8;  // tmem base, abort flag
 constexpr int OFF_PAR = OFF_MISC + 16;          // int [32] draft parents
 constexpr int OFF_SLOTK = OFF_PAR + MAX_T * 4;  // int [128] slots of the block being gathered (direct mode)
+static_assert(GATHER_WARPS * 64 == BN, "each gather warp takes half of a block's keys");
 constexpr int SMEM_TOTAL = OFF_SLOTK + BN * 4;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -84,6 +91,7 @@ constexpr int MB_P = 6;       // P^T written, O^T rescaled (one arrival per soft
 constexpr int MB_Q = 7;       // Q tile in fp16 (one arrival per softmax warp)
 constexpr int MB_OT = 8;      // [4] O^T tile d done (tcgen05.commit)
 constexpr int MB_DONE = 12;   // after an abort: every MMA the CTA issued is done
+constexpr int MB_RAW = 13;    // [5] direct mode: piece g's rows landed (cp.async arrivals, bf16)
 
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t TM_S = 256;                  // S^T columns; O^T tile d at d * 64
@@ -215,7 +223,7 @@ __device__ __forceinline__ void transpose_max32(float (&v)[32], int lane) {
 __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split, int row0, int tid) {
   const float nan = __int_as_float(0x7fc00000);
   const size_t ws_row = ws_base(p, b, split);
-  for (int i = tid; i < BM * D_V; i += NTHREADS) {
+  for (int i = tid; i < BM * D_V; i += static_cast<int>(blockDim.x)) {
     const int lr = i / D_V, d = i - lr * D_V;
     const int gr = row0 + lr;
     if (gr >= p.R) continue;
@@ -231,7 +239,12 @@ __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int split
   }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p) {
+// kDirect: no pack, the CTAs gather their own key blocks (p.direct_all).
+// The two modes are separate instantiations so that neither's softmax loop
+// is scheduled around the other's code: with the direct-mode widening in the
+// same loop body the packed path measured ~15 % slower on one-block splits.
+template <bool kDirect>
+__global__ void __launch_bounds__(kDirect ? NTHREADS : NTHREADS - 32, 1) partial_tc_kernel(const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int split = blockIdx.x, rt = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -295,7 +308,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   if (tid < p.T) s_par[tid] = p.draft_parent[b * p.T + tid];
   if (tid < BM) s_tofr[tid] = row0 + tid < p.R ? (row0 + tid) / p.H : -1;
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) tc::mbar_init(mbar(MB_CHUNK + i), 1);
+    for (int i = 0; i < 5; ++i) {
+      tc::mbar_init(mbar(MB_CHUNK + i), kDirect ? SOFTMAX_WARPS : 1);
+      tc::mbar_init(mbar(MB_RAW + i), GATHER_WARPS * 32);
+    }
     tc::mbar_init(mbar(MB_S), 1);
     tc::mbar_init(mbar(MB_P), SOFTMAX_WARPS);
     tc::mbar_init(mbar(MB_Q), SOFTMAX_WARPS);
@@ -310,8 +326,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == COPY_WARP && p.direct_all) {
-    // direct mode: the softmax warps gather the key blocks themselves
+  if (kDirect && warp >= COPY_WARP) {
+    // ===================== direct gather (no pack) ==========================
+    // Gather warp w copies keys 64w .. 64w+63 of every block, in the packed
+    // producer's order: chunk pair g of block k as soon as O^T(k-1) tile g
+    // has read pair g of the previous block, the rope chunk (where P^T(k-1)
+    // lived) last -- 16-byte cp.async of the scattered rows, zero-filled
+    // past the request, each lane's copies arriving on the piece's MB_RAW
+    // barrier when they land.  The softmax warps, idle until S^T(k), widen
+    // each piece in place and release it to the MMA warp.
+    const int gw = warp - COPY_WARP;
+    int* wslot = s_slotk + 64 * gw;
+    const int ka = 64 * gw + lane, kbk = ka + 32;   // the keys whose slots this lane looks up
+    int sa = nb > 0 ? block_slot(p, rq, kb0, ka, false) : -1;
+    int sb = nb > 0 ? block_slot(p, rq, kb0, kbk, false) : -1;
+    // Exit decisions are warp-uniform (the abort flag is read lane by lane).
+    auto aborted = [&]() { return __any_sync(0xffffffffu, *s_abort != 0); };
+#pragma unroll 1
+    for (int it = 0; it < nb && !aborted(); ++it) {
+      __syncwarp();
+      wslot[lane] = sa;
+      wslot[32 + lane] = sb;
+      __syncwarp();
+      if (it + 1 < nb) {   // the next block's slots, in flight while this one is gathered
+        sa = block_slot(p, rq, kb0 + it + 1, ka, false);
+        sb = block_slot(p, rq, kb0 + it + 1, kbk, false);
+      }
+      const uint32_t prev = static_cast<uint32_t>((it - 1) & 1);
+#pragma unroll 1
+      for (int g = 0; g < 5; ++g) {
+        if (it > 0 && g < 4) wait_warp(mbar(MB_OT + g), prev, s_abort, p.err);
+        if (aborted()) break;
+        // Lane l: granules l % 16 of chunk pair g of keys 2i + l / 16, or
+        // granule l % 8 of the rope chunk of keys 4i + l / 8.
+        const int n = g < 4 ? 32 : 16;
+#pragma unroll 4
+        for (int i = 0; i < n; ++i) {
+          const int key = g < 4 ? 2 * i + (lane >> 4) : 4 * i + (lane >> 3);
+          const int q = g < 4 ? 16 * g + (lane & 15) : 64 + (lane & 7);
+          const int k = 64 * gw + key;
+          const int sl = wslot[key];
+          cp_async16(sbase + OFF_KV + (q >> 3) * KV_CHUNK + k * 128 + (((q & 7) ^ (k & 7)) << 4),
+                     sl >= 0 ? p.kv + static_cast<size_t>(sl) * D_QK + q * 8 : p.kv, sl >= 0 ? 16 : 0);
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar(MB_RAW + g)) : "memory");
+      }
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");   // nothing in flight at exit
   } else if (warp == COPY_WARP) {
     // ======================= packed-block producer ==========================
     // The whole warp runs the loop; one elected lane issues each copy.
@@ -388,7 +449,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
         wait_drain(mbar(MB_DONE), 0, p.err);
       }
     }
-  } else {
+  } else if (warp < SOFTMAX_WARPS) {
     // ============================= softmax =================================
     // The Q tile (issued at entry) to fp16.  The ancestor masks are ready
     // after the barrier that follows the load.
@@ -421,7 +482,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
 #pragma unroll
     for (int c = 0; c < HALF; ++c) lpart[c] = 0.f;
     // Direct mode: out-of-cache slots are reported here (else by the pack).
-    const bool direct = p.direct_all != 0;
+    constexpr bool direct = kDirect;
     int slot_next = nb > 0 ? block_slot(p, rq, kb0, j, direct) : -1;
     bool next_ok = slot_next >= 0;
 #pragma unroll 1
@@ -429,45 +490,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
       const int kb = kb0 + it;
       const uint32_t par = static_cast<uint32_t>(it & 1);
       const bool key_ok = next_ok;
+      if (it + 1 < nb) next_ok = block_slot(p, rq, kb + 1, j, direct) >= 0;
       if (direct) {
-        // Gather block kb: 128 scattered rows straight from the cache into
-        // the swizzled chunk tiles (absent or invalid keys zero-filled),
-        // once O^T(kb-1) has read the previous block and its P^T; widen to
-        // fp16 in place; release the chunk barriers to the MMA warp as if
-        // the copies had landed.
-        if (it > 0) {
-          wait_warp(mbar(MB_OT + 3), static_cast<uint32_t>((it - 1) & 1), s_abort, p.err);
-          tc::fence_after_sync();
-        }
-        if (hc == 0) s_slotk[j] = slot_next;
-        named_sync(1, SOFTMAX_WARPS * 32);
-#pragma unroll 1
-        for (int e = tid; e < BN * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
-          const int k = e / ROW_CHUNKS, q = e - k * ROW_CHUNKS;
-          const int sl = s_slotk[k];
-          cp_async16(sbase + OFF_KV + (q >> 3) * KV_CHUNK + k * 128 + (((q & 7) ^ (k & 7)) << 4),
-                     sl >= 0 ? p.kv + static_cast<size_t>(sl) * D_QK + q * 8 : p.kv, sl >= 0 ? 16 : 0);
-        }
-        asm volatile("cp.async.commit_group;\n" ::: "memory");
-        if (it + 1 < nb) {   // the next block's slot, while the rows are in flight
-          slot_next = block_slot(p, rq, kb + 1, j, true);
-          next_ok = slot_next >= 0;
-        }
-        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-        named_sync(1, SOFTMAX_WARPS * 32);
+        // Block kb's pieces as the gather warps' copies land: widen to fp16
+        // in place (8 granules a thread per chunk pair, 4 of the rope chunk)
+        // and release each to the MMA warp.
         bool bad = false;
 #pragma unroll 1
-        for (int e = tid; e < BN * ROW_CHUNKS; e += SOFTMAX_WARPS * 32) {
-          uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_KV + e * 16);
-          *ptr = widen_bf16x8(*ptr, bad);
+        for (int g = 0; g < 5; ++g) {
+          wait_warp(mbar(MB_RAW + g), par, s_abort, p.err);
+          const int n = g < 4 ? 8 : 4;
+#pragma unroll
+          for (int i = 0; i < n; ++i) {
+            const int e = tid + 256 * i;
+            const int k = g < 4 ? e >> 4 : e >> 3;
+            const int q = g < 4 ? 16 * g + (e & 15) : 64 + (e & 7);
+            uint4* ptr = reinterpret_cast<uint4*>(smem + OFF_KV + (q >> 3) * KV_CHUNK + k * 128 +
+                                                  (((q & 7) ^ (k & 7)) << 4));
+            *ptr = widen_bf16x8(*ptr, bad);
+          }
+          tc::fence_async_smem();   // the tensor core reads the widened rows next
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(mbar(MB_CHUNK + g));
         }
         report_range(bad, p.err);
-        tc::fence_async_smem();
-        named_sync(1, SOFTMAX_WARPS * 32);
-        if (tid == 0)
-          for (int g = 0; g < 5; ++g) tc::mbar_arrive(mbar(MB_CHUNK + g));
-      } else if (it + 1 < nb) {
-        next_ok = block_slot(p, rq, kb + 1, j, false) >= 0;
       }
       const int jg = kb * BN + j;
       wait_warp(mbar(MB_S), par, s_abort, p.err);
@@ -708,17 +754,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params p)
 }  // namespace
 
 cudaError_t partial_tc_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_TOTAL);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
+  for (auto fn : {partial_tc_kernel<false>, partial_tc_kernel<true>}) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.nsplit, (p.R + BM - 1) / BM, p.batch);
-  cfg.blockDim = dim3(NTHREADS);
+  // The second gather warp exists only when the CTAs gather their own keys.
+  cfg.blockDim = dim3(p.direct_all ? NTHREADS : NTHREADS - 32);
   cfg.dynamicSmemBytes = SMEM_TOTAL;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -726,7 +775,8 @@ cudaError_t launch_partial_tc(const Params& p, cudaStream_t stream, bool overlap
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, partial_tc_kernel, p);
+  return p.direct_all ? cudaLaunchKernelEx(&cfg, partial_tc_kernel<true>, p)
+                      : cudaLaunchKernelEx(&cfg, partial_tc_kernel<false>, p);
 }
 
 }  // namespace mlav
