@@ -249,8 +249,12 @@ int mla_verify_attn(mla_verify_plan* plan, int batch, const void* q,
  * kv_cache on the device (the cache is resident model state).  Copies the
  * inputs into the plan's device staging buffers on `stream`, runs
  * mla_verify_attn, copies out/lse back and synchronises `stream` before
- * returning.  kv_indptr[batch] entries of kv_indices are copied; that count
- * must not exceed max_batch * max_kv_len.  Not capturable.
+ * returning.  When all five inputs are page-locked and mapped into the
+ * device's address space (cudaHostAlloc / pinned tensors on a unified-
+ * address system) one copy kernel moves them; otherwise one DMA copy per
+ * array.  The results likewise (both output buffers mapped: one kernel).
+ * kv_indptr[batch] entries of kv_indices are copied; that count must not
+ * exceed max_batch * max_kv_len.  Not capturable.
  */
 int mla_verify_attn_host(mla_verify_plan* plan, int batch, const void* q_host,
                          const void* kv_cache, const int32_t* kv_indices_host,

@@ -263,6 +263,18 @@ cudaError_t note_done(mla_verify_plan* pl, cudaStream_t s) {
   return e;
 }
 
+// The device address of a page-locked host buffer mapped into the device's
+// address space, or nullptr (pageable memory: the caller's copies go through
+// DMA instead).  A cleared lookup error leaves no sticky state behind.
+const void* device_view(const void* host) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 int check_device(const mla_verify_plan* pl) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_VERIFY_ERR_CUDA;
@@ -645,20 +657,55 @@ int mla_verify_attn_host(mla_verify_plan* pl, int batch, const void* q_host, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t rows = static_cast<size_t>(batch) * pl->R;
   const size_t out_elt = pl->out_dtype == MLA_VERIFY_OUT_BF16 ? 2 : 4;
-  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
-  bool ok =
-      cudaMemcpyAsync(pl->st_q, q_host, rows * mlav::ROW_BYTES, h2d, s) == cudaSuccess &&
-      cudaMemcpyAsync(pl->st_idx, kv_indices_host, static_cast<size_t>(nidx) * 4, h2d, s) == cudaSuccess &&
-      cudaMemcpyAsync(pl->st_indptr, kv_indptr_host, static_cast<size_t>(batch + 1) * 4, h2d, s) == cudaSuccess &&
-      cudaMemcpyAsync(pl->st_lens, kv_lens_host, static_cast<size_t>(batch) * 4, h2d, s) == cudaSuccess &&
-      cudaMemcpyAsync(pl->st_parent, draft_parent_host, static_cast<size_t>(batch) * pl->T * 4, h2d, s) == cudaSuccess;
+  // Inputs: one copy kernel when every host array is mapped into the
+  // device's address space (page-locked), else one DMA copy each.
+  const void* in_host[5] = {q_host, kv_indices_host, kv_indptr_host, kv_lens_host, draft_parent_host};
+  void* in_dev[5] = {pl->st_q, pl->st_idx, pl->st_indptr, pl->st_lens, pl->st_parent};
+  const long long in_bytes[5] = {static_cast<long long>(rows * mlav::ROW_BYTES), nidx * 4, (batch + 1) * 4LL,
+                                 batch * 4LL, static_cast<long long>(batch) * pl->T * 4};
+  mlav::CopyRegions in{};
+  bool mapped = true;
+  for (int r = 0; r < 5 && mapped; ++r) {
+    in.src[r] = device_view(in_host[r]);
+    in.dst[r] = in_dev[r];
+    in.bytes[r] = in_bytes[r];
+    mapped = in.src[r] != nullptr;
+  }
+  in.n = 5;
+  bool ok = true;
+  if (mapped) {
+    ok = mlav::launch_copy_regions(in, s) == cudaSuccess;
+  } else {
+    for (int r = 0; r < 5 && ok; ++r)
+      ok = cudaMemcpyAsync(in_dev[r], in_host[r], static_cast<size_t>(in_bytes[r]), cudaMemcpyHostToDevice, s) ==
+           cudaSuccess;
+  }
   if (!ok) return MLA_VERIFY_ERR_CUDA;
   const int st = mla_verify_attn(pl, batch, pl->st_q, kv_cache, pl->st_idx, pl->st_indptr,
                                  pl->st_lens, pl->st_parent, scale, pl->st_out, pl->st_lse, stream);
   if (st != MLA_VERIFY_OK) return st;
-  ok = cudaMemcpyAsync(out_host, pl->st_out, rows * mlav::D_V * out_elt, d2h, s) == cudaSuccess &&
-       cudaMemcpyAsync(lse_host, pl->st_lse, rows * sizeof(float), d2h, s) == cudaSuccess &&
-       cudaStreamSynchronize(s) == cudaSuccess;
+  // Results: the same, in the other direction.
+  void* out_dst[2] = {out_host, lse_host};
+  const void* out_src[2] = {pl->st_out, pl->st_lse};
+  const long long out_bytes[2] = {static_cast<long long>(rows * mlav::D_V * out_elt),
+                                  static_cast<long long>(rows * sizeof(float))};
+  mlav::CopyRegions out{};
+  bool out_mapped = true;
+  for (int r = 0; r < 2 && out_mapped; ++r) {
+    out.src[r] = out_src[r];
+    out.dst[r] = const_cast<void*>(device_view(out_dst[r]));
+    out.bytes[r] = out_bytes[r];
+    out_mapped = out.dst[r] != nullptr;
+  }
+  out.n = 2;
+  if (out_mapped) {
+    ok = mlav::launch_copy_regions(out, s) == cudaSuccess;
+  } else {
+    for (int r = 0; r < 2 && ok; ++r)
+      ok = cudaMemcpyAsync(out_dst[r], out_src[r], static_cast<size_t>(out_bytes[r]), cudaMemcpyDeviceToHost, s) ==
+           cudaSuccess;
+  }
+  ok = ok && cudaStreamSynchronize(s) == cudaSuccess;
   return ok ? MLA_VERIFY_OK : MLA_VERIFY_ERR_CUDA;
 }
 

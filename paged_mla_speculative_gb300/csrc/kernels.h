@@ -51,6 +51,18 @@ cudaError_t launch_pack_kv_overlap(const Params& p, void* packed, int max_blocks
 // scheduled early; it waits for the partial kernel with griddepcontrol.wait).
 cudaError_t launch_combine(const Params& p, cudaStream_t stream, bool overlap);
 
+// Up to kMax copies between device-addressable regions (device memory, or
+// page-locked host memory mapped into the device's address space) in one
+// kernel launch.  Byte counts are multiples of 4.
+struct CopyRegions {
+  static constexpr int kMax = 8;
+  const void* src[kMax];
+  void* dst[kMax];
+  long long bytes[kMax];
+  int n;
+};
+cudaError_t launch_copy_regions(const CopyRegions& c, cudaStream_t stream);
+
 // Per-step index builder (index_builder.cu).
 struct IndexArgs {
   const int32_t* req_to_token;      // [pool_size][stride] cache slot of each token position

@@ -131,17 +131,37 @@ def test_indptr_mismatch_is_reported():
     assert torch.isnan(out).all()
 
 
-def test_host_entry_point_matches_device_entry_point():
+@pytest.mark.parametrize("memory", ["pinned", "mixed", "pageable"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_host_entry_point_matches_device_entry_point(memory, out_dtype):
+    """The host-buffer entry moves its inputs and results with one copy
+    kernel per direction when every host buffer is page-locked (mapped into
+    the device's address space), else with one DMA copy per array; both give
+    the device entry's bits, repeated calls included."""
     inp = _case(seed=6)
-    with G.make_plan(inp) as plan:
+    pin = {"pinned": lambda t: t.pin_memory(), "pageable": lambda t: t,
+           "mixed": None}[memory]
+
+    def host(t, i):
+        t = t.cpu()
+        if memory == "mixed":
+            return t.pin_memory() if i % 2 == 0 else t
+        return pin(t)
+
+    with G.make_plan(inp, out_dtype=out_dtype) as plan:
         o_dev, l_dev = G.run(plan, inp)
         B = inp.q.shape[0]
-        out = torch.empty((B, 4, 16, 512), dtype=torch.float32).pin_memory()
-        lse = torch.empty((B, 4, 16), dtype=torch.float32).pin_memory()
-        mb.mla_verify_attn_host(plan, inp.q.cpu().pin_memory(), inp.kv_cache,
-                                inp.kv_indices.cpu().pin_memory(), inp.kv_indptr.cpu(),
-                                inp.kv_lens.cpu(), inp.draft_parent.cpu(), inp.scale, out, lse)
-    assert torch.equal(out, o_dev.cpu()) and torch.equal(lse, l_dev.cpu())
+        out = host(torch.empty((B, 4, 16, 512), dtype=out_dtype), 0)
+        lse = host(torch.empty((B, 4, 16), dtype=torch.float32), 1)
+        args = [host(t, i) for i, t in enumerate((inp.q, inp.kv_indices, inp.kv_indptr, inp.kv_lens,
+                                                  inp.draft_parent))]
+        for _ in range(3):
+            out.zero_()
+            lse.zero_()
+            mb.mla_verify_attn_host(plan, args[0], inp.kv_cache, args[1], args[2], args[3], args[4],
+                                    inp.scale, out, lse)
+            assert torch.equal(out, o_dev.cpu()) and torch.equal(lse, l_dev.cpu())
+        assert plan.get_error() == 0
 
 
 @pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_PAIR, id="pair"), pytest.param(mb.KERNEL_TC, id="tc")])
