@@ -252,7 +252,8 @@ int mla_verify_attn(mla_verify_plan* plan, int batch, const void* q,
  * returning.  When all five inputs are page-locked and mapped into the
  * device's address space (cudaHostAlloc / pinned tensors on a unified-
  * address system) one copy kernel moves them; otherwise one DMA copy per
- * array.  The results likewise (both output buffers mapped: one kernel).
+ * array.  The results likewise; when both output buffers are mapped and the
+ * call ends in the split combine, the combine kernel writes them in place.
  * kv_indptr[batch] entries of kv_indices are copied; that count must not
  * exceed max_batch * max_kv_len.  Not capturable.
  */

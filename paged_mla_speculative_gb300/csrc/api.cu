@@ -681,10 +681,18 @@ int mla_verify_attn_host(mla_verify_plan* pl, int batch, const void* q_host, con
            cudaSuccess;
   }
   if (!ok) return MLA_VERIFY_ERR_CUDA;
-  const int st = mla_verify_attn(pl, batch, pl->st_q, kv_cache, pl->st_idx, pl->st_indptr,
-                                 pl->st_lens, pl->st_parent, scale, pl->st_out, pl->st_lse, stream);
+  // Results: when the call ends in the split combine (plain stores) and both
+  // output buffers are mapped, the combine writes them in host memory
+  // directly; otherwise into the staging buffers, then copied back below.
+  void* out_view = const_cast<void*>(device_view(out_host));
+  void* lse_view = const_cast<void*>(device_view(lse_host));
+  const bool direct_out = out_view && lse_view && aligned16(out_view) && aligned16(lse_view) &&
+                          effective_nsplit(pl, batch) > 1;
+  const int st = mla_verify_attn(pl, batch, pl->st_q, kv_cache, pl->st_idx, pl->st_indptr, pl->st_lens,
+                                 pl->st_parent, scale, direct_out ? out_view : pl->st_out,
+                                 direct_out ? static_cast<float*>(lse_view) : pl->st_lse, stream);
   if (st != MLA_VERIFY_OK) return st;
-  // Results: the same, in the other direction.
+  if (direct_out) return cudaStreamSynchronize(s) == cudaSuccess ? MLA_VERIFY_OK : MLA_VERIFY_ERR_CUDA;
   void* out_dst[2] = {out_host, lse_host};
   const void* out_src[2] = {pl->st_out, pl->st_lse};
   const long long out_bytes[2] = {static_cast<long long>(rows * mlav::D_V * out_elt),
