@@ -105,21 +105,35 @@ __device__ __forceinline__ Request load_request(const Params& p, int b) {
   return r;
 }
 
+// Units [u0, u1) that part `part` of `parts` takes of `n` units: n / parts
+// each, the remainder to the first parts.  The last part of a request's keys
+// holds its draft keys (the tree-masked block, the slowest one) and, with
+// pair blocks, possibly a lone block: it gets the smaller share.  (An even
+// division by floor(n * part / parts) gives the last part the larger one;
+// measured on the 93k sweep point the last split then ended ~5 us after the
+// other long splits and set the kernel's end.)
+__device__ __forceinline__ void split_units(long long n, int part, int parts, long long& u0, long long& u1) {
+  const long long q = n / parts, r = n % parts;
+  u0 = part * q + min(static_cast<long long>(part), r);
+  u1 = u0 + q + (part < r ? 1 : 0);
+}
+
 // Blocks [kb0, kb1) of `bn` keys that split `split` of `nsplit` takes of the
-// request's range [lo, hi): the range's blocks divided evenly.
+// request's range [lo, hi).
 __device__ __forceinline__ void split_blocks(const Request& rq, int bn, int split, int nsplit, int& kb0,
                                              int& kb1) {
   const int a = rq.lo / bn, z = (rq.hi + bn - 1) / bn;
-  const long long nb = z > a ? z - a : 0;
-  kb0 = a + static_cast<int>(nb * split / nsplit);
-  kb1 = a + static_cast<int>(nb * (split + 1) / nsplit);
+  long long u0, u1;
+  split_units(z > a ? z - a : 0, split, nsplit, u0, u1);
+  kb0 = a + static_cast<int>(u0);
+  kb1 = a + static_cast<int>(u1);
 }
 
 // The 128-key blocks [kb0, kb1) that split `split` takes of the request's
-// range: its blocks divided evenly, or its pairs of blocks when the
-// attention kernel works on pair blocks (a range with an odd block count
-// ends on a lone block).  The pack and the attention kernel both use it, so
-// the pack order follows the order the attention kernel reads blocks in.
+// range: its blocks, or its pairs of blocks when the attention kernel works
+// on pair blocks (a range with an odd block count ends on a lone block).
+// The pack and the attention kernel both use it, so the pack order follows
+// the order the attention kernel reads blocks in.
 __device__ __forceinline__ void split_range(const Params& p, const Request& rq, int split, int& kb0,
                                             int& kb1) {
   if (!p.split_pairs) {
@@ -127,9 +141,10 @@ __device__ __forceinline__ void split_range(const Params& p, const Request& rq, 
     return;
   }
   const int a = rq.lo / 128, z = (rq.hi + 127) / 128;
-  const long long npb = z > a ? (z - a + 1) / 2 : 0;
-  kb0 = a + 2 * static_cast<int>(npb * split / p.nsplit);
-  kb1 = min(z, a + 2 * static_cast<int>(npb * (split + 1) / p.nsplit));
+  long long u0, u1;
+  split_units(z > a ? (z - a + 1) / 2 : 0, split, p.nsplit, u0, u1);
+  kb0 = a + 2 * static_cast<int>(u0);
+  kb1 = min(z, a + 2 * static_cast<int>(u1));
 }
 
 // First workspace row of split s of request b.
