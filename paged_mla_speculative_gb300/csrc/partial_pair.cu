@@ -582,6 +582,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       // Read while S^T(it) is still being computed.
       const bool key_ok = block_slot(p, rq, kb, j) >= 0;
       const int jg = kb * BN + j;
+      // The group's rows that see this key (bit c: row c0 + c), decided
+      // while S^T(it) is computed: every row for a prefix key, the draft's
+      // ancestors for a draft key, none past the request.  (Applying the
+      // tree mask row by row after the scores arrive cost ~3 us per pass on
+      // the block that holds the drafts.)
+      uint32_t vis = 0;
+      if (key_ok) {
+        if (jg < rq.P && all_rows) {
+          vis = 0xffffffffu;
+        } else {
+          const int di = jg - rq.P;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int t = s_tofr[c0 + c];
+            bool v = t >= 0;
+            if (v && di >= 0) v = (s_mask[t] >> di) & 1u;
+            vis |= (v ? 1u : 0u) << c;
+          }
+        }
+      }
       const uint32_t sb = static_cast<uint32_t>(it & 1);
       wait_warp(mbar(MB_S + sb), static_cast<uint32_t>((it >> 1) & 1), s_abort, p.err);
       tc::fence_after_sync();
@@ -589,21 +609,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       float s[32];
       auto load_scores = [&]() { tc::tmem_ld32f(s_addr, s); };
       auto mask_scores = [&]() {
-        if (!key_ok) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[c] = -INFINITY;
-        } else if (jg < rq.P && all_rows) {
+        if (vis == 0xffffffffu) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) s[c] *= scale2;
         } else {
-          const int di = jg - rq.P;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int t = s_tofr[c0 + c];
-            bool vis = t >= 0;
-            if (vis && di >= 0) vis = (s_mask[t] >> di) & 1u;
-            s[c] = vis ? s[c] * scale2 : -INFINITY;
-          }
+          for (int c = 0; c < 32; ++c) s[c] = (vis >> c) & 1u ? s[c] * scale2 : -INFINITY;
         }
       };
       load_scores();

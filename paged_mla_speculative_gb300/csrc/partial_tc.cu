@@ -516,27 +516,36 @@ __global__ void __launch_bounds__(kDirect ? NTHREADS : NTHREADS - 32, 1) partial
         report_range(bad, p.err);
       }
       const int jg = kb * BN + j;
+      // The half's rows that see this key (bit c: row c0 + c), decided
+      // before the scores arrive: every row for a prefix key, the draft's
+      // ancestors for a draft key, none past the request.
+      uint32_t vis = 0;
+      if (key_ok) {
+        if (jg < rq.P && all_rows) {
+          vis = 0xffffffffu;
+        } else {
+          const int di = jg - rq.P;   // draft index when >= 0
+#pragma unroll
+          for (int c = 0; c < HALF; ++c) {
+            const int t = s_tofr[c0 + c];
+            bool v = t >= 0;
+            if (v && di >= 0) v = (s_mask[t] >> di) & 1u;
+            vis |= (v ? 1u : 0u) << c;
+          }
+        }
+      }
       wait_warp(mbar(MB_S), par, s_abort, p.err);
       tc::fence_after_sync();
       uint32_t sr[HALF];
       tc::tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + TM_S + c0, sr);
       tc::tmem_wait_ld();
       float* s = reinterpret_cast<float*>(sr);   // scores overwrite the raw bits in place
-      if (!key_ok) {
-#pragma unroll
-        for (int c = 0; c < HALF; ++c) s[c] = -INFINITY;
-      } else if (jg < rq.P && all_rows) {
+      if (vis == 0xffffffffu) {
 #pragma unroll
         for (int c = 0; c < HALF; ++c) s[c] = __uint_as_float(sr[c]) * scale2;
       } else {
-        const int di = jg - rq.P;   // draft index when >= 0
 #pragma unroll
-        for (int c = 0; c < HALF; ++c) {
-          const int t = s_tofr[c0 + c];
-          bool vis = t >= 0;
-          if (vis && di >= 0) vis = (s_mask[t] >> di) & 1u;
-          s[c] = vis ? __uint_as_float(sr[c]) * scale2 : -INFINITY;
-        }
+        for (int c = 0; c < HALF; ++c) s[c] = (vis >> c) & 1u ? __uint_as_float(sr[c]) * scale2 : -INFINITY;
       }
       // Column (query row) max: over this warp's 32 keys (lane l ends with
       // column c0 + l), then over the four quads.  Lane l keeps the running
