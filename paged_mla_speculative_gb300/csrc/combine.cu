@@ -16,8 +16,9 @@
 namespace mlav {
 namespace {
 
-constexpr int WARPS = 8;
+constexpr int WARPS = 4;   // rows per CTA: more CTAs over the SMs for the few rows of a call
 constexpr int EARLY = 2;   // splits whose rows are loaded before the weights are known
+constexpr int GROUP = 4;   // later splits whose rows are in flight together
 
 __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
   // The split partials come from the kernel just before this one on the
@@ -70,17 +71,31 @@ __global__ void __launch_bounds__(WARPS * 32) combine_kernel(const Params p) {
       acc[k].w += ws * early[s][k].w;
     }
   }
-  for (int s = EARLY; s < ns; ++s) {
-    const float ws = __shfl_sync(0xffffffffu, w, s);
-    if (ws == 0.f) continue;  // uniform across the warp
-    const float4* src = reinterpret_cast<const float4*>(p.ws_o + (ws_base(p, b, s) + r) * D_V);
+  // The rest GROUP splits at a time: every load of a group is issued before
+  // any is used, one memory round trip per group instead of one per split.
+  for (int s0 = EARLY; s0 < ns; s0 += GROUP) {
+    float wg[GROUP];
+    float4 v[GROUP][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 v = __ldcs(src + lane + 32 * k);
-      acc[k].x += ws * v.x;
-      acc[k].y += ws * v.y;
-      acc[k].z += ws * v.z;
-      acc[k].w += ws * v.w;
+    for (int g = 0; g < GROUP; ++g) {
+      const int s = s0 + g;   // uniform across the warp, < 32
+      wg[g] = s < ns ? __shfl_sync(0xffffffffu, w, s) : 0.f;
+      if (wg[g] != 0.f) {
+        const float4* src = reinterpret_cast<const float4*>(p.ws_o + (ws_base(p, b, s) + r) * D_V);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[g][k] = __ldcs(src + lane + 32 * k);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < GROUP; ++g) {
+      if (wg[g] == 0.f) continue;  // uniform across the warp
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[k].x += wg[g] * v[g][k].x;
+        acc[k].y += wg[g] * v[g][k].y;
+        acc[k].z += wg[g] * v[g][k].z;
+        acc[k].w += wg[g] * v[g][k].w;
+      }
     }
   }
   const float nan = __int_as_float(0x7fc00000);
