@@ -352,7 +352,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   if (warp == MMA_WARP) tc::tmem_alloc_pair<TMEM_COLS>(smem_u32(s_tmem));
   tc::fence_before_sync();
   __syncthreads();
-  tc::cluster_sync();   // the peer's barriers exist and the pair's TMEM is allocated
+  // The peer's barriers exist (their initialisation was published by
+  // fence.mbarrier_init) and the pair's TMEM is allocated.  A release arrive
+  // here would first wait for this CTA's Q loads, still in flight.
+  tc::cluster_sync_relaxed();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
   const uint32_t even_mbar0 = tc::peer_addr(mbar0, 0);   // the even CTA's barriers

@@ -288,5 +288,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint4 v, uint
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
+// Cluster barrier whose arrive orders nothing: for a sync that only has to
+// publish mbarrier initialisations (made visible at cluster scope by
+// fence.mbarrier_init beforehand).  A release arrive waits for the thread's
+// outstanding memory operations, e.g. loads still in flight.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 }  // namespace tc
 }  // namespace mlav
