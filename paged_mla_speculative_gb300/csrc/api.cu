@@ -135,16 +135,24 @@ PackSchedule pack_plan(const mla_verify_plan* pl, int fam, int batch, int nsplit
   return PackSchedule{MLA_VERIFY_PACK_IDLE_SMS, std::min(wide, positions), static_cast<int>(idle)};
 }
 
-// What the pack leaves on a call's critical path (us): the wide phase
-// (~9 us) when it overlaps, else the whole gather of up to batch x
-// max_kv_len rows (1152 B read + 1152 B written each at ~4.5 TB/s, plus
-// ~3 us); nothing when the attention CTAs gather directly.
+// What the pack leaves on a call's critical path (us), at ~4.5 TB/s for a
+// block's 1152-B rows read plus its 147 456 B written, plus ~3 us: the wide
+// phase (`wide` block positions of every split) when it overlaps the
+// attention kernel, else the whole gather of up to batch x max_kv_len rows;
+// nothing when the attention CTAs gather directly.
 double pack_us(const mla_verify_plan* pl, int fam, int batch, int nsplit, int shards) {
   if (fam == MLA_VERIFY_KERNEL_MMA || gathers_directly(pl)) return 0.0;
   const PackSchedule ps = pack_plan(pl, fam, batch, nsplit, true, shards);
-  if (ps.mode != MLA_VERIFY_PACK_WHOLE) return 9.0;
+  if (ps.mode != MLA_VERIFY_PACK_WHOLE)
+    return 2.0 * 147456.0 * ps.wide * nsplit * batch / 4.5e12 * 1e6 + 3.0;
   return 2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0;
 }
+
+// Split steps run ~15 % slower beside the overlapping pack (its loads and
+// stores share L2 and HBM with the attention kernel's copies): measured on
+// the 93k sweep point, 15 splits with the pack on 32 idle SMs, 151.8 us per
+// call against 158.3 with 19 splits and the whole pack first.
+constexpr double kBesidePack = 1.155;
 
 // Keys a request can hold in a call covering one of `shards` shards: a
 // shard takes at most ceil(nb / shards) of the request's nb 128-key blocks.
@@ -160,11 +168,26 @@ long long max_steps(const mla_verify_plan* pl, int kernel, int shards) {
 }
 
 // Moving the split partials through the combine (us): a launch, and the
-// partials' bytes at ~3.5 TB/s.
+// partials' bytes (just written, in L2) at ~15 TB/s -- measured: 8.2 us for
+// 2 splits and 10.2 us for 19 splits of 512 rows.
 double combine_us(const mla_verify_plan* pl, int kernel, int batch, int ns) {
   if (ns <= 1) return 0.0;
   const double units = static_cast<double>(batch) * ceil_div(pl->R, rows_per_unit(kernel));
-  return 3.4 + units * rows_per_unit(kernel) * ns * 4096.0 / 3.5e6;
+  return 3.4 + units * rows_per_unit(kernel) * ns * 4096.0 / 15e6;
+}
+
+// Estimated time (us) of a call of family `kernel` with `ns` splits: waves of
+// units, each its fixed cost plus its split steps (slower beside an
+// overlapping pack), then the combine and what the pack leaves on the
+// critical path.
+double split_call_us(const mla_verify_plan* pl, int kernel, int batch, int ns, int shards) {
+  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, rows_per_unit(kernel));
+  const double waves = static_cast<double>(ceil_div(units * ns, pl->num_sms / ctas_per_unit(kernel)));
+  const double steps = static_cast<double>(ceil_div(max_steps(pl, kernel, shards), ns));
+  const bool beside = kernel != MLA_VERIFY_KERNEL_MMA && !gathers_directly(pl) &&
+                      pack_plan(pl, kernel, batch, ns, true, shards).mode == MLA_VERIFY_PACK_IDLE_SMS;
+  return waves * (fixed_us(kernel) + steps * step_us(kernel) * (beside ? kBesidePack : 1.0)) +
+         combine_us(pl, kernel, batch, ns) + pack_us(pl, kernel, batch, ns, shards);
 }
 
 // Split count for `batch` requests: minimise (waves of units) x (steps per
@@ -190,13 +213,22 @@ int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel, int shards = 1
     }
     return best;
   };
-  const int best = best_split(false);
-  // A choice that needs several waves of attention CTAs also runs the whole
-  // pack first; weigh the pack in then (one wave with the pack overlapping
-  // can win: tree, 4 x 16 row tiles x 16k keys, 278 -> 256 us).  Single-wave
-  // choices are kept: beside a running pack the attention blocks take longer
-  // than the planner's step, and weighing the pack picked worse splits there.
-  if (kernel != MLA_VERIFY_KERNEL_MMA && units * best > slots) return best_split(true);
+  if (kernel == MLA_VERIFY_KERNEL_MMA || gathers_directly(pl)) return best_split(false);
+  // Packed families: the split count whose whole call -- attention waves,
+  // combine, and the pack schedule pack_plan picks for it -- is cheapest.
+  // Fewer splits can leave enough SMs idle for the pack to run beside the
+  // attention kernel instead of ahead of it (the 93k sweep point: 15 splits
+  // and the overlapping pack, 151.8 us, against 19 and the whole pack first,
+  // 158.3 us).
+  int best = 1;
+  double best_us = 1e300;
+  for (int ns = 1; ns <= cap; ++ns) {
+    const double us = split_call_us(pl, kernel, batch, ns, shards);
+    if (us < best_us - 1e-9) {
+      best_us = us;
+      best = ns;
+    }
+  }
   return best;
 }
 
@@ -210,12 +242,7 @@ int family_nsplit(const mla_verify_plan* pl, int fam, int batch, int shards) {
 // fixed cost plus its split steps, then the combine and what the pack leaves
 // on the critical path.
 double call_estimate_us(const mla_verify_plan* pl, int fam, int batch, int shards) {
-  const int ns = family_nsplit(pl, fam, batch, shards);
-  const long long units = static_cast<long long>(batch) * ceil_div(pl->R, rows_per_unit(fam));
-  const double waves = static_cast<double>(ceil_div(units * ns, pl->num_sms / ctas_per_unit(fam)));
-  const double steps = static_cast<double>(ceil_div(max_steps(pl, fam, shards), ns));
-  return waves * (fixed_us(fam) + steps * step_us(fam)) + combine_us(pl, fam, batch, ns) +
-         pack_us(pl, fam, batch, ns, shards);
+  return split_call_us(pl, fam, batch, family_nsplit(pl, fam, batch, shards), shards);
 }
 
 // The partial kernel a call launches.  One row tile per request, or no
