@@ -148,11 +148,12 @@ double pack_us(const mla_verify_plan* pl, int fam, int batch, int nsplit, int sh
   return 2304.0 * batch * ceil_div(pl->max_kv_len, shards) / 4.5e12 * 1e6 + 3.0;
 }
 
-// Split steps run ~15 % slower beside the overlapping pack (its loads and
-// stores share L2 and HBM with the attention kernel's copies): measured on
-// the 93k sweep point, 15 splits with the pack on 32 idle SMs, 151.8 us per
-// call against 158.3 with 19 splits and the whole pack first.
-constexpr double kBesidePack = 1.155;
+// Split steps run ~7 % slower beside the overlapping pack (its loads and
+// stores share L2 and HBM with the attention kernel's copies): fitted on the
+// 93k sweep point, 15 / 16 / 17 splits with the pack on 32 / 24 / 16 idle SMs
+// at 142.6 / 145.5 / 152.4 us per call against 157.8 with 19 splits and the
+// whole pack first.
+constexpr double kBesidePack = 1.07;
 
 // Keys a request can hold in a call covering one of `shards` shards: a
 // shard takes at most ceil(nb / shards) of the request's nb 128-key blocks.
@@ -218,8 +219,8 @@ int auto_nsplit(const mla_verify_plan* pl, int batch, int kernel, int shards = 1
   // combine, and the pack schedule pack_plan picks for it -- is cheapest.
   // Fewer splits can leave enough SMs idle for the pack to run beside the
   // attention kernel instead of ahead of it (the 93k sweep point: 15 splits
-  // and the overlapping pack, 151.8 us, against 19 and the whole pack first,
-  // 158.3 us).
+  // and the overlapping pack, 142.6 us, against 19 and the whole pack first,
+  // 157.8 us).
   int best = 1;
   double best_us = 1e300;
   for (int ns = 1; ns <= cap; ++ns) {

@@ -403,8 +403,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       for (int u = 0; u < 4; ++u, ++n) {
         const int slot = n % NSLOT;
         if (slot != cw) continue;
-        if (n >= NSLOT) wait_warp(mbar(MB_EMPTY + slot), static_cast<uint32_t>((n / NSLOT - 1) & 1), s_abort, p.err);
-        if (*s_abort) break;
         // S units: the own block (the peer loads its own); O units: block
         // (i, h) in both CTAs.
         const int h = is_s ? static_cast<int>(rank) : (u & 1);
@@ -412,13 +410,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const int kb = kb0 + 2 * i + h;
         const bool mine = kb < kb1;
         const bool peers = is_s ? present(i, static_cast<int>(peer)) : mine;
+        // An overlapping pack's ready flags first: the acquire round trip
+        // then overlaps the wait for the slot instead of following it.
+        if (mine && !ensure_packed(kb)) break;
+        if (n >= NSLOT) wait_warp(mbar(MB_EMPTY + slot), static_cast<uint32_t>((n / NSLOT - 1) & 1), s_abort, p.err);
+        if (*s_abort) break;
         if (rank == 0) {
           if (lane == 0)
             tc::mbar_arrive_expect(mbar(MB_FULL + slot), (mine ? 2 * CHUNK : 0) + (peers ? 2 * CHUNK : ABSENT_BYTES));
           __syncwarp();
         }
         if (mine) {
-          if (!ensure_packed(kb)) break;
           tc::tma_load_2d_pair(sbase + OFF_RING + slot * 2 * CHUNK, &tm_pair, 0, chunk_row(kb, 2 * pair_idx),
                                even_mbar(MB_FULL + slot));
         } else if (rank == 1) {
@@ -429,16 +431,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       if (*s_abort) break;
       if (is_s && cw == NCOPY - 1) {
         // The rope chunk of the own block, once S^T(i-1) has read the last one.
-        if (i > 0) wait_warp(mbar(MB_REMPTY), static_cast<uint32_t>((i - 1) & 1), s_abort, p.err);
-        if (*s_abort) break;
         const int kb = kb0 + 2 * i + static_cast<int>(rank);
         const bool mine = kb < kb1, peers = present(i, static_cast<int>(peer));
+        if (mine && !ensure_packed(kb)) break;
+        if (i > 0) wait_warp(mbar(MB_REMPTY), static_cast<uint32_t>((i - 1) & 1), s_abort, p.err);
+        if (*s_abort) break;
         if (rank == 0) {
           if (lane == 0) tc::mbar_arrive_expect(mbar(MB_RFULL), (mine ? CHUNK : 0) + (peers ? CHUNK : ABSENT_BYTES));
           __syncwarp();
         }
         if (mine) {
-          if (!ensure_packed(kb)) break;
           tc::tma_load_2d_pair(sbase + OFF_ROPE, &tm_chunk, 0, chunk_row(kb, 8), even_mbar(MB_RFULL));
         } else if (rank == 1) {
           if (lane == 0) tc::st_async_b32(absent_word, 0, even_mbar(MB_RFULL));
