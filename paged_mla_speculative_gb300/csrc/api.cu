@@ -98,10 +98,10 @@ bool gathers_directly(const mla_verify_plan* pl) {
 // `stay` = those idle SMs keep packing while the attention kernel runs, the
 // others first pack the `wide` leading block positions of every split.
 // `wide` is the fewest positions that keep the narrow phase ahead of the
-// attention kernel, from rates measured on GB300: ~0.2 blocks/us per
-// packing SM (the staged pack of pack_kv.cu beside a running attention
-// kernel), one split step per step_us per attention unit, ~5 us before its
-// first block.  When that needs more than half the positions, or
+// attention kernel, from rates measured on GB300: ~0.23 blocks/us per
+// packing SM (the staged pack of pack_kv.cu, ~36 GB/s of rows alone on 24
+// SMs, a little less beside a running attention kernel), one split step per
+// step_us per attention unit, ~5 us before its first block.  When that needs more than half the positions, or
 // otherwise, the whole pack runs first (stay = 0).
 struct PackSchedule {
   int mode;       // MLA_VERIFY_PACK_WHOLE or _IDLE_SMS
@@ -122,7 +122,7 @@ PackSchedule pack_plan(const mla_verify_plan* pl, int fam, int batch, int nsplit
   const bool forced_idle = pl->pack_mode == MLA_VERIFY_PACK_IDLE_SMS;
   if (idle < (forced_idle ? 1 : kMinPackSms)) return whole;
   const double per_block_us = pairs ? step_us(fam) / 2 : step_us(fam), lead_us = 5.0,
-               blocks_per_us_per_sm = 0.2;
+               blocks_per_us_per_sm = 0.23;
   const double narrow_us = static_cast<double>(nsplit) * batch / (idle * blocks_per_us_per_sm);
   // Position q >= wide is ready after (q - wide + 1) narrow steps and needed
   // after lead + q attention steps; with narrow steps the slower, the last

@@ -23,13 +23,13 @@
 //    attention kernel, whose copy warp waits for it with griddepcontrol.wait.
 //  * pack_kv_overlap_kernel: when the attention grid leaves SMs idle
 //    (decode batches: 128 attention CTAs on 152 SMs), a persistent grid of
-//    one 512-thread CTA per SM, in two phases: the CTAs beyond the idle
+//    one 768-thread CTA per SM, in two phases: the CTAs beyond the idle
 //    count pack the first block positions of every split and exit -- their
 //    SMs take the attention CTAs (programmatic dependent launch) -- while
 //    the others pack the rest on the idle SMs as the attention kernel runs.
-//    Each warp packs 4-key units through three shared-memory stages (16-byte
-//    cp.async of the unit's rows, so two units' loads stay in flight while
-//    it widens and stores the third, without registers held per load) and
+//    Each warp packs 4-key units through two shared-memory stages (16-byte
+//    cp.async of the unit's rows, so one unit's loads stay in flight while
+//    it widens and stores the other, without registers held per load) and
 //    publishes every unit with a release store of this call's tag (epoch +
 //    1) into pack_sync, 32 flags per block, which the attention kernel's
 //    copy warp waits for block by block.  Units run in split-position order
@@ -120,14 +120,15 @@ constexpr int PER_LANE = ROW_CHUNKS / 8;            // 9 granules per lane (8 la
 static_assert(UNIT_KEYS * 8 == 32 && PER_LANE * 8 == ROW_CHUNKS, "8 lanes per key");
 static_assert(UNITS_PER_BLOCK == 32, "one flag per lane of the reader's warp");
 
-// pack_kv_overlap_kernel: warps per CTA and units staged per warp.  Sixteen
-// warps of three stages fill shared memory; measured on GB300 (the narrow
-// phase alone, 93k scattered keys): ~31 GB/s of rows read per SM, against
-// ~23 with the units held in registers.  Fewer warps with deeper stages were
-// slower: every unit's publication waits for the warp's outstanding memory
-// operations, so the parallel warps, not the depth, carry the throughput.
-constexpr int OV_WARPS = 16;
-constexpr int OV_DEPTH = 3;
+// pack_kv_overlap_kernel: warps per CTA and units staged per warp.  24
+// warps of two stages fill shared memory; measured on GB300 (the narrow phase
+// alone, 93k scattered keys, 24 SMs): ~36 GB/s of rows read per SM, against
+// ~32 with 16 warps of three stages, ~29 with 12 of four, ~23 with 8 of six,
+// and ~23 with the units held in registers.  Every unit's publication waits
+// for the warp's outstanding memory operations, so the parallel warps, not
+// the depth, carry the throughput.
+constexpr int OV_WARPS = 24;
+constexpr int OV_DEPTH = 2;
 constexpr int UNIT_BYTES = UNIT_KEYS * ROW_BYTES;   // 4608: a unit's rows as they are in the cache
 constexpr int OV_SMEM = OV_WARPS * OV_DEPTH * UNIT_BYTES;
 
@@ -186,8 +187,8 @@ __device__ __forceinline__ void stage_unit(const Params& p, uint32_t stage, int 
 }
 
 // Pack this warp's units u, u + stride, .. below `end` through its
-// OV_DEPTH stages: unit k lands in stage k % OV_DEPTH while units k+1 and
-// k+2 are in flight; each lane widens and stores exactly the granules it
+// OV_DEPTH stages: unit k lands in stage k % OV_DEPTH while the next
+// OV_DEPTH - 1 units are in flight; each lane widens and stores exactly the granules it
 // copied (its own cp.async data, visible to it after the group wait), into
 // chunk i of key j at the swizzled granule, then the warp publishes the unit.
 __device__ __forceinline__ void pack_units(const Params& p, uint8_t* packed, int max_blocks, int u, int end,
