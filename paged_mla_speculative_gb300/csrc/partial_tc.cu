@@ -700,12 +700,14 @@ __global__ void __launch_bounds__(kDirect ? NTHREADS : NTHREADS - 32, 1) partial
   if (*s_abort != 0) {
     write_nan_rows(p, b, split, row0, tid);
   } else {
-    const int nrows = min(BM, p.R - row0);
     const bool out16 = p.nsplit == 1 && p.out_bf16;
-    uint8_t* stage = smem + OFF_KV;            // [64 rows][512 dims] fp32 or bf16
+    const size_t ws_row = ws_base(p, b, split);
     if (warp < SOFTMAX_WARPS) {
       // Softmax warp (quad, half): the half's 32 rows of every O^T tile, two
-      // tiles per TMEM wait, the row reciprocals four at a time.
+      // tiles per TMEM wait, thread = value dim, stored straight from
+      // registers: each warp store covers 32 consecutive dims of one row (128
+      // contiguous bytes of fp32).  Staging the tile in shared memory for
+      // bulk row stores measured ~3 us slower per CTA in the pair kernel.
       const int h = warp >> 2;
 #pragma unroll 1
       for (int d = 0; d < 4; d += 2) {
@@ -718,40 +720,29 @@ __global__ void __launch_bounds__(kDirect ? NTHREADS : NTHREADS - 32, 1) partial
         }
         const int dim0 = d * 128 + quad * 32 + lane, dim1 = dim0 + 128;
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 inv4 = *reinterpret_cast<const float4*>(s_l + h * 32 + c);
-          const float inv[4] = {inv4.x, inv4.y, inv4.z, inv4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int r = h * 32 + c + e;
-            const bool ok = inv[e] > 0.f && nb > 0;
-            const float o0 = ok ? __uint_as_float(v0[c + e]) * inv[e] : 0.f;
-            const float o1 = ok ? __uint_as_float(v1[c + e]) * inv[e] : 0.f;
+        for (int c = 0; c < 32; ++c) {
+          const int r = h * 32 + c, gr = row0 + r;
+          if (gr >= p.R) continue;   // rows past R (warp-uniform)
+          const float inv = s_l[r];
+          const bool ok = inv > 0.f && nb > 0;
+          const float o0 = ok ? __uint_as_float(v0[c]) * inv : 0.f;
+          const float o1 = ok ? __uint_as_float(v1[c]) * inv : 0.f;
+          if (p.nsplit > 1) {
+            float* dst = p.ws_o + (ws_row + gr) * D_V;
+            dst[dim0] = o0;
+            dst[dim1] = o1;
+          } else {
+            const size_t e = (static_cast<size_t>(b) * p.R + gr) * D_V;
             if (out16) {
-              reinterpret_cast<__nv_bfloat16*>(stage)[r * D_V + dim0] = __float2bfloat16_rn(o0);
-              reinterpret_cast<__nv_bfloat16*>(stage)[r * D_V + dim1] = __float2bfloat16_rn(o1);
+              reinterpret_cast<__nv_bfloat16*>(p.out)[e + dim0] = __float2bfloat16_rn(o0);
+              reinterpret_cast<__nv_bfloat16*>(p.out)[e + dim1] = __float2bfloat16_rn(o1);
             } else {
-              reinterpret_cast<float*>(stage)[r * D_V + dim0] = o0;
-              reinterpret_cast<float*>(stage)[r * D_V + dim1] = o1;
+              reinterpret_cast<float*>(p.out)[e + dim0] = o0;
+              reinterpret_cast<float*>(p.out)[e + dim1] = o1;
             }
           }
         }
       }
-      tc::fence_async_smem();
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t row_bytes = out16 ? D_V * 2 : D_V * 4;
-      for (int r = lane; r < nrows; r += 32) {
-        const size_t grow = static_cast<size_t>(b) * p.R + row0 + r;
-        void* dst = p.nsplit == 1
-                        ? static_cast<void*>(static_cast<uint8_t*>(p.out) + grow * row_bytes)
-                        : static_cast<void*>(p.ws_o + (ws_base(p, b, split) + row0 + r) * D_V);
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
-                     "r"(sbase + OFF_KV + r * row_bytes), "r"(row_bytes)
-                     : "memory");
-      }
-      asm volatile("cp.async.bulk.commit_group;\ncp.async.bulk.wait_group 0;\n" ::: "memory");
     }
   }
   tc::fence_before_sync();
