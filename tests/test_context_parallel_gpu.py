@@ -144,3 +144,50 @@ def test_bad_shard_arguments_are_rejected():
             mb.mla_verify_combine_parts(plan, big, bigl)
         mb.mla_verify_combine_parts(plan, po.zero_(), pl.fill_(0.0))
         torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 5, 8, 9, 16, 17, 25, 32])
+def test_combine_parts_every_count_against_the_merge(S, out_dtype):
+    """The combine on synthetic partials, for part counts across every launch
+    shape of the combine kernel (1-2, 3-4, 5-8 and 9-16 parts in one round
+    trip; 17-32 in two), against the oracle's fp64 LSE merge (the reduce step
+    of "The Decisive A/B ...", section "The Context").  About a quarter of
+    the (part, row) entries have no visible key: lse -inf and rows of NaN,
+    which must carry weight 0 and never be read into the result.  One row
+    has every part empty (lse -inf, out 0) and one row has a NaN lse in one
+    part (the row becomes NaN)."""
+    B, T, H = 2, 4, 16
+    g = torch.Generator().manual_seed(1700 + S)
+    po = torch.randn((S, B, T, H, 512), generator=g) * 4.0
+    pl = torch.randn((S, B, T, H), generator=g) * 3.0 + 5.0
+    empty = torch.rand((S, B, T, H), generator=g) < 0.25
+    empty[:, 0, 0, 0] = True                      # a row with no visible key in any part
+    pl[empty] = float("-inf")
+    clean = po.clone()
+    clean[empty] = 0.0
+    po[empty] = float("nan")                      # never to be read
+    nan_part = S // 2
+    empty[nan_part, 1, 1, 1] = False
+    pl[nan_part, 1, 1, 1] = float("nan")
+    ref_o, ref_l = oracle.lse_merge(clean.numpy(), pl.numpy())
+
+    w = W.Workload(name="cpm", batch=B, num_drafts=T, num_heads=H, prefix=(64, 64), tree="chain",
+                   num_slots=1024, seed=1700)
+    inp = G.to_cuda(W.make_inputs(w))
+    with G.make_plan(inp, out_dtype=out_dtype) as plan:
+        out, lse = mb.mla_verify_combine_parts(plan, po.cuda(), pl.cuda())
+        torch.cuda.synchronize()
+        assert plan.get_error() == 0
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64)
+    assert np.isnan(l[1, 1, 1]) and np.isnan(o[1, 1, 1]).all(), "a NaN part makes its row NaN"
+    keep = np.ones((B, T, H), dtype=bool)
+    keep[1, 1, 1] = False
+    assert np.isneginf(l[0, 0, 0]) and (o[0, 0, 0] == 0).all(), "a row with no visible key"
+    assert np.isfinite(o[keep]).all() and (np.isneginf(l[keep]) == np.isneginf(ref_l[keep])).all()
+    fin = keep & np.isfinite(ref_l)
+    assert np.abs(l[fin] - ref_l[fin]).max() <= 1e-4
+    # fp32: the merge's own rounding; bf16: one rounding of the result on top.
+    bound = 1e-4 if out_dtype == torch.float32 else 2.0 ** -8 * np.abs(ref_o[keep]).max() + 1e-4
+    assert np.abs(o[keep] - ref_o[keep]).max() <= bound
