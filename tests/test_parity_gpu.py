@@ -61,6 +61,26 @@ def test_kernel_families_small_ragged(kernel, nsplit):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("ps", [1, 64])
+def test_thirty_two_drafts_deep_random_tree(kernel, ps):
+    """The largest draft count (32: every bit of the ancestor words) on a
+    random tree up to 12 deep, 8 heads (R = 256: two pair tiles, four
+    single-SM tiles), ragged prefixes with an empty one, both page sizes."""
+    w = small(batch=3, num_drafts=32, num_heads=8, prefix=(650, 37, 0), tree="random", max_depth=12,
+              page_size=ps, seed=1800 + ps)
+    check_full(W.make_inputs(w), kernel=kernel)
+
+
+@pytest.mark.parametrize("nsplit", [1, 2, 4])
+@pytest.mark.parametrize("ps", [1, 64])
+def test_fifteen_rows_direct_gather(nsplit, ps):
+    """T·H = 15 (3 drafts x 5 heads): one partial 64-row tile, whose CTAs
+    gather their own key rows (no pack); rows 15..63 of the tile are idle."""
+    w = small(batch=2, num_drafts=3, num_heads=5, prefix=(520, 200), page_size=ps, seed=1820 + nsplit)
+    check_full(W.make_inputs(w), nsplit=nsplit)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_kernel_families_spiky_long(kernel):
     """Spiky keys (1% x8) over a few thousand keys: the precision case."""
     w = small(batch=2, prefix=(3000, 2500), num_drafts=8, num_heads=64, tree="chain",
