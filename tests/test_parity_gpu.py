@@ -71,6 +71,17 @@ def test_thirty_two_drafts_deep_random_tree(kernel, ps):
     check_full(W.make_inputs(w), kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("scale", [0.5, 1e-3], ids=["peaked", "flat"])
+def test_softmax_scale_extremes(kernel, scale):
+    """A large scale (0.5: a few keys carry nearly all the weight, so the
+    running max moves often) and a tiny one (1e-3: near-uniform weights over
+    every key, so the sums run long), against the oracle at the same scale."""
+    w = small(batch=2, num_drafts=8, num_heads=16, prefix=(3000, 700), tree="random", scale=scale,
+              seed=1830 if scale > 0.1 else 1831)
+    check_full(W.make_inputs(w), kernel=kernel, nsplit=3)
+
+
 @pytest.mark.parametrize("nsplit", [1, 2, 4])
 @pytest.mark.parametrize("ps", [1, 64])
 def test_fifteen_rows_direct_gather(nsplit, ps):
