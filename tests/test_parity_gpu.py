@@ -71,6 +71,30 @@ def test_thirty_two_drafts_deep_random_tree(kernel, ps):
     check_full(W.make_inputs(w), kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel,ps", [
+    pytest.param(mb.KERNEL_AUTO, 1, id="auto-ps1"), pytest.param(mb.KERNEL_AUTO, 64, id="auto-ps64"),
+    pytest.param(mb.KERNEL_PAIR, 1, id="pair-ps1"), pytest.param(mb.KERNEL_TC, 1, id="tc-ps1"),
+    pytest.param(mb.KERNEL_MMA, 1, id="mma-ps1")])
+def test_one_plan_serves_smaller_batches(kernel, ps):
+    """A plan sized for 6 requests serves calls of 6, 2, 5 and 1 requests in
+    a row, each with its own inputs: the split count, the pack's layout and
+    its epoch tags (counted over each call's grid) follow each call's batch."""
+    T, H, slots = 8, 16, 8192
+    shapes = [(900, 40, 0, 1300, 257, 64), (1500, 3), (100, 700, 1200, 9, 0), (2000,)]
+    inputs = [W.make_inputs(W.Workload(name=f"mb{i}", batch=len(pre), num_drafts=T, num_heads=H, prefix=pre,
+                                       tree="random", num_slots=slots, page_size=ps, spike_frac=0.01,
+                                       seed=1900 + 10 * i + ps))
+              for i, pre in enumerate(shapes)]
+    max_kv = max(int(x.kv_lens.max()) for x in inputs)
+    with mb.Plan(6, T, H, ps, slots, max_kv) as plan:
+        plan.set_kernel(kernel)
+        for inp in inputs:
+            out, lse = G.run(plan, G.to_cuda(inp))
+            assert plan.get_error() == 0
+            ref_o, ref_l = G.oracle_full(inp)
+            G.assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("scale", [0.5, 1e-3], ids=["peaked", "flat"])
 def test_softmax_scale_extremes(kernel, scale):
