@@ -217,11 +217,17 @@ int mla_verify_plan_set_profile_events(mla_verify_plan* plan, void* after_pack,
  * attention kernel waiting for per-block ready flags but not the pack kernel
  * that sets them, so every block wait runs out after its cycle limit (about
  * a second): the rows come out NaN, the device status word gets
- * MLA_VERIFY_DEV_TIMEOUT and the context stays usable.  MLA_VERIFY_OK, or
- * MLA_VERIFY_ERR_ARG for an unknown fault.
+ * MLA_VERIFY_DEV_TIMEOUT and the context stays usable.
+ * MLA_VERIFY_FAULT_EPOCH_NEAR_WRAP (a call that packs its keys): before the
+ * call, the pack hand-off epoch is set to 2^32 - 3, so the calls from there
+ * on use the tags 2^32 - 2, 2^32 - 1, 2^32, .. (the epoch and the tags are
+ * 64-bit: they do not wrap); every result must stay exact.  The value is
+ * written by a pageable host copy: not for a call under stream capture.
+ * MLA_VERIFY_OK, or MLA_VERIFY_ERR_ARG for an unknown fault.
  */
 #define MLA_VERIFY_FAULT_NONE         0
 #define MLA_VERIFY_FAULT_SKIP_PACK    1
+#define MLA_VERIFY_FAULT_EPOCH_NEAR_WRAP 2
 int mla_verify_plan_inject_fault(mla_verify_plan* plan, int fault);
 
 /* Bytes of device workspace the plan holds (partials, packed key blocks,

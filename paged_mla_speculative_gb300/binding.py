@@ -29,6 +29,7 @@ PACK_IDLE_SMS = 2
 PACK_NONE = 4
 FAULT_NONE = 0
 FAULT_SKIP_PACK = 1
+FAULT_EPOCH_NEAR_WRAP = 2
 MAX_NSPLIT = 32
 
 DEV_BAD_SLOT = 1

@@ -398,7 +398,8 @@ int mla_verify_plan_create(mla_verify_plan** out, int max_batch, int num_drafts,
   ok = ok && cudaMalloc(&pl->packed, packed_bytes) == cudaSuccess;
   ok = ok && mlav::make_pack_maps(&pl->pack_maps, pl->packed, packed_bytes) == cudaSuccess;
   const size_t sync_bytes =
-      (mlav::PACK_SYNC_HEADER + static_cast<size_t>(max_batch) * pl->pack_blocks * 32) * sizeof(unsigned);
+      mlav::PACK_SYNC_HEADER * sizeof(unsigned) +
+      static_cast<size_t>(max_batch) * pl->pack_blocks * 32 * sizeof(unsigned long long);
   ok = ok && cudaMalloc(&pl->pack_sync, sync_bytes) == cudaSuccess;
   pl->pack_sync_bytes = sync_bytes;
   if (!ok) {
@@ -480,7 +481,9 @@ int mla_verify_plan_get_pack_mode(const mla_verify_plan* pl, int batch) {
 
 int mla_verify_plan_inject_fault(mla_verify_plan* pl, int fault) {
   if (!pl) return MLA_VERIFY_ERR_NULL;
-  if (fault != MLA_VERIFY_FAULT_NONE && fault != MLA_VERIFY_FAULT_SKIP_PACK) return MLA_VERIFY_ERR_ARG;
+  if (fault != MLA_VERIFY_FAULT_NONE && fault != MLA_VERIFY_FAULT_SKIP_PACK &&
+      fault != MLA_VERIFY_FAULT_EPOCH_NEAR_WRAP)
+    return MLA_VERIFY_ERR_ARG;
   pl->fault = fault;
   return MLA_VERIFY_OK;
 }
@@ -577,11 +580,18 @@ int launch_call(mla_verify_plan* pl, int batch, const void* q, const void* kv_ca
   const bool overlap = !pl->ev_after_pack && !pl->ev_after_partial;
   cudaError_t le = cudaSuccess;
   if (packs && pl->pack_flags_dirty) {
-    // Zero the flags, keep the epoch and the (reset) ticket: no tag is 0.
+    // Zero the flags and the ticket, keep the epoch: no tag is 0.
     const size_t head = mlav::PACK_SYNC_HEADER * sizeof(unsigned);
     le = cudaMemsetAsync(reinterpret_cast<uint8_t*>(pl->pack_sync) + head, 0, pl->pack_sync_bytes - head, s);
-    if (le == cudaSuccess) le = cudaMemsetAsync(pl->pack_sync + 1, 0, sizeof(unsigned), s);
+    if (le == cudaSuccess) le = cudaMemsetAsync(pl->pack_sync + mlav::PACK_SYNC_TICKET, 0, sizeof(unsigned), s);
     if (le == cudaSuccess) pl->pack_flags_dirty = false;
+  }
+  if (le == cudaSuccess && packs && pl->fault == MLA_VERIFY_FAULT_EPOCH_NEAR_WRAP) {
+    // Testing: the tags of this call and the next cross 2^32, where 32-bit
+    // tags would wrap (a pageable copy: the value is staged before
+    // cudaMemcpyAsync returns).
+    const unsigned long long near_wrap = 0xfffffffdull;
+    le = cudaMemcpyAsync(pl->pack_sync, &near_wrap, sizeof(near_wrap), cudaMemcpyHostToDevice, s);
   }
   const bool skip_pack = pl->fault == MLA_VERIFY_FAULT_SKIP_PACK;
   pl->fault = MLA_VERIFY_FAULT_NONE;

@@ -64,14 +64,26 @@ struct Params {
   // Workspace row of split s of request b, query row r:
   // b * ws_stride_b + s * ws_stride_s + r (rows of 512 floats / one lse).
   long long ws_stride_b, ws_stride_s;
-  // Hand-off between the pack and the attention kernel of one call:
-  // [0] epoch (calls completed), [1] ticket (attention CTAs done this call),
-  // [4 + 32 * (b * packed_max_blocks + kb) + g] = epoch + 1 once keys
-  // 4g .. 4g+3 of block kb of request b are packed in this call.
+  // Hand-off between the pack and the attention kernel of one call, 32-bit
+  // words: [0..1] epoch (64-bit: calls completed), [2] ticket (attention
+  // CTAs done this call), then 64-bit flags from word PACK_SYNC_HEADER on:
+  // flag 32 * (b * packed_max_blocks + kb) + g = epoch + 1 once keys
+  // 4g .. 4g+3 of block kb of request b are packed in this call.  64-bit
+  // tags never repeat in practice: with 32-bit ones, a flag left by a call
+  // 2^32 calls earlier (a block position nothing packed since) would pass
+  // for this call's after the wrap.
   unsigned* pack_sync;
 };
 
-constexpr int PACK_SYNC_HEADER = 4;   // words before the per-quarter flags
+constexpr int PACK_SYNC_HEADER = 4;   // 32-bit words before the flags (16 bytes)
+constexpr int PACK_SYNC_TICKET = 2;   // word of the ticket
+
+__device__ __forceinline__ unsigned long long pack_epoch(const unsigned* pack_sync) {
+  return *reinterpret_cast<const volatile unsigned long long*>(pack_sync);
+}
+__device__ __forceinline__ unsigned long long* pack_flags(unsigned* pack_sync) {
+  return reinterpret_cast<unsigned long long*>(pack_sync + PACK_SYNC_HEADER);
+}
 
 // Per-request facts every CTA of the request derives the same way.
 struct Request {

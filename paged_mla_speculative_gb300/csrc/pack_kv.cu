@@ -192,7 +192,7 @@ __device__ __forceinline__ void stage_unit(const Params& p, uint32_t stage, int 
 // copied (its own cp.async data, visible to it after the group wait), into
 // chunk i of key j at the swizzled granule, then the warp publishes the unit.
 __device__ __forceinline__ void pack_units(const Params& p, uint8_t* packed, int max_blocks, int u, int end,
-                                           int stride, int lane, unsigned tag, uint32_t stages) {
+                                           int stride, int lane, unsigned long long tag, uint32_t stages) {
   if (u >= end) return;
   bool bad = false;
   const uint64_t pol = evict_first_policy();
@@ -244,9 +244,9 @@ __device__ __forceinline__ void pack_units(const Params& p, uint8_t* packed, int
     asm volatile("fence.proxy.async.global;\n" ::: "memory");
     __syncwarp();
     if (lane == 0) {
-      unsigned* flag = p.pack_sync + PACK_SYNC_HEADER + UNITS_PER_BLOCK * static_cast<size_t>(cblk) +
+      unsigned long long* flag = pack_flags(p.pack_sync) + UNITS_PER_BLOCK * static_cast<size_t>(cblk) +
                        (u & (UNITS_PER_BLOCK - 1));
-      asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(flag), "r"(tag) : "memory");
+      asm volatile("st.release.gpu.global.u64 [%0], %1;\n" ::"l"(flag), "l"(tag) : "memory");
     }
   }
   asm volatile("cp.async.wait_all;\n" ::: "memory");
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(OV_WARPS * 32, 1)
   const int nq = p.nsplit * p.batch * per_split;     // blocks in the pack order
   const int units = UNITS_PER_BLOCK * nq;            // < 2^31 (host check)
   const int wide_end = min(wide_units, units);
-  const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
+  const unsigned long long tag = pack_epoch(p.pack_sync) + 1ull;
   const int n = gridDim.x - stay;     // CTAs of the wide phase: warp w of CTA c takes units
   const bool wide = cta >= stay;      // w * n + c, w * n + c + 16 n, ..
   const int first = wide ? warp * n + (cta - stay) : wide_end + cta * OV_WARPS + warp;

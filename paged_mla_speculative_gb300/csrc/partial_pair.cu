@@ -161,15 +161,15 @@ __device__ __forceinline__ void wait_drain(uint32_t mbar, uint32_t parity, int* 
 
 // Same as partial_tc.cu: wait (bounded) for the 32 ready flags of packed
 // block kb of request b carrying this call's tag.  Whole warp.
-__device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsigned tag,
+__device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsigned long long tag,
                                             volatile int* abort, int* err) {
   const int lane = threadIdx.x & 31;
-  const unsigned* flag = p.pack_sync + PACK_SYNC_HEADER +
-                         32 * (static_cast<size_t>(b) * p.packed_max_blocks + kb) + lane;
+  const unsigned long long* flag =
+      pack_flags(p.pack_sync) + 32 * (static_cast<size_t>(b) * p.packed_max_blocks + kb) + lane;
   const long long t0 = clock64();
   while (true) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(flag) : "memory");
     if (__all_sync(0xffffffffu, v == tag)) break;
     if (__any_sync(0xffffffffu, *abort != 0)) return false;
     if (__any_sync(0xffffffffu, clock64() - t0 > WAIT_LIMIT)) {
@@ -188,10 +188,9 @@ __device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsi
 __device__ __forceinline__ void finish_call(const Params& p) {
   __threadfence();
   const unsigned total = gridDim.x * gridDim.y * gridDim.z;
-  if (atomicAdd(p.pack_sync + 1, 1u) == total - 1) {
-    p.pack_sync[1] = 0;
-    const unsigned e = *reinterpret_cast<volatile unsigned*>(p.pack_sync);
-    *reinterpret_cast<volatile unsigned*>(p.pack_sync) = e + 1u == 0xffffffffu ? 0u : e + 1u;
+  if (atomicAdd(p.pack_sync + PACK_SYNC_TICKET, 1u) == total - 1) {
+    p.pack_sync[PACK_SYNC_TICKET] = 0;
+    *reinterpret_cast<volatile unsigned long long*>(p.pack_sync) = pack_epoch(p.pack_sync) + 1ull;
   }
 }
 
@@ -383,7 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     auto chunk_row = [&](int kb, int c) {
       return ((b * p.packed_max_blocks + kb) * 9 + c) * BN;
     };
-    const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
+    const unsigned long long tag = pack_epoch(p.pack_sync) + 1ull;
     if (!p.pack_flags) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     int waited = kb0 - 1;   // highest block whose pack flags were seen
     auto ensure_packed = [&](int kb) {

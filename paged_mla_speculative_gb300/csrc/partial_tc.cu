@@ -159,15 +159,15 @@ __device__ __forceinline__ int block_slot(const Params& p, const Request& rq, in
 // Wait (bounded) until the pack kernel has published all 32 four-key units
 // of block kb of request b for this call: lane l watches unit l's flag with
 // acquire loads.  Whole warp; false on a timeout or an earlier abort.
-__device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsigned tag,
+__device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsigned long long tag,
                                             volatile int* abort, int* err) {
   const int lane = threadIdx.x & 31;
-  const unsigned* flag = p.pack_sync + PACK_SYNC_HEADER +
-                         32 * (static_cast<size_t>(b) * p.packed_max_blocks + kb) + lane;
+  const unsigned long long* flag =
+      pack_flags(p.pack_sync) + 32 * (static_cast<size_t>(b) * p.packed_max_blocks + kb) + lane;
   const long long t0 = clock64();
   while (true) {   // every exit decision is warp-uniform
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(flag) : "memory");
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(flag) : "memory");
     if (__all_sync(0xffffffffu, v == tag)) break;
     if (__any_sync(0xffffffffu, *abort != 0)) return false;
     if (__any_sync(0xffffffffu, clock64() - t0 > WAIT_LIMIT)) {
@@ -187,15 +187,15 @@ __device__ __forceinline__ bool wait_packed(const Params& p, int b, int kb, unsi
 
 // Every CTA takes one ticket when it is done; the last one of the grid
 // advances the epoch, so the next call's pack kernel publishes a new tag.
-// The epoch stays below 2^32 - 1, so the tag (epoch + 1) is never 0 -- the
-// value of a flag no call has written -- and consecutive tags differ.
+// The 64-bit tag (epoch + 1) is never 0 -- the value of a flag no call has
+// written -- and never repeats, so no flag left by an earlier call passes
+// for this call's.
 __device__ __forceinline__ void finish_call(const Params& p) {
   __threadfence();
   const unsigned total = gridDim.x * gridDim.y * gridDim.z;
-  if (atomicAdd(p.pack_sync + 1, 1u) == total - 1) {
-    p.pack_sync[1] = 0;
-    const unsigned e = *reinterpret_cast<volatile unsigned*>(p.pack_sync);
-    *reinterpret_cast<volatile unsigned*>(p.pack_sync) = e + 1u == 0xffffffffu ? 0u : e + 1u;
+  if (atomicAdd(p.pack_sync + PACK_SYNC_TICKET, 1u) == total - 1) {
+    p.pack_sync[PACK_SYNC_TICKET] = 0;
+    *reinterpret_cast<volatile unsigned long long*>(p.pack_sync) = pack_epoch(p.pack_sync) + 1ull;
   }
 }
 
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kDirect ? NTHREADS : NTHREADS - 32, 1) partial
     // the stream, which may still be running: with per-unit flags each block
     // is read once its 32 units carry this call's tag, else after the whole
     // pack grid (a no-op when launched without overlap).
-    const unsigned tag = *reinterpret_cast<volatile unsigned*>(p.pack_sync) + 1u;
+    const unsigned long long tag = pack_epoch(p.pack_sync) + 1ull;
     if (!p.pack_flags) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     int issued = 0;   // copies issued, in (block, g) order
 #pragma unroll 1

@@ -127,6 +127,46 @@ def test_overlapping_pack_new_data_each_call(kernel):
     plan.close()
 
 
+@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_PAIR, id="pair")])
+def test_hand_off_tags_past_2_32(kernel):
+    """The pack's ready flags carry 64-bit tags.  A first call packs long
+    requests (its flags hold tag 1); the epoch is then moved to 2^32 - 3
+    (MLA_VERIFY_FAULT_EPOCH_NEAR_WRAP), short calls take the tags across
+    2^32, and long calls with new data follow.  With 32-bit tags the epoch
+    would wrap and a later call would reuse tag 1, finding the first call's
+    flags on blocks it has not packed yet."""
+    def make(pre, seed):
+        return W.make_inputs(W.Workload(name="tag", batch=3, num_drafts=4, num_heads=32, prefix=pre,
+                                        tree="random", num_slots=8192, spike_frac=0.01, seed=seed))
+    long_a, long_b = make((1800, 1900, 1500), 640), make((1700, 1890, 1600), 641)
+    short = make((64, 100, 33), 642)
+    dev = torch.device("cuda")
+    q = torch.empty_like(long_a.q, device=dev)
+    cache = torch.empty_like(long_a.kv_cache, device=dev)
+    idx = torch.zeros(max(c.kv_indices.numel() for c in (long_a, long_b, short)), dtype=torch.int32, device=dev)
+    indptr = torch.empty(4, dtype=torch.int32, device=dev)
+    lens = torch.empty(3, dtype=torch.int32, device=dev)
+    par = torch.empty((3, 4), dtype=torch.int32, device=dev)
+    with mb.Plan(3, 4, 32, 1, 8192, 1904) as plan:
+        plan.set_kernel(kernel)
+        plan.set_nsplit(2)
+        plan.set_pack_schedule(mb.PACK_IDLE_SMS)
+        for i, c in enumerate([long_a, short, short, long_b, long_a, long_b]):
+            if i == 1:
+                plan.inject_fault(mb.FAULT_EPOCH_NEAR_WRAP)
+            q.copy_(c.q)
+            cache.copy_(c.kv_cache)
+            idx[:c.kv_indices.numel()].copy_(c.kv_indices)
+            indptr.copy_(c.kv_indptr)
+            lens.copy_(c.kv_lens)
+            par.copy_(c.draft_parent)
+            out, lse = mb.mla_verify_attn(plan, q, cache, idx, indptr, lens, par, c.scale)
+            torch.cuda.synchronize()
+            ref_o, ref_l = G.oracle_full(c)
+            G.assert_parity(out.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l)
+        assert plan.get_error() == 0
+
+
 def test_whole_pack_when_no_sm_is_idle():
     """As many attention CTAs as SMs: the whole pack runs first."""
     tiles = 8                                   # 512 rows
