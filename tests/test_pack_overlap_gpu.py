@@ -167,6 +167,44 @@ def test_hand_off_tags_past_2_32(kernel):
         assert plan.get_error() == 0
 
 
+@pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_TC, id="tc"), pytest.param(mb.KERNEL_PAIR, id="pair")])
+def test_two_plans_on_two_streams_at_once(kernel):
+    """Two plans, each with its own pack hand-off, issue calls on two streams
+    with no synchronisation between them, so their pack and attention kernels
+    share the GPU.  A call's attention kernel becomes launchable only once
+    every CTA of its own pack kernel has started (each triggers the dependent
+    launch at its entry), so its flag waits never depend on CTAs that cannot
+    get an SM.  Every output must be the oracle's."""
+    cases = [W.make_inputs(W.Workload(name=f"two{i}", batch=2, num_drafts=8, num_heads=32, prefix=pre,
+                                      tree="random", num_slots=16384, spike_frac=0.01, seed=660 + i))
+             for i, pre in enumerate([(3000, 2100), (2600, 3100)])]
+    gpu = [G.to_cuda(c) for c in cases]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    plans = []
+    for c in cases:
+        pl = mb.Plan(2, 8, 32, 1, 16384, max(int(x) for x in c.kv_lens))
+        pl.set_kernel(kernel)
+        pl.set_nsplit(3)
+        pl.set_pack_schedule(mb.PACK_IDLE_SMS)
+        plans.append(pl)
+    torch.cuda.synchronize()
+    results = []
+    for rep in range(4):
+        for i in (0, 1):
+            g = gpu[i]
+            with torch.cuda.stream(streams[i]):
+                out, lse = mb.mla_verify_attn(plans[i], g.q, g.kv_cache, g.kv_indices, g.kv_indptr, g.kv_lens,
+                                              g.draft_parent, g.scale, stream=streams[i])
+            results.append((i, out, lse))
+    torch.cuda.synchronize()
+    refs = [G.oracle_full(c) for c in cases]
+    for i, out, lse in results:
+        G.assert_parity(out.cpu().numpy(), lse.cpu().numpy(), refs[i][0], refs[i][1])
+    for pl in plans:
+        assert pl.get_error() == 0
+        pl.close()
+
+
 def test_whole_pack_when_no_sm_is_idle():
     """As many attention CTAs as SMs: the whole pack runs first."""
     tiles = 8                                   # 512 rows
