@@ -164,6 +164,32 @@ def test_host_entry_point_matches_device_entry_point(memory, out_dtype):
         assert plan.get_error() == 0
 
 
+@pytest.mark.parametrize("memory", ["pinned", "pageable"])
+def test_host_entry_on_smaller_batches(memory):
+    """The host-buffer entry on a plan sized for 5 requests, called with 2,
+    then 5, then 1 requests, each with its own inputs: the staged copies,
+    the index count taken from kv_indptr[batch] and the results (stored
+    straight into mapped host buffers when the call ends in the combine)
+    follow each call's batch.  Each result against the oracle."""
+    shapes = [(700, 90), (300, 1200, 0, 64, 900), (1500,)]
+    cases = [W.make_inputs(W.Workload(name=f"hb{i}", batch=len(pre), num_drafts=4, num_heads=16, prefix=pre,
+                                      tree="random", num_slots=4096, spike_frac=0.01, seed=1950 + i))
+             for i, pre in enumerate(shapes)]
+    pin = (lambda t: t.pin_memory()) if memory == "pinned" else (lambda t: t)
+    max_kv = max(int(c.kv_lens.max()) for c in cases)
+    with mb.Plan(5, 4, 16, 1, 4096, max_kv) as plan:
+        for c in cases:
+            B = c.q.shape[0]
+            cache = c.kv_cache.cuda()
+            out = pin(torch.full((B, 4, 16, 512), float("nan")))
+            lse = pin(torch.full((B, 4, 16), float("nan")))
+            mb.mla_verify_attn_host(plan, pin(c.q), cache, pin(c.kv_indices), pin(c.kv_indptr), pin(c.kv_lens),
+                                    pin(c.draft_parent), c.scale, out, lse)
+            ref_o, ref_l = G.oracle_full(c)
+            G.assert_parity(out.numpy(), lse.numpy(), ref_o, ref_l)
+        assert plan.get_error() == 0
+
+
 @pytest.mark.parametrize("kernel", [pytest.param(mb.KERNEL_PAIR, id="pair"), pytest.param(mb.KERNEL_TC, id="tc")])
 @pytest.mark.parametrize("nsplit", [1, 2])
 def test_bounded_wait_runs_out_and_reports_timeout(nsplit, kernel):
